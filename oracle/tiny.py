@@ -1,0 +1,188 @@
+"""Pure-Python model of one HiSparse cache unit -- TEST INFRASTRUCTURE ONLY.
+
+A *unit* is one (request, layer) pair.  Units are independent: each keeps its
+own slots, LRU order and page table ([P1] §3.3, last paragraph: cross-layer
+coordination was dropped, every layer manages its own cache).
+
+State of a unit ([P1] §3.2 and §5.2):
+  * ``B`` LRU slots (the hot buffer), plus one extra row with index ``B`` that
+    holds the newest token and never takes part in the LRU ([P1] §5.2,
+    "newest_slot = HOT_BUFFER_SIZE").
+  * ``slot_pos[s]``: the logical position stored in slot ``s`` (-1 = empty).
+  * ``lru``: a list of the ``B`` slot ids, oldest first.
+  * ``page_table``: ``dict`` logical position -> slot; an absent key means the
+    record lives only on the host.
+  * ``hot``: the bytes of each slot (only when a host pool is attached).
+
+``resolve`` follows the five stages of the fused kernel ([P1] §3.5) in their
+plainest sequential form, with the replacement rule of [P1] §3.3 ("hits of
+this step rank as more recent than this step's new misses") and these
+readings of points the pages leave open:
+  R1  hits of one step are ordered by ascending slot id (the lowest slot is
+      evicted first among them);
+  R2  misses take victims in selection-list order: the j-th miss takes the
+      j-th oldest evictable slot, and among the new fetches an earlier list
+      index ends up older;
+  R3  empty slots are evictable like any other and keep their LRU place;
+  R4  a selection equal to ``newest`` binds to row ``B`` and is a hit that is
+      never counted as a miss;
+  R6  ``-1`` is padding (output -1); a duplicate or out-of-range position makes
+      the whole unit fail with its state untouched and an output row of -1;
+  R8  the miss count excludes padding and the newest binding.
+
+See ``tests/test_oracle_pins.py`` for what pins each of these.
+
+[P1] = gentlecold.top, "HiSparse 深度解析：论文、SGLang 实现与 vLLM Hybrid
+HiSparse" (sections as numbered on that page).
+"""
+
+ERR_RANGE = 1  # a position outside [-1, P), or newest outside [-1, P)
+ERR_DUP = 2    # the same position appears twice in one selection
+
+
+class Unit:
+    """One (request, layer) cache: B slots + newest row, LRU, page table."""
+
+    def __init__(self, B, P, k=None, host=None):
+        if k is not None and B < k:
+            raise ValueError("B must be >= k ([P1] §1: B >= k)")
+        self.B = B
+        self.P = P
+        self.slot_pos = [-1] * B
+        self.lru = list(range(B))          # oldest first; reset order 0..B-1
+        self.page_table = {}               # pos -> slot
+        self.host = host                   # callable pos -> bytes, or None
+        self.hot = [None] * (B + 1)        # row B = newest slot
+        self.miss_count = 0
+
+    # ------------------------------------------------------------------ #
+    def resolve(self, sel, newest=-1, skip_io=False):
+        """One RESOLVE of this unit for the selection list ``sel``.
+
+        Returns ``(out, plan, err)``: ``out[i]`` is the physical slot for
+        ``sel[i]`` (``B`` for the newest token, -1 for padding); ``plan`` is
+        the list of ``(pos, slot)`` fetches in miss order ([P1] §5.5, the miss
+        plan written where the eviction is decided); ``err`` is 0 or a bit-OR
+        of ``ERR_RANGE`` / ``ERR_DUP``.
+        """
+        B, P = self.B, self.P
+        k = len(sel)
+
+        # Validation (reading R6).
+        err = 0
+        seen = set()
+        for p in sel:
+            if p == -1:
+                continue
+            if p < -1 or p >= P:
+                err |= ERR_RANGE
+                continue
+            if p in seen:
+                err |= ERR_DUP
+            seen.add(p)
+        if newest < -1 or newest >= P:
+            err |= ERR_RANGE
+        if err:
+            self.miss_count = 0            # nothing was fetched this step
+            return [-1] * k, [], err
+
+        # Stages 1-2: classify every selection as padding, newest, hit or miss.
+        out = [None] * k
+        hit_slots = set()
+        misses = []                        # selection indices, in list order
+        for i, p in enumerate(sel):
+            if p == -1:
+                out[i] = -1
+            elif newest >= 0 and p == newest:
+                out[i] = B                 # reading R4
+            elif p in self.page_table:
+                s = self.page_table[p]
+                out[i] = s
+                hit_slots.add(s)
+            else:
+                misses.append(i)
+
+        # Stage 3: evictable slots in LRU order; miss j takes the j-th oldest.
+        ev = [s for s in self.lru if s not in hit_slots]
+        M = len(misses)
+        assert M <= len(ev), "B >= k guarantees a victim for every miss"
+
+        # Stages 4-5: fetch into the victims and publish the new mapping.
+        plan = []
+        for j, i in enumerate(misses):
+            s = ev[j]
+            p = sel[i]
+            old = self.slot_pos[s]
+            if old >= 0:
+                del self.page_table[old]
+            self.slot_pos[s] = p
+            self.page_table[p] = s
+            if self.host is not None and not skip_io:
+                self.hot[s] = self.host(p)
+            out[i] = s
+            plan.append((p, s))
+
+        # New recency order: untouched evictables (oldest), then this step's
+        # fetches, then this step's hits (newest) -- [P1] §3.3 and the worked
+        # example of [P1] §3.5; readings R1 and R2 fix the order inside groups.
+        self.lru = ev[M:] + ev[:M] + sorted(hit_slots)
+        self.miss_count = M
+        return out, plan, 0
+
+    # ------------------------------------------------------------------ #
+    def set_newest(self, record):
+        """The caller writes the new token's KV into row B ([P1] §3.4 step 4)."""
+        self.hot[self.B] = record
+
+    def writeback(self, pos, host_store):
+        """Write-through of the newest row to the host pool ([P1] §3.4 step 4)."""
+        host_store[pos] = self.hot[self.B]
+
+    def resident(self):
+        return {p for p in self.slot_pos if p >= 0}
+
+
+def replay(plan, follower_hot, follower_host):
+    """Copy-only replay of an anchor's miss plan into a shared layer.
+
+    A shared layer keeps its slots in lockstep with its anchor, so the anchor's
+    ``(pos, slot)`` list is also the shared layer's list; only the bytes come
+    from the shared layer's own host pool ([P1] §3.6 and §5.6).
+    """
+    for p, s in plan:
+        follower_hot[s] = follower_host(p)
+
+
+# ---------------------------------------------------------------------- #
+# Brute-force optimal replacement (Belady's offline optimum), for bounds.  #
+# ---------------------------------------------------------------------- #
+def optimal_misses(trace, B):
+    """Fewest misses any replacement policy with ``B`` slots can reach.
+
+    Exhaustive search over which resident positions to keep at each step.
+    The positions selected in the current step must all be resident after
+    it (they are protected), and a miss is a selected position that was not
+    resident before the step.  Only for tiny traces (B <= 4, a handful of
+    positions and steps).
+    """
+    from functools import lru_cache
+    from itertools import combinations
+
+    steps = [frozenset(p for p in s if p != -1) for s in trace]
+
+    @lru_cache(maxsize=None)
+    def best(t, resident):
+        if t == len(steps):
+            return 0
+        S = steps[t]
+        if len(S) > B:
+            raise ValueError("selection larger than B")
+        cost = len(S - resident)
+        others = sorted(resident - S)
+        room = B - len(S)
+        keep_n = min(room, len(others))
+        # Keeping more never hurts, so only maximal keep-sets are searched.
+        return cost + min(best(t + 1, S | frozenset(keep))
+                          for keep in combinations(others, keep_n))
+
+    return best(0, frozenset())

@@ -1,0 +1,264 @@
+"""The oracle pinned to the pages and to mathematics (CPU only)."""
+import random
+
+import numpy as np
+import pytest
+
+from oracle.tiny import Unit, optimal_misses, ERR_DUP, ERR_RANGE
+import pins
+from pins import CUnit, ALL_PINS
+
+MODELS = {"python": Unit, "c": CUnit}
+
+
+@pytest.mark.parametrize("model", sorted(MODELS))
+@pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
+def test_pin(model, pin):
+    pin(MODELS[model])
+
+
+def test_error_codes_match_between_models():
+    from oracle import coracle
+    assert (ERR_RANGE, ERR_DUP) == (coracle.ERR_RANGE, coracle.ERR_DUP) == (1, 2)
+
+
+# ---------------------------------------------------------------------- #
+# The brute-force optimum, pinned on its own                              #
+# ---------------------------------------------------------------------- #
+def belady_min(refs, frames):
+    """Belady's MIN for single-page references: evict the page used furthest ahead."""
+    mem, faults = set(), 0
+    for t, p in enumerate(refs):
+        if p in mem:
+            continue
+        faults += 1
+        if len(mem) == frames:
+            def nxt(q):
+                for u in range(t + 1, len(refs)):
+                    if refs[u] == q:
+                        return u
+                return len(refs) + 1
+            mem.remove(max(sorted(mem), key=nxt))
+        mem.add(p)
+    return faults
+
+
+def test_optimal_textbook_example():
+    # Silberschatz et al., Operating System Concepts: optimal replacement on this
+    # reference string with 3 frames takes 9 page faults.
+    refs = [7, 0, 1, 2, 0, 3, 0, 4, 2, 3, 0, 3, 2, 1, 2, 0, 1, 7, 0, 1]
+    assert optimal_misses([[p] for p in refs], 3) == 9
+    assert belady_min(refs, 3) == 9
+
+
+def test_optimal_matches_belady_min_for_single_page_steps():
+    for seed in range(30):
+        rnd = random.Random(seed)
+        frames = rnd.randint(1, 4)
+        refs = [rnd.randrange(7) for _ in range(rnd.randint(3, 14))]
+        assert optimal_misses([[p] for p in refs], frames) == belady_min(refs, frames)
+
+
+def test_optimal_closed_forms():
+    rnd = random.Random(7)
+    for _ in range(20):
+        B = rnd.randint(2, 4)
+        trace = [rnd.sample(range(8), rnd.randint(1, B)) for _ in range(rnd.randint(1, 5))]
+        distinct = len(set().union(*map(set, trace)))
+        # enough room for everything: only the first touch of each position misses
+        assert optimal_misses(trace, 8) == distinct
+        # every step needs its own positions, and the first step all misses
+        assert optimal_misses(trace, B) >= len(set(trace[0]))
+
+
+# ---------------------------------------------------------------------- #
+# Python model == C model, full state, on random traces                   #
+# ---------------------------------------------------------------------- #
+@pytest.mark.parametrize("seed", range(12))
+def test_python_equals_c(seed):
+    from oracle.coracle import OracleLayer
+    rnd = random.Random(seed)
+    R = rnd.randint(1, 3)
+    k = rnd.randint(1, 12)
+    B = k + rnd.randint(0, 10)
+    P = rnd.randint(k + 1, 60)
+    rec = 16
+    host = np.random.default_rng(seed).integers(0, 256, size=(R, P, rec), dtype=np.uint8)
+    py = [Unit(B, P, k=k, host=lambda p, r=r: bytes(host[r, p])) for r in range(R)]
+    c = OracleLayer(R, k, B, P, rec, host=host)
+    c.reset()
+    for t in range(30):
+        sel = np.full((R, k), -1, np.int32)
+        newest = np.full(R, -1, np.int32)
+        for r in range(R):
+            n = rnd.randint(0, k)
+            S = rnd.sample(range(P), n)
+            if rnd.random() < 0.08 and n >= 2:
+                S[1] = S[0]                      # duplicate
+            if rnd.random() < 0.05 and n >= 1:
+                S[0] = rnd.choice([P, P + 5, -3])  # out of range
+            sel[r, :n] = S
+            rnd.shuffle(sel[r])
+            if S and rnd.random() < 0.3:
+                newest[r] = rnd.choice(S)
+        out_c, e_c = c.resolve(sel, newest)
+        e_py = 0
+        for r in range(R):
+            out, plan, err = py[r].resolve([int(x) for x in sel[r]], int(newest[r]))
+            e_py |= err
+            assert out == list(out_c[r]), (t, r)
+            assert err == c.unit_err[r]
+            assert py[r].slot_pos == list(c.slot_pos[r])
+            assert py[r].lru == list(c.lru[r])
+            pt = {int(p): int(c.page_table[r, p]) for p in np.flatnonzero(c.page_table[r] >= 0)}
+            assert py[r].page_table == pt
+            assert py[r].miss_count == c.miss_count[r]
+            assert plan == [(int(c.plan_pos[r, j]), int(c.plan_slot[r, j]))
+                            for j in range(c.plan_count[r])]
+            for s in range(B):
+                if py[r].hot[s] is not None:
+                    assert py[r].hot[s] == bytes(c.hot[r, s])
+        assert e_py == e_c
+
+
+# ---------------------------------------------------------------------- #
+# Write-through and plan replay (C model)                                 #
+# ---------------------------------------------------------------------- #
+def test_writeback_then_fetch_returns_written_bytes():
+    from oracle.coracle import OracleLayer
+    R, k, B, L_ctx, steps, rec = 2, 3, 4, 10, 3, 16
+    P = L_ctx + steps
+    rng = np.random.default_rng(3)
+    host = rng.integers(0, 256, size=(R, P, rec), dtype=np.uint8)
+    c = OracleLayer(R, k, B, P, rec, host=host, host_split=L_ctx)
+    c.reset()
+    assert (c.host_tail == 0xA5).all()                 # unwritten rows are poisoned
+    newrec = rng.integers(0, 256, size=(steps, R, rec), dtype=np.uint8)
+    for t in range(steps):
+        if t > 0:
+            c.writeback(np.full(R, L_ctx + t - 1, np.int32))
+        c.set_newest_rows(newrec[t])
+        # select the previous token (now on the host) and the newest one
+        sel = np.full((R, k), -1, np.int32)
+        sel[:, 0] = L_ctx + t
+        if t > 0:
+            sel[:, 1] = L_ctx + t - 1
+        out, e = c.resolve(sel, np.full(R, L_ctx + t, np.int32))
+        assert e == 0
+        assert (out[:, 0] == B).all()
+        if t > 0:
+            for r in range(R):
+                assert bytes(c.hot[r, out[r, 1]]) == bytes(newrec[t - 1, r])
+
+
+def test_replay_follows_anchor_slots():
+    from oracle.coracle import OracleLayer
+    R, k, B, P, rec = 3, 5, 7, 40, 16
+    rng = np.random.default_rng(11)
+    host_a = rng.integers(0, 256, size=(R, P, rec), dtype=np.uint8)
+    host_f = rng.integers(0, 256, size=(R, P, rec), dtype=np.uint8)
+    a = OracleLayer(R, k, B, P, rec, host=host_a)
+    f = OracleLayer(R, k, B, P, rec, host=host_f, metadata=False)
+    a.reset()
+    for t in range(20):
+        sel = np.stack([rng.choice(P, size=k, replace=False) for _ in range(R)]).astype(np.int32)
+        a.resolve(sel)
+        a.replay_into(f)
+        for r in range(R):
+            for s in range(B):
+                p = a.slot_pos[r, s]
+                if p >= 0:
+                    assert bytes(f.hot[r, s]) == bytes(host_f[r, p])
+                    assert bytes(a.hot[r, s]) == bytes(host_a[r, p])
+
+
+# ---------------------------------------------------------------------- #
+# Planted mistakes: each must fail at least one pin                       #
+# ---------------------------------------------------------------------- #
+class _Mutant(Unit):
+    mutation = None
+
+    def resolve(self, sel, newest=-1, skip_io=False):
+        m = self.mutation
+        B, P, k = self.B, self.P, len(sel)
+        err, seen = 0, set()
+        for p in sel:
+            if p == -1:
+                continue
+            if p < -1 or p >= P:
+                err |= ERR_RANGE
+                continue
+            if p in seen and m != "no_dup_check":
+                err |= ERR_DUP
+            seen.add(p)
+        if newest < -1 or newest >= P:
+            err |= ERR_RANGE
+        if err:
+            return [-1] * k, [], err
+        out, hits, misses = [None] * k, [], []
+        for i, p in enumerate(sel):
+            if p == -1:
+                out[i] = -1
+            elif newest >= 0 and p == newest and m != "newest_is_miss":
+                out[i] = B
+            elif p in self.page_table:
+                out[i] = self.page_table[p]
+                hits.append(out[i])
+            else:
+                misses.append(i)
+        ev = [s for s in self.lru if s not in hits]
+        if m == "victims_from_newest_end":
+            ev = ev[::-1]
+        M = len(misses)
+        plan = []
+        for j, i in enumerate(misses):
+            s = ev[j]
+            p = sel[i]
+            old = self.slot_pos[s]
+            if old >= 0 and m != "keep_stale_mapping":
+                del self.page_table[old]
+            self.slot_pos[s] = p
+            self.page_table[p] = s
+            if self.host is not None and not skip_io and m != "no_fetch":
+                self.hot[s] = self.host(p + 1 if m == "fetch_off_by_one" else p)
+            out[i] = s
+            plan.append((p, s))
+        hs = sorted(hits)
+        if m == "hits_in_selection_order":
+            hs = hits
+        if m == "hits_before_misses":
+            self.lru = ev[M:] + hs + ev[:M]
+        elif m == "misses_oldest":
+            self.lru = ev[:M] + ev[M:] + hs
+        elif m == "misses_reversed":
+            self.lru = ev[M:] + ev[:M][::-1] + hs
+        elif m == "victims_from_newest_end":
+            self.lru = (ev[M:] + ev[:M])[::-1][::-1]
+            self.lru = [s for s in self.lru if s not in hs] + hs
+        else:
+            self.lru = ev[M:] + ev[:M] + hs
+        self.miss_count = M + (1 if m == "count_newest" and newest in sel else 0)
+        return out, plan, 0
+
+
+MUTATIONS = ["no_dup_check", "newest_is_miss", "victims_from_newest_end", "keep_stale_mapping",
+             "no_fetch", "fetch_off_by_one", "hits_in_selection_order", "hits_before_misses",
+             "misses_oldest", "misses_reversed", "count_newest"]
+
+
+@pytest.mark.parametrize("mutation", MUTATIONS)
+def test_planted_mistake_is_caught(mutation):
+    cls = type("M_" + mutation, (_Mutant,), {"mutation": mutation})
+    failed = []
+    for pin in ALL_PINS:
+        try:
+            pin(cls)
+        except (AssertionError, KeyError, IndexError, TypeError, ValueError):
+            failed.append(pin.__name__)
+    assert failed, f"no pin catches the planted mistake {mutation!r}"
+
+
+def test_unmutated_copy_passes_every_pin():
+    cls = type("M_none", (_Mutant,), {"mutation": None})
+    for pin in ALL_PINS:
+        pin(cls)

@@ -1,0 +1,1027 @@
+// hisparse.cu -- RESOLVE, write-through and plan-replay kernels for GB300
+// (sm_103a), and the C ABI declared in include/hisparse.h.
+//
+// Pages (cited by title and section):
+//   [DD] gentlecold.top, "HiSparse 深度解析：论文、SGLang 实现与 vLLM Hybrid
+//        HiSparse": §3.3 replacement policy, §3.4 write-through, §3.5 the five
+//        RESOLVE stages and the worked example, §3.6 exact prefetch, §5.2
+//        newest slot, §5.5 swap-in kernel (num_real_reqs, miss plan, one warp
+//        per miss, 16-byte non-coherent loads), §5.6 copy-only replay kernel.
+//   [VD] docs.vllm.ai, "HiSparse local KV offload architecture":
+//        "Hot lookup and LRU", "Performance invariants".
+//
+// GB300 design (what differs from the pages' one-CTA-per-request kernel):
+//   * One thread-block CLUSTER per request.  CTA 0 of the cluster (the
+//     leader) runs stages 1-3 and 5 on its shared memory; then every CTA of
+//     the cluster reads the miss list out of the leader's shared memory
+//     (distributed shared memory) and takes a share of stage 4.  A batch of 8
+//     requests thus fetches with 8 x 16 SMs instead of 8 SMs, which keeps
+//     enough 16-byte loads in flight to cover the host link's latency.
+//   * Stage 4 treats the misses of a request as one flat run of 16-byte
+//     chunks (miss j, chunk o), so no lane idles on records that are not a
+//     multiple of 512 bytes (1152-byte records are 72 chunks).
+//   * The scans of stage 3 give each warp one contiguous segment: warps count
+//     with __ballot_sync/__popc, one barrier publishes the 32 warp totals,
+//     each warp prefix-sums them with shuffles, and a second ballot pass writes
+//     the compacted lists -- two block barriers for all three scans.
+//   * No spin-waits: the only cross-CTA waits are hardware cluster barriers,
+//     and hash probing is bounded by the table size.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <climits>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "hisparse.h"
+
+namespace {
+
+constexpr int kThreads = 1024;            // threads per resolve CTA
+constexpr int kWarps = kThreads / 32;     // == 32: one warp total per lane
+constexpr int kUnroll = 4;                // 16-byte loads in flight per thread
+constexpr int32_t kUnresolved = INT32_MIN;
+constexpr unsigned kFull = 0xffffffffu;
+static_assert(kWarps == 32, "warp-total scan assumes 32 warps");
+
+thread_local int g_last_cuda_error = 0;
+
+// ---------------------------------------------------------------------------
+// Shared-memory layout of a resolve CTA (identical on host and device).
+// ---------------------------------------------------------------------------
+struct SmemLayout {
+  uint32_t key, val, sel, out, slotpos, hit, lru, newlru, missidx, victim, misc, total;
+};
+
+__host__ __device__ inline uint32_t align16(uint32_t x) { return (x + 15u) & ~15u; }
+
+__host__ __device__ inline SmemLayout smem_layout(int k, int B, int cap) {
+  SmemLayout L;
+  uint32_t o = 0;
+  L.key = o;     o += align16(4u * cap);   // hash keys; later the fetch positions
+  L.val = o;     o += align16(2u * cap);   // hash values (selection index); later fetch slots
+  L.sel = o;     o += align16(4u * k);
+  L.out = o;     o += align16(4u * k);
+  L.slotpos = o; o += align16(4u * B);
+  L.hit = o;     o += align16(1u * B);
+  L.lru = o;     o += align16(2u * B);
+  L.newlru = o;  o += align16(2u * B);
+  L.missidx = o; o += align16(2u * k);
+  L.victim = o;  o += align16(2u * k);
+  L.misc = o;    o += align16(4u * (8 + 3 * kWarps));
+  L.total = o;
+  return L;
+}
+
+// misc words
+enum { kMiscErr = 0, kMiscM = 1 };
+
+// ---------------------------------------------------------------------------
+// Kernel arguments
+// ---------------------------------------------------------------------------
+struct ResolveArgs {
+  int32_t R, k, B, cap_log2, rec16, io;
+  int64_t P;
+  const int32_t *sel, *num_reqs, *newest;
+  int32_t *out;
+  int32_t *slot_pos;
+  int16_t *lru;
+  int32_t *page_table, *miss_count, *unit_err;
+  uint32_t *status;
+  int32_t *plan_pos, *plan_slot, *plan_count;
+  const char *src;             // host pool (device-visible address) or HBM mirror
+  int64_t src_req_stride, src_row_stride;
+  char *hot;
+  int64_t hot_req_stride, hot_row_stride;
+};
+
+struct LayerDev {              // one layer's buffers, device-visible addresses
+  const char *host;            // host pool
+  char *host_w;                // same, writable
+  int64_t host_req_stride, host_row_stride;
+  char *hot;
+  int64_t hot_req_stride, hot_row_stride;
+  const char *mirror;
+};
+
+struct WritebackArgs {
+  const LayerDev *layers;      // device array [L]
+  int32_t layer0, R, B, rec16;
+  int64_t P;
+  const int32_t *pos;          // [nl][R]
+  const int32_t *num_reqs;
+  uint32_t *status;
+};
+
+struct ReplayArgs {
+  int32_t R, k, rec16;
+  const int32_t *num_reqs;
+  const int32_t *plan_pos, *plan_slot, *plan_count;
+  const char *src;
+  int64_t src_req_stride, src_row_stride;
+  char *hot;
+  int64_t hot_req_stride, hot_row_stride;
+};
+
+// ---------------------------------------------------------------------------
+// PTX helpers: cluster barrier, cluster rank, distributed shared memory,
+// non-coherent 16-byte loads.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of `p` (this CTA's shared memory) in the shared window of CTA `rank`.
+__device__ __forceinline__ uint32_t dsmem_addr(const void *p, uint32_t rank) {
+  uint32_t local = static_cast<uint32_t>(__cvta_generic_to_shared(p)), remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+  return remote;
+}
+__device__ __forceinline__ uint32_t ld_dsmem_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint4 ld_dsmem_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+// 16-byte load through the non-coherent path ([DD] §5.5: GPU threads read
+// pinned host memory directly with vectorised non-coherent loads).
+__device__ __forceinline__ uint4 ld_nc_v4(const void *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ void st_v4(void *p, uint4 v) {
+  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// Knuth's multiplicative hash into a table of 2^cap_log2 entries ([DD] §3.5
+// stage 1).
+__device__ __forceinline__ uint32_t hash_pos(int32_t p, int cap_log2) {
+  return (static_cast<uint32_t>(p) * 2654435761u) >> (32 - cap_log2);
+}
+
+// ---------------------------------------------------------------------------
+// Leader CTA: stages 1, 2, 3 and 5 for request r.  On return (after a block
+// barrier) misc[kMiscM] holds the number of misses M and, for j < M,
+// fpos[j] / fslot[j] hold the position and victim slot of miss j.
+// ---------------------------------------------------------------------------
+template <bool kRecordPlan>
+__device__ void leader_resolve(const ResolveArgs &a, int r, unsigned char *smem,
+                               const SmemLayout &L) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int k = a.k, B = a.B, cap = 1 << a.cap_log2;
+  const int64_t P = a.P;
+  int32_t *s_key = reinterpret_cast<int32_t *>(smem + L.key);
+  int16_t *s_val = reinterpret_cast<int16_t *>(smem + L.val);
+  int32_t *s_sel = reinterpret_cast<int32_t *>(smem + L.sel);
+  int32_t *s_out = reinterpret_cast<int32_t *>(smem + L.out);
+  int32_t *s_slotpos = reinterpret_cast<int32_t *>(smem + L.slotpos);
+  uint8_t *s_hit = reinterpret_cast<uint8_t *>(smem + L.hit);
+  int16_t *s_lru = reinterpret_cast<int16_t *>(smem + L.lru);
+  int16_t *s_newlru = reinterpret_cast<int16_t *>(smem + L.newlru);
+  int16_t *s_missidx = reinterpret_cast<int16_t *>(smem + L.missidx);
+  int16_t *s_victim = reinterpret_cast<int16_t *>(smem + L.victim);
+  uint32_t *s_misc = reinterpret_cast<uint32_t *>(smem + L.misc);
+  int32_t *s_cnt = reinterpret_cast<int32_t *>(s_misc + 8);  // [3][32]
+  int32_t *s_fpos = s_key;                                   // reused after stage 2
+  int16_t *s_fslot = s_val;
+
+  const int32_t newest = a.newest ? a.newest[r] : -1;
+  const int32_t *g_sel = a.sel + static_cast<int64_t>(r) * k;
+  int32_t *g_slotpos = a.slot_pos + static_cast<int64_t>(r) * B;
+  int16_t *g_lru = a.lru + static_cast<int64_t>(r) * B;
+  int32_t *g_pt = a.page_table + static_cast<int64_t>(r) * P;
+
+  // ---- stage 0: load the unit's inputs, clear the hash table ----
+  for (int i = tid; i < cap; i += kThreads) s_key[i] = -1;
+  for (int i = tid; i < k; i += kThreads) s_sel[i] = g_sel[i];
+  for (int s = tid; s < B; s += kThreads) {
+    s_slotpos[s] = g_slotpos[s];
+    s_lru[s] = g_lru[s];
+  }
+  if (tid == 0) s_misc[kMiscErr] = (newest < -1 || newest >= P) ? HISPARSE_ERR_RANGE : 0u;
+  __syncthreads();
+
+  // ---- stage 1: stage the selection in the hash, validate ----
+  for (int i = tid; i < k; i += kThreads) {
+    const int32_t p = s_sel[i];
+    int32_t o = -1;
+    if (p != -1) {
+      if (p < -1 || p >= P) {
+        atomicOr(&s_misc[kMiscErr], HISPARSE_ERR_RANGE);
+      } else {
+        o = (p == newest) ? B : kUnresolved;
+        uint32_t h = hash_pos(p, a.cap_log2);
+        for (int probe = 0; probe < cap; ++probe) {
+          const int32_t prev = atomicCAS(&s_key[h], -1, p);
+          if (prev == -1) {
+            s_val[h] = static_cast<int16_t>(i);
+            break;
+          }
+          if (prev == p) {
+            atomicOr(&s_misc[kMiscErr], HISPARSE_ERR_DUP);
+            break;
+          }
+          h = (h + 1) & (cap - 1);
+        }
+      }
+    }
+    s_out[i] = o;
+  }
+  __syncthreads();
+
+  const uint32_t err = s_misc[kMiscErr];
+  if (err) {  // uniform: the unit keeps its state, its out row is all -1
+    for (int i = tid; i < k; i += kThreads) a.out[static_cast<int64_t>(r) * k + i] = -1;
+    if (tid == 0) {
+      a.unit_err[r] = static_cast<int32_t>(err);
+      atomicOr(a.status, err);
+      a.miss_count[r] = 0;
+      a.plan_count[r] = 0;
+      s_misc[kMiscM] = 0;
+    }
+    __syncthreads();
+    return;
+  }
+
+  // ---- stage 2: mark each slot hit or evictable ----
+  for (int s = tid; s < B; s += kThreads) {
+    const int32_t p = s_slotpos[s];
+    uint8_t hit = 0;
+    if (p >= 0 && p != newest) {
+      uint32_t h = hash_pos(p, a.cap_log2);
+      for (int probe = 0; probe < cap; ++probe) {
+        const int32_t key = s_key[h];
+        if (key == p) {
+          s_out[s_val[h]] = s;
+          hit = 1;
+          break;
+        }
+        if (key == -1) break;
+        h = (h + 1) & (cap - 1);
+      }
+    }
+    s_hit[s] = hit;
+  }
+  __syncthreads();
+
+  // ---- stage 3: three order-stable compactions ----
+  //   misses     : selection indices still unresolved, in list order
+  //   evictables : slots that are not hits, in LRU order (oldest first)
+  //   hits       : hit slots, in ascending slot order
+  const int segk = ((k + kWarps * 32 - 1) / (kWarps * 32)) * 32;
+  const int segb = ((B + kWarps * 32 - 1) / (kWarps * 32)) * 32;
+  const int k0 = warp * segk, k1 = min(k, k0 + segk);
+  const int b0 = warp * segb, b1 = min(B, b0 + segb);
+  int cm = 0, ce = 0, ch = 0;
+  for (int i0 = k0; i0 < k1; i0 += 32) {
+    const int i = i0 + lane;
+    cm += __popc(__ballot_sync(kFull, i < k1 && s_out[i] == kUnresolved));
+  }
+  for (int j0 = b0; j0 < b1; j0 += 32) {
+    const int j = j0 + lane;
+    const bool in = j < b1;
+    ce += __popc(__ballot_sync(kFull, in && !s_hit[in ? s_lru[j] : 0]));
+    ch += __popc(__ballot_sync(kFull, in && s_hit[in ? j : 0]));
+  }
+  if (lane == 0) {
+    s_cnt[warp] = cm;
+    s_cnt[32 + warp] = ce;
+    s_cnt[64 + warp] = ch;
+  }
+  __syncthreads();
+  int vm = s_cnt[lane], ve = s_cnt[32 + lane], vh = s_cnt[64 + lane];
+  int im = vm, ie = ve, ih = vh;  // inclusive scans over the 32 warps
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int tm = __shfl_up_sync(kFull, im, d), te = __shfl_up_sync(kFull, ie, d),
+              th = __shfl_up_sync(kFull, ih, d);
+    if (lane >= d) {
+      im += tm;
+      ie += te;
+      ih += th;
+    }
+  }
+  const int M = __shfl_sync(kFull, im, 31);
+  const int E = __shfl_sync(kFull, ie, 31);
+  int om = __shfl_sync(kFull, im - vm, warp);
+  int oe = __shfl_sync(kFull, ie - ve, warp);
+  int oh = __shfl_sync(kFull, ih - vh, warp);
+  const uint32_t lt = lanemask_lt();
+  for (int i0 = k0; i0 < k1; i0 += 32) {
+    const int i = i0 + lane;
+    const bool f = i < k1 && s_out[i] == kUnresolved;
+    const uint32_t m = __ballot_sync(kFull, f);
+    if (f) s_missidx[om + __popc(m & lt)] = static_cast<int16_t>(i);
+    om += __popc(m);
+  }
+  for (int j0 = b0; j0 < b1; j0 += 32) {
+    const int j = j0 + lane;
+    const bool in = j < b1;
+    const int16_t sl = in ? s_lru[j] : 0;
+    const bool fe = in && !s_hit[sl];
+    uint32_t m = __ballot_sync(kFull, fe);
+    if (fe) {
+      const int e = oe + __popc(m & lt);
+      if (e < M) s_victim[e] = sl;                            // miss e takes it
+      s_newlru[e >= M ? e - M : E - M + e] = sl;              // untouched, then fetched
+    }
+    oe += __popc(m);
+    const bool fh = in && s_hit[in ? j : 0];
+    m = __ballot_sync(kFull, fh);
+    if (fh) s_newlru[E + oh + __popc(m & lt)] = static_cast<int16_t>(j);  // hits newest
+    oh += __popc(m);
+  }
+  __syncthreads();
+
+  // ---- stage 5 (metadata half): victims, page table, slot map, plan ----
+  for (int j = tid; j < M; j += kThreads) {
+    const int i = s_missidx[j];
+    const int16_t v = s_victim[j];
+    const int32_t p = s_sel[i];
+    const int32_t old = s_slotpos[v];
+    s_out[i] = v;
+    if (old >= 0) g_pt[old] = -1;
+    g_pt[p] = v;
+    g_slotpos[v] = p;
+    s_fpos[j] = p;
+    s_fslot[j] = v;
+    if (kRecordPlan) {
+      a.plan_pos[static_cast<int64_t>(r) * k + j] = p;
+      a.plan_slot[static_cast<int64_t>(r) * k + j] = v;
+    }
+  }
+  if (tid == 0) {
+    s_misc[kMiscM] = static_cast<uint32_t>(M);
+    a.miss_count[r] = M;
+    a.unit_err[r] = 0;
+    a.plan_count[r] = kRecordPlan ? M : 0;  // a replay follows only a recorded plan
+  }
+  __syncthreads();
+  for (int i = tid; i < k; i += kThreads) a.out[static_cast<int64_t>(r) * k + i] = s_out[i];
+  for (int s = tid; s < B; s += kThreads) g_lru[s] = s_newlru[s];
+}
+
+// ---------------------------------------------------------------------------
+// RESOLVE: grid = R clusters of `cs` CTAs; cluster c serves request c.
+// ---------------------------------------------------------------------------
+template <bool kRecordPlan>
+__global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const uint32_t cs = cluster_nctarank();
+  const uint32_t rank = cluster_ctarank();
+  const int r = static_cast<int>(blockIdx.x / cs);
+  const int nreq = a.num_reqs ? min(*a.num_reqs, a.R) : a.R;
+  if (r >= nreq) return;  // graph padding: the whole cluster leaves together
+
+  const SmemLayout L = smem_layout(a.k, a.B, 1 << a.cap_log2);
+  int32_t *s_fpos = reinterpret_cast<int32_t *>(smem + L.key);
+  int16_t *s_fslot = reinterpret_cast<int16_t *>(smem + L.val);
+  uint32_t *s_misc = reinterpret_cast<uint32_t *>(smem + L.misc);
+
+  if (rank == 0) leader_resolve<kRecordPlan>(a, r, smem, L);
+  cluster_arrive_release();
+  cluster_wait_acquire();
+
+  // Every CTA takes the miss list out of the leader's shared memory.
+  int M;
+  if (rank == 0) {
+    M = static_cast<int>(s_misc[kMiscM]);
+  } else {
+    M = static_cast<int>(ld_dsmem_u32(dsmem_addr(&s_misc[kMiscM], 0)));
+    const int n_pos16 = (M * 4 + 15) / 16, n_slot16 = (M * 2 + 15) / 16;
+    const uint32_t rp = dsmem_addr(s_fpos, 0), rs = dsmem_addr(s_fslot, 0);
+    for (int c = threadIdx.x; c < n_pos16; c += kThreads)
+      reinterpret_cast<uint4 *>(s_fpos)[c] = ld_dsmem_v4(rp + 16u * c);
+    for (int c = threadIdx.x; c < n_slot16; c += kThreads)
+      reinterpret_cast<uint4 *>(s_fslot)[c] = ld_dsmem_v4(rs + 16u * c);
+    __syncthreads();
+  }
+  cluster_arrive_relaxed();  // this CTA is done reading the leader's memory
+
+  // ---- stage 4: fetch, all CTAs of the cluster ----
+  if (a.io && M > 0) {
+    const int64_t total = static_cast<int64_t>(M) * a.rec16;
+    const int64_t T = static_cast<int64_t>(cs) * kThreads;
+    const char *src = a.src + static_cast<int64_t>(r) * a.src_req_stride;
+    char *dst = a.hot + static_cast<int64_t>(r) * a.hot_req_stride;
+    for (int64_t base = static_cast<int64_t>(rank) * kThreads + threadIdx.x; base < total;
+         base += T * kUnroll) {
+      uint4 v[kUnroll];
+      char *d[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int64_t c = base + u * T;
+        d[u] = nullptr;
+        if (c < total) {
+          const uint32_t c32 = static_cast<uint32_t>(c);
+          const int j = static_cast<int>(c32 / static_cast<uint32_t>(a.rec16));
+          const int o = static_cast<int>(c32 - static_cast<uint32_t>(j) * a.rec16);
+          v[u] = ld_nc_v4(src + static_cast<int64_t>(s_fpos[j]) * a.src_row_stride + 16 * o);
+          d[u] = dst + static_cast<int64_t>(s_fslot[j]) * a.hot_row_stride + 16 * o;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u)
+        if (d[u]) st_v4(d[u], v[u]);
+    }
+  }
+  cluster_wait_acquire();  // the leader's memory must outlive every reader
+}
+
+// ---------------------------------------------------------------------------
+// Write-through: grid (R, layers); copies hot row B to host row pos.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(128) writeback_kernel(const WritebackArgs a) {
+  const int r = blockIdx.x, li = blockIdx.y;
+  const int nreq = a.num_reqs ? min(*a.num_reqs, a.R) : a.R;
+  if (r >= nreq) return;
+  const int32_t p = a.pos[static_cast<int64_t>(li) * a.R + r];
+  if (p < 0) return;
+  if (p >= a.P) {
+    if (threadIdx.x == 0) atomicOr(a.status, HISPARSE_ERR_RANGE);
+    return;
+  }
+  const LayerDev &Ld = a.layers[a.layer0 + li];
+  const uint4 *s = reinterpret_cast<const uint4 *>(Ld.hot + static_cast<int64_t>(r) * Ld.hot_req_stride +
+                                                   static_cast<int64_t>(a.B) * Ld.hot_row_stride);
+  uint4 *d = reinterpret_cast<uint4 *>(Ld.host_w + static_cast<int64_t>(r) * Ld.host_req_stride +
+                                       static_cast<int64_t>(p) * Ld.host_row_stride);
+  for (int c = threadIdx.x; c < a.rec16; c += blockDim.x) st_v4(d + c, s[c]);
+}
+
+// ---------------------------------------------------------------------------
+// Plan replay for a shared-index layer ([DD] §3.6, §5.6): a small fixed grid
+// walks the flattened (request, miss, 16-byte chunk) space.
+// ---------------------------------------------------------------------------
+constexpr int kReplayThreads = 512;
+
+__global__ void __launch_bounds__(kReplayThreads) replay_kernel(const ReplayArgs a) {
+  extern __shared__ int32_t s_pref[];  // [R + 1] exclusive prefix of plan counts
+  const int nreq = a.num_reqs ? min(*a.num_reqs, a.R) : a.R;
+  if (threadIdx.x < 32) {
+    int run = 0;
+    for (int r0 = 0; r0 < nreq; r0 += 32) {
+      const int r = r0 + threadIdx.x;
+      int v = r < nreq ? a.plan_count[r] : 0, inc = v;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int t = __shfl_up_sync(kFull, inc, d);
+        if ((int)threadIdx.x >= d) inc += t;
+      }
+      if (r < nreq) s_pref[r] = run + inc - v;
+      run += __shfl_sync(kFull, inc, 31);
+    }
+    if (threadIdx.x == 0) s_pref[nreq] = run;
+  }
+  __syncthreads();
+  const int64_t total = static_cast<int64_t>(s_pref[nreq]) * a.rec16;
+  const int64_t T = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; base < total;
+       base += T * kUnroll) {
+    uint4 v[kUnroll];
+    char *d[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t c = base + u * T;
+      d[u] = nullptr;
+      if (c < total) {
+        const uint32_t c32 = static_cast<uint32_t>(c);
+        const int m = static_cast<int>(c32 / static_cast<uint32_t>(a.rec16));
+        const int o = static_cast<int>(c32 - static_cast<uint32_t>(m) * a.rec16);
+        int lo = 0, hi = nreq - 1;  // last r with s_pref[r] <= m
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (s_pref[mid] <= m) lo = mid; else hi = mid - 1;
+        }
+        const int j = m - s_pref[lo];
+        const int64_t pk = static_cast<int64_t>(lo) * a.k + j;
+        v[u] = ld_nc_v4(a.src + static_cast<int64_t>(lo) * a.src_req_stride +
+                        static_cast<int64_t>(a.plan_pos[pk]) * a.src_row_stride + 16 * o);
+        d[u] = a.hot + static_cast<int64_t>(lo) * a.hot_req_stride +
+               static_cast<int64_t>(a.plan_slot[pk]) * a.hot_row_stride + 16 * o;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+      if (d[u]) st_v4(d[u], v[u]);
+  }
+}
+
+// Reset: slot_pos = -1, lru = 0..B-1 for `n` units; page table -1 via memset.
+__global__ void reset_kernel(int32_t *slot_pos, int16_t *lru, int64_t n_units, int32_t B) {
+  const int64_t total = n_units * B;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    slot_pos[i] = -1;
+    lru[i] = static_cast<int16_t>(i % B);
+  }
+}
+
+}  // namespace
+
+// ===========================================================================
+// Host side
+// ===========================================================================
+struct AnchorMeta {
+  int32_t *slot_pos = nullptr;
+  int16_t *lru = nullptr;
+  int32_t *page_table = nullptr;
+  int32_t *miss_count = nullptr;
+  int32_t *unit_err = nullptr;
+  int32_t *plan_pos = nullptr;
+  int32_t *plan_slot = nullptr;
+  int32_t *plan_count = nullptr;
+};
+
+struct hisparse_handle {
+  int32_t R, L, k, B, rec;
+  int64_t P;
+  int32_t cs, cap_log2, replay_ctas, sm_count, device;
+  uint32_t smem;
+  std::vector<int32_t> anchor_of;
+  std::vector<LayerDev> layers;
+  std::vector<AnchorMeta> meta;
+  LayerDev *d_layers = nullptr;
+  uint32_t *d_status = nullptr;
+  int32_t *d_unit_err_all = nullptr;  // [L][R]
+  void *arena = nullptr;
+  int64_t arena_bytes = 0;
+};
+
+namespace {
+
+int cuda_fail(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return HISPARSE_ECUDA;
+}
+#define HS_CUDA(call)                              \
+  do {                                             \
+    cudaError_t e_ = (call);                       \
+    if (e_ != cudaSuccess) return cuda_fail(e_);   \
+  } while (0)
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int layer_ok(const hisparse_handle *h, int32_t layer) {
+  if (!h || layer < 0 || layer >= h->L) return HISPARSE_EINVAL;
+  return HISPARSE_OK;
+}
+
+int configure_resolve(hisparse_handle *h, int want_cs) {
+  const SmemLayout L = smem_layout(h->k, h->B, 1 << h->cap_log2);
+  h->smem = L.total;
+  if (L.total > 227u * 1024u) return HISPARSE_EBOUND;
+  const void *fns[2] = {reinterpret_cast<const void *>(&resolve_kernel<false>),
+                        reinterpret_cast<const void *>(&resolve_kernel<true>)};
+  for (const void *f : fns) {
+    HS_CUDA(cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total));
+    HS_CUDA(cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
+  }
+  auto active_clusters = [&](int cs) -> int {
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(static_cast<unsigned>(cs) * h->R);
+    lc.blockDim = dim3(kThreads);
+    lc.dynamicSmemBytes = L.total;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = cs;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    lc.attrs = at;
+    lc.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void *>(&resolve_kernel<true>), &lc) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    return n;
+  };
+  if (want_cs > 0) {
+    if (want_cs > 16) return HISPARSE_EBOUND;
+    if (active_clusters(want_cs) < 1) return HISPARSE_EBOUND;
+    h->cs = want_cs;
+    return HISPARSE_OK;
+  }
+  h->cs = 1;
+  for (int cs = 16; cs >= 2; cs >>= 1) {
+    if (cs * h->R > h->sm_count) continue;
+    if (active_clusters(cs) >= h->R) {
+      h->cs = cs;
+      break;
+    }
+  }
+  return HISPARSE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int hisparse_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char *hisparse_strerror(int code) {
+  switch (code) {
+    case HISPARSE_OK: return "ok";
+    case HISPARSE_EINVAL: return "invalid argument";
+    case HISPARSE_EBOUND: return "size outside supported bounds";
+    case HISPARSE_ENOMEM: return "out of memory";
+    case HISPARSE_ECUDA: return "CUDA call failed";
+    case HISPARSE_EROLE: return "layer role mismatch (anchor / shared layer)";
+    default: return "unknown error";
+  }
+}
+
+int hisparse_host_alloc(size_t bytes, void **out) {
+  if (!out || bytes == 0) return HISPARSE_EINVAL;
+  *out = nullptr;
+  cudaError_t e = cudaHostAlloc(out, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
+  if (e != cudaSuccess) {
+    g_last_cuda_error = static_cast<int>(e);
+    cudaGetLastError();
+    *out = nullptr;
+    return HISPARSE_ENOMEM;
+  }
+  return HISPARSE_OK;
+}
+
+int hisparse_host_free(void *p) {
+  if (!p) return HISPARSE_EINVAL;
+  HS_CUDA(cudaFreeHost(p));
+  return HISPARSE_OK;
+}
+
+int hisparse_init(const hisparse_config *cfg, const hisparse_layer_buffers *layers,
+                  hisparse_handle **out) {
+  if (!cfg || !layers || !out) return HISPARSE_EINVAL;
+  *out = nullptr;
+  const int32_t R = cfg->num_requests, L = cfg->num_layers, k = cfg->top_k, B = cfg->buffer_slots;
+  const int64_t P = cfg->host_rows;
+  const int32_t rec = cfg->record_bytes;
+  if (R < 1 || L < 1 || k < 1 || P < 1) return HISPARSE_EINVAL;
+  if (rec <= 0 || rec % 16) return HISPARSE_EINVAL;
+  if (R > 8192 || L > 4096 || B < k || B > 32767 || P > INT32_MAX) return HISPARSE_EBOUND;
+  // chunk indices of one launch's fetches stay below 2^31 (32-bit index math)
+  if (static_cast<int64_t>(R) * k * (rec / 16) >= (int64_t(1) << 31)) return HISPARSE_EBOUND;
+  if (cfg->ctas_per_request < 0 || cfg->ctas_per_request > 16 || cfg->replay_ctas < 0)
+    return HISPARSE_EBOUND;
+  std::vector<int32_t> anchor(L, -1);
+  if (cfg->anchor_of) {
+    for (int l = 0; l < L; ++l) anchor[l] = cfg->anchor_of[l];
+    for (int l = 0; l < L; ++l) {
+      const int a = anchor[l];
+      if (a == -1) continue;
+      if (a < 0 || a >= L || a == l || anchor[a] != -1) return HISPARSE_EROLE;
+    }
+  }
+  for (int l = 0; l < L; ++l) {
+    const hisparse_layer_buffers &b = layers[l];
+    if (!b.host_pool || !b.hot) return HISPARSE_EINVAL;
+    if (!aligned16(b.host_pool) || !aligned16(b.hot) || (b.mirror && !aligned16(b.mirror)))
+      return HISPARSE_EINVAL;
+    if (b.host_req_stride % 16 || b.host_row_stride % 16 || b.hot_req_stride % 16 ||
+        b.hot_row_stride % 16)
+      return HISPARSE_EINVAL;
+    if (b.host_row_stride < rec || b.hot_row_stride < rec || b.host_req_stride < 0 ||
+        b.hot_req_stride < 0)
+      return HISPARSE_EINVAL;
+  }
+
+  hisparse_handle *h = new (std::nothrow) hisparse_handle();
+  if (!h) return HISPARSE_ENOMEM;
+  h->R = R; h->L = L; h->k = k; h->B = B; h->P = P; h->rec = rec;
+  h->anchor_of = anchor;
+  int cap_log2 = 1;
+  while ((1 << cap_log2) < 2 * k) ++cap_log2;
+  h->cap_log2 = cap_log2;
+  int rc = HISPARSE_OK;
+  auto fail = [&](int code) {
+    hisparse_destroy(h);
+    return code;
+  };
+  cudaError_t e = cudaGetDevice(&h->device);
+  if (e != cudaSuccess) return fail(cuda_fail(e));
+  e = cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, h->device);
+  if (e != cudaSuccess) return fail(cuda_fail(e));
+  h->replay_ctas = cfg->replay_ctas > 0 ? cfg->replay_ctas : 16;
+
+  // device-visible addresses of the host pools
+  h->layers.resize(L);
+  for (int l = 0; l < L; ++l) {
+    const hisparse_layer_buffers &b = layers[l];
+    void *dp = nullptr;
+    e = cudaHostGetDevicePointer(&dp, b.host_pool, 0);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      g_last_cuda_error = static_cast<int>(e);
+      return fail(HISPARSE_EINVAL);  // not pinned + mapped host memory
+    }
+    LayerDev &d = h->layers[l];
+    d.host = static_cast<const char *>(dp);
+    d.host_w = static_cast<char *>(dp);
+    d.host_req_stride = b.host_req_stride;
+    d.host_row_stride = b.host_row_stride;
+    d.hot = static_cast<char *>(b.hot);
+    d.hot_req_stride = b.hot_req_stride;
+    d.hot_row_stride = b.hot_row_stride;
+    d.mirror = static_cast<const char *>(b.mirror);
+  }
+
+  rc = configure_resolve(h, cfg->ctas_per_request);
+  if (rc != HISPARSE_OK) return fail(rc);
+
+  // one arena for all metadata
+  auto al = [](int64_t x) { return (x + 255) & ~int64_t(255); };
+  int64_t per_anchor = al(4LL * R * B) + al(2LL * R * B) + al(4LL * R * P) + 3 * al(4LL * R) +
+                       2 * al(4LL * R * k);
+  int n_anchor = 0;
+  for (int l = 0; l < L; ++l) n_anchor += anchor[l] == -1;
+  const int64_t bytes = per_anchor * n_anchor + al(4LL * L * R) + al(sizeof(LayerDev) * L) + 256;
+  e = cudaMalloc(&h->arena, bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    g_last_cuda_error = static_cast<int>(e);
+    return fail(HISPARSE_ENOMEM);
+  }
+  h->arena_bytes = bytes;
+  char *cur = static_cast<char *>(h->arena);
+  auto take = [&](int64_t n) {
+    char *p = cur;
+    cur += al(n);
+    return p;
+  };
+  h->d_status = reinterpret_cast<uint32_t *>(take(256));
+  h->d_unit_err_all = reinterpret_cast<int32_t *>(take(4LL * L * R));
+  h->d_layers = reinterpret_cast<LayerDev *>(take(sizeof(LayerDev) * L));
+  h->meta.resize(L);
+  for (int l = 0; l < L; ++l) {
+    if (anchor[l] != -1) continue;
+    AnchorMeta &m = h->meta[l];
+    m.slot_pos = reinterpret_cast<int32_t *>(take(4LL * R * B));
+    m.lru = reinterpret_cast<int16_t *>(take(2LL * R * B));
+    m.page_table = reinterpret_cast<int32_t *>(take(4LL * R * P));
+    m.miss_count = reinterpret_cast<int32_t *>(take(4LL * R));
+    m.unit_err = h->d_unit_err_all + static_cast<int64_t>(l) * R;
+    m.plan_count = reinterpret_cast<int32_t *>(take(4LL * R));
+    take(4LL * R);
+    m.plan_pos = reinterpret_cast<int32_t *>(take(4LL * R * k));
+    m.plan_slot = reinterpret_cast<int32_t *>(take(4LL * R * k));
+  }
+  e = cudaMemset(h->arena, 0, bytes);
+  if (e != cudaSuccess) return fail(cuda_fail(e));
+  e = cudaMemcpy(h->d_layers, h->layers.data(), sizeof(LayerDev) * L, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return fail(cuda_fail(e));
+  rc = hisparse_reset(h, -1, nullptr);
+  if (rc != HISPARSE_OK) return fail(rc);
+  e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return fail(cuda_fail(e));
+  *out = h;
+  return HISPARSE_OK;
+}
+
+int hisparse_destroy(hisparse_handle *h) {
+  if (!h) return HISPARSE_EINVAL;
+  int rc = HISPARSE_OK;
+  if (h->arena) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaFree(h->arena);
+    if (e != cudaSuccess) rc = cuda_fail(e);
+  }
+  delete h;
+  return rc;
+}
+
+int hisparse_reset(hisparse_handle *h, int32_t layer, void *stream) {
+  if (!h) return HISPARSE_EINVAL;
+  if (layer != -1) {
+    if (layer_ok(h, layer)) return HISPARSE_EINVAL;
+    if (h->anchor_of[layer] != -1) return HISPARSE_EROLE;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int l = 0; l < h->L; ++l) {
+    if (h->anchor_of[l] != -1 || (layer != -1 && l != layer)) continue;
+    const AnchorMeta &m = h->meta[l];
+    HS_CUDA(cudaMemsetAsync(m.page_table, 0xff, sizeof(int32_t) * h->R * h->P, s));
+    HS_CUDA(cudaMemsetAsync(m.miss_count, 0, sizeof(int32_t) * h->R, s));
+    HS_CUDA(cudaMemsetAsync(m.plan_count, 0, sizeof(int32_t) * h->R, s));
+    HS_CUDA(cudaMemsetAsync(m.unit_err, 0, sizeof(int32_t) * h->R, s));
+    const int64_t n = static_cast<int64_t>(h->R) * h->B;
+    const int grid = static_cast<int>(std::min<int64_t>((n + 255) / 256, 4096));
+    reset_kernel<<<grid, 256, 0, s>>>(m.slot_pos, m.lru, h->R, h->B);
+    HS_CUDA(cudaGetLastError());
+  }
+  return HISPARSE_OK;
+}
+
+int hisparse_resolve(hisparse_handle *h, int32_t layer, const int32_t *d_sel,
+                     const int32_t *d_num_reqs, const int32_t *d_newest, int32_t *d_out,
+                     uint32_t flags, void *stream) {
+  if (layer_ok(h, layer)) return HISPARSE_EINVAL;
+  if (!d_sel || !d_out) return HISPARSE_EINVAL;
+  if (flags & ~(HISPARSE_RECORD_PLAN | HISPARSE_SKIP_IO | HISPARSE_FROM_MIRROR)) return HISPARSE_EINVAL;
+  if (h->anchor_of[layer] != -1) return HISPARSE_EROLE;
+  const LayerDev &Ld = h->layers[layer];
+  const AnchorMeta &m = h->meta[layer];
+  if ((flags & HISPARSE_FROM_MIRROR) && !Ld.mirror) return HISPARSE_EINVAL;
+  ResolveArgs a;
+  a.R = h->R; a.k = h->k; a.B = h->B; a.cap_log2 = h->cap_log2; a.rec16 = h->rec / 16;
+  a.io = (flags & HISPARSE_SKIP_IO) ? 0 : 1;
+  a.P = h->P;
+  a.sel = d_sel; a.num_reqs = d_num_reqs; a.newest = d_newest; a.out = d_out;
+  a.slot_pos = m.slot_pos; a.lru = m.lru; a.page_table = m.page_table;
+  a.miss_count = m.miss_count; a.unit_err = m.unit_err; a.status = h->d_status;
+  a.plan_pos = m.plan_pos; a.plan_slot = m.plan_slot; a.plan_count = m.plan_count;
+  a.src = (flags & HISPARSE_FROM_MIRROR) ? Ld.mirror : Ld.host;
+  a.src_req_stride = Ld.host_req_stride; a.src_row_stride = Ld.host_row_stride;
+  a.hot = Ld.hot; a.hot_req_stride = Ld.hot_req_stride; a.hot_row_stride = Ld.hot_row_stride;
+
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(static_cast<unsigned>(h->cs) * h->R);
+  lc.blockDim = dim3(kThreads);
+  lc.dynamicSmemBytes = h->smem;
+  lc.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = h->cs;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  lc.attrs = at;
+  lc.numAttrs = 1;
+  cudaError_t e = (flags & HISPARSE_RECORD_PLAN) ? cudaLaunchKernelEx(&lc, resolve_kernel<true>, a)
+                                                 : cudaLaunchKernelEx(&lc, resolve_kernel<false>, a);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return HISPARSE_OK;
+}
+
+int hisparse_writeback(hisparse_handle *h, int32_t layer, const int32_t *d_pos,
+                       const int32_t *d_num_reqs, void *stream) {
+  if (!h || !d_pos) return HISPARSE_EINVAL;
+  if (layer != -1 && layer_ok(h, layer)) return HISPARSE_EINVAL;
+  WritebackArgs a;
+  a.layers = h->d_layers;
+  a.layer0 = layer == -1 ? 0 : layer;
+  a.R = h->R; a.B = h->B; a.rec16 = h->rec / 16; a.P = h->P;
+  a.pos = d_pos; a.num_reqs = d_num_reqs; a.status = h->d_status;
+  const dim3 grid(h->R, layer == -1 ? h->L : 1);
+  writeback_kernel<<<grid, 128, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  HS_CUDA(cudaGetLastError());
+  return HISPARSE_OK;
+}
+
+int hisparse_prefetch_plan(hisparse_handle *h, int32_t anchor_layer, int32_t follower_layer,
+                           const int32_t *d_num_reqs, void *stream) {
+  if (layer_ok(h, anchor_layer) || layer_ok(h, follower_layer)) return HISPARSE_EINVAL;
+  if (h->anchor_of[anchor_layer] != -1 || h->anchor_of[follower_layer] != anchor_layer)
+    return HISPARSE_EROLE;
+  const AnchorMeta &m = h->meta[anchor_layer];
+  const LayerDev &Lf = h->layers[follower_layer];
+  ReplayArgs a;
+  a.R = h->R; a.k = h->k; a.rec16 = h->rec / 16; a.num_reqs = d_num_reqs;
+  a.plan_pos = m.plan_pos; a.plan_slot = m.plan_slot; a.plan_count = m.plan_count;
+  a.src = Lf.host; a.src_req_stride = Lf.host_req_stride; a.src_row_stride = Lf.host_row_stride;
+  a.hot = Lf.hot; a.hot_req_stride = Lf.hot_req_stride; a.hot_row_stride = Lf.hot_row_stride;
+  const size_t smem = sizeof(int32_t) * (h->R + 1);
+  replay_kernel<<<h->replay_ctas, kReplayThreads, smem, static_cast<cudaStream_t>(stream)>>>(a);
+  HS_CUDA(cudaGetLastError());
+  return HISPARSE_OK;
+}
+
+int hisparse_copy_miss_counts(hisparse_handle *h, int32_t layer, int32_t *d_dst, void *stream) {
+  if (layer_ok(h, layer) || !d_dst) return HISPARSE_EINVAL;
+  if (h->anchor_of[layer] != -1) return HISPARSE_EROLE;
+  HS_CUDA(cudaMemcpyAsync(d_dst, h->meta[layer].miss_count, sizeof(int32_t) * h->R,
+                          cudaMemcpyDeviceToDevice, static_cast<cudaStream_t>(stream)));
+  return HISPARSE_OK;
+}
+
+int hisparse_get_status(hisparse_handle *h, uint32_t *flags_out, int32_t *unit_err_out) {
+  if (!h || !flags_out) return HISPARSE_EINVAL;
+  HS_CUDA(cudaDeviceSynchronize());
+  HS_CUDA(cudaMemcpy(flags_out, h->d_status, sizeof(uint32_t), cudaMemcpyDeviceToHost));
+  HS_CUDA(cudaMemset(h->d_status, 0, sizeof(uint32_t)));
+  if (unit_err_out)
+    HS_CUDA(cudaMemcpy(unit_err_out, h->d_unit_err_all, sizeof(int32_t) * h->L * h->R,
+                       cudaMemcpyDeviceToHost));
+  HS_CUDA(cudaDeviceSynchronize());
+  return HISPARSE_OK;
+}
+
+int hisparse_export_state(hisparse_handle *h, int32_t layer, int32_t *slot_pos, int16_t *lru,
+                          int32_t *page_table, int32_t *miss_counts) {
+  if (layer_ok(h, layer)) return HISPARSE_EINVAL;
+  if (h->anchor_of[layer] != -1) return HISPARSE_EROLE;
+  const AnchorMeta &m = h->meta[layer];
+  HS_CUDA(cudaDeviceSynchronize());
+  const size_t RB = static_cast<size_t>(h->R) * h->B;
+  if (slot_pos) HS_CUDA(cudaMemcpy(slot_pos, m.slot_pos, 4 * RB, cudaMemcpyDeviceToHost));
+  if (lru) HS_CUDA(cudaMemcpy(lru, m.lru, 2 * RB, cudaMemcpyDeviceToHost));
+  if (page_table)
+    HS_CUDA(cudaMemcpy(page_table, m.page_table, 4 * static_cast<size_t>(h->R) * h->P,
+                       cudaMemcpyDeviceToHost));
+  if (miss_counts) HS_CUDA(cudaMemcpy(miss_counts, m.miss_count, 4 * h->R, cudaMemcpyDeviceToHost));
+  return HISPARSE_OK;
+}
+
+int hisparse_import_state(hisparse_handle *h, int32_t layer, const int32_t *slot_pos,
+                          const int16_t *lru, const int32_t *page_table) {
+  if (layer_ok(h, layer) || !slot_pos || !lru || !page_table) return HISPARSE_EINVAL;
+  if (h->anchor_of[layer] != -1) return HISPARSE_EROLE;
+  const int32_t B = h->B;
+  const int64_t P = h->P;
+  std::vector<uint8_t> seen(B);
+  for (int r = 0; r < h->R; ++r) {
+    const int32_t *sp = slot_pos + static_cast<int64_t>(r) * B;
+    const int16_t *lr = lru + static_cast<int64_t>(r) * B;
+    const int32_t *pt = page_table + static_cast<int64_t>(r) * P;
+    std::fill(seen.begin(), seen.end(), 0);
+    for (int j = 0; j < B; ++j) {
+      if (lr[j] < 0 || lr[j] >= B || seen[lr[j]]) return HISPARSE_EINVAL;
+      seen[lr[j]] = 1;
+    }
+    int64_t occupied = 0;
+    for (int s = 0; s < B; ++s) {
+      if (sp[s] < -1 || sp[s] >= P) return HISPARSE_EINVAL;
+      if (sp[s] >= 0) {
+        if (pt[sp[s]] != s) return HISPARSE_EINVAL;  // also rules out a position twice
+        ++occupied;
+      }
+    }
+    int64_t mapped = 0;
+    for (int64_t p = 0; p < P; ++p) {
+      if (pt[p] == -1) continue;
+      if (pt[p] < 0 || pt[p] >= B || sp[pt[p]] != p) return HISPARSE_EINVAL;
+      ++mapped;
+    }
+    if (mapped != occupied) return HISPARSE_EINVAL;
+  }
+  const AnchorMeta &m = h->meta[layer];
+  HS_CUDA(cudaDeviceSynchronize());
+  const size_t RB = static_cast<size_t>(h->R) * B;
+  HS_CUDA(cudaMemcpy(m.slot_pos, slot_pos, 4 * RB, cudaMemcpyHostToDevice));
+  HS_CUDA(cudaMemcpy(m.lru, lru, 2 * RB, cudaMemcpyHostToDevice));
+  HS_CUDA(cudaMemcpy(m.page_table, page_table, 4 * static_cast<size_t>(h->R) * P,
+                     cudaMemcpyHostToDevice));
+  return HISPARSE_OK;
+}
+
+int hisparse_export_plan(hisparse_handle *h, int32_t layer, int32_t *count, int32_t *pos,
+                         int32_t *slot) {
+  if (layer_ok(h, layer) || !count || !pos || !slot) return HISPARSE_EINVAL;
+  if (h->anchor_of[layer] != -1) return HISPARSE_EROLE;
+  const AnchorMeta &m = h->meta[layer];
+  HS_CUDA(cudaDeviceSynchronize());
+  const size_t Rk = static_cast<size_t>(h->R) * h->k;
+  HS_CUDA(cudaMemcpy(count, m.plan_count, 4 * h->R, cudaMemcpyDeviceToHost));
+  HS_CUDA(cudaMemcpy(pos, m.plan_pos, 4 * Rk, cudaMemcpyDeviceToHost));
+  HS_CUDA(cudaMemcpy(slot, m.plan_slot, 4 * Rk, cudaMemcpyDeviceToHost));
+  return HISPARSE_OK;
+}
+
+int hisparse_get_info(const hisparse_handle *h, hisparse_info *out) {
+  if (!h || !out) return HISPARSE_EINVAL;
+  out->ctas_per_request = h->cs;
+  out->threads_per_cta = kThreads;
+  out->smem_bytes = static_cast<int32_t>(h->smem);
+  out->hash_capacity = 1 << h->cap_log2;
+  out->replay_ctas = h->replay_ctas;
+  out->sm_count = h->sm_count;
+  out->metadata_bytes = h->arena_bytes;
+  return HISPARSE_OK;
+}
+
+}  // extern "C"

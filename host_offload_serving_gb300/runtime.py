@@ -1,0 +1,245 @@
+"""Host-side orchestration of the HiSparse hot path (memory, streams, events).
+
+``HostPool``   pinned, device-mapped host memory from ``hisparse_host_alloc``.
+``HiSparse``   one library instance: holds the handle, checks every return code.
+``DecodeStep`` issues one decode step over all layers the way the pages order
+               it (gentlecold.top "HiSparse 深度解析" §3.4 write-through, §3.6 and
+               §5.6 plan-then-IO prefetch; docs.vllm.ai "HiSparse local KV
+               offload architecture", performance invariants):
+                 backup stream : write-through of the previous token, event
+                 compute stream: wait for the write-through, place the new
+                                 token's KV in row B, RESOLVE each anchor
+                                 (recording its plan when it has followers)
+                 side stream   : after each anchor, replay its plan into each
+                                 follower, one event per follower
+               No call in a step allocates or reads device values on the host,
+               so a whole step can be captured in a CUDA graph.
+
+torch is used for device memory, streams, events and graphs only; every byte
+and index of the hot path is produced by the kernels in ``libhisparse.so``.
+"""
+import ctypes
+
+import numpy as np
+import torch
+
+from . import hisparse as H
+
+
+class HostPool:
+    """Pinned + mapped host memory of exactly ``nbytes`` (freed by ``close``)."""
+
+    def __init__(self, nbytes):
+        rc, ptr = H.hisparse_host_alloc(int(nbytes))
+        H.check(rc, f"hisparse_host_alloc({nbytes})")
+        self.ptr = ptr
+        self.nbytes = int(nbytes)
+
+    def numpy(self):
+        buf = (ctypes.c_uint8 * self.nbytes).from_address(self.ptr)
+        return np.ctypeslib.as_array(buf)
+
+    def close(self):
+        if self.ptr:
+            H.check(H.hisparse_host_free(self.ptr), "hisparse_host_free")
+            self.ptr = 0
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+class HiSparse:
+    """One instance of the C library (R requests, L layers, k, B, P, record)."""
+
+    def __init__(self, R, L, k, B, P, rec, layers, anchor_of=None, ctas_per_request=0,
+                 replay_ctas=0):
+        self.R, self.L, self.k, self.B, self.P, self.rec = R, L, k, B, P, rec
+        self.anchor_of = list(anchor_of) if anchor_of is not None else [-1] * L
+        self._anchor_arr = (ctypes.c_int32 * L)(*self.anchor_of)
+        cfg = H.Config(R, L, k, B, P, rec, ctas_per_request, replay_ctas,
+                       ctypes.cast(self._anchor_arr, ctypes.c_void_p))
+        rc, h = H.hisparse_init(cfg, layers)
+        H.check(rc, "hisparse_init")
+        self.h = h
+
+    # ---- launches (asynchronous, graph-capturable) ----
+    def resolve(self, layer, sel, out, num_reqs=None, newest=None, flags=0, stream=None):
+        H.check(H.hisparse_resolve(self.h, layer, _ptr(sel), _ptr(num_reqs), _ptr(newest),
+                                   _ptr(out), flags, _stream(stream)), "hisparse_resolve")
+
+    def writeback(self, layer, pos, num_reqs=None, stream=None):
+        H.check(H.hisparse_writeback(self.h, layer, _ptr(pos), _ptr(num_reqs), _stream(stream)),
+                "hisparse_writeback")
+
+    def prefetch_plan(self, anchor, follower, num_reqs=None, stream=None):
+        H.check(H.hisparse_prefetch_plan(self.h, anchor, follower, _ptr(num_reqs),
+                                         _stream(stream)), "hisparse_prefetch_plan")
+
+    def copy_miss_counts(self, layer, dst, stream=None):
+        H.check(H.hisparse_copy_miss_counts(self.h, layer, _ptr(dst), _stream(stream)),
+                "hisparse_copy_miss_counts")
+
+    def reset(self, layer=-1, stream=None):
+        H.check(H.hisparse_reset(self.h, layer, _stream(stream)), "hisparse_reset")
+
+    # ---- synchronous queries ----
+    def status(self):
+        ue = np.zeros((self.L, self.R), np.int32)
+        rc, flags = H.hisparse_get_status(self.h, ue.ctypes.data)
+        H.check(rc, "hisparse_get_status")
+        return flags, ue
+
+    def export_state(self, layer):
+        sp = np.empty((self.R, self.B), np.int32)
+        lru = np.empty((self.R, self.B), np.int16)
+        pt = np.empty((self.R, self.P), np.int32)
+        mc = np.empty(self.R, np.int32)
+        H.check(H.hisparse_export_state(self.h, layer, sp.ctypes.data, lru.ctypes.data,
+                                        pt.ctypes.data, mc.ctypes.data), "hisparse_export_state")
+        return sp, lru, pt, mc
+
+    def import_state(self, layer, slot_pos, lru, page_table):
+        sp = np.ascontiguousarray(slot_pos, np.int32)
+        lr = np.ascontiguousarray(lru, np.int16)
+        pt = np.ascontiguousarray(page_table, np.int32)
+        return H.hisparse_import_state(self.h, layer, sp.ctypes.data, lr.ctypes.data,
+                                       pt.ctypes.data)
+
+    def export_plan(self, layer):
+        c = np.empty(self.R, np.int32)
+        p = np.empty((self.R, self.k), np.int32)
+        s = np.empty((self.R, self.k), np.int32)
+        H.check(H.hisparse_export_plan(self.h, layer, c.ctypes.data, p.ctypes.data, s.ctypes.data),
+                "hisparse_export_plan")
+        return c, p, s
+
+    def info(self):
+        rc, info = H.hisparse_get_info(self.h)
+        H.check(rc, "hisparse_get_info")
+        return {f: getattr(info, f) for f, _ in H.Info._fields_}
+
+    def close(self):
+        if self.h:
+            H.check(H.hisparse_destroy(self.h), "hisparse_destroy")
+            self.h = None
+
+
+class WorkloadMemory:
+    """Host pools, hot buffers and optional HBM mirrors for a workload.
+
+    Host pool of layer l: ``pool + l*layer_stride``, rows [R][P][rec].
+    Hot buffer of layer l: ``hot[l]`` (uint8 [R][B+1][rec], device).
+    """
+
+    def __init__(self, R, L, B, P, rec, device="cuda", mirror=False):
+        self.R, self.L, self.B, self.P, self.rec = R, L, B, P, rec
+        self.req_stride = P * rec
+        self.layer_stride = R * P * rec
+        self.pool = HostPool(L * self.layer_stride)
+        self.hot = torch.zeros((L, R, B + 1, rec), dtype=torch.uint8, device=device)
+        self.mirror = None
+        if mirror:
+            self.mirror = torch.empty((L, R, P, rec), dtype=torch.uint8, device=device)
+
+    def host_view(self, layer):
+        """numpy uint8 [R][P][rec] view of one layer's host pool."""
+        a = self.pool.numpy()
+        return a[layer * self.layer_stride:(layer + 1) * self.layer_stride].reshape(
+            self.R, self.P, self.rec)
+
+    def layer_buffers(self):
+        out = []
+        for l in range(self.L):
+            out.append(H.LayerBuffers(
+                self.pool.ptr + l * self.layer_stride, self.req_stride, self.rec,
+                self.hot[l].data_ptr(), (self.B + 1) * self.rec, self.rec,
+                self.mirror[l].data_ptr() if self.mirror is not None else None))
+        return out
+
+    def fill_mirror(self):
+        """Copy the host pool into the HBM mirror (pinned -> device)."""
+        src = torch.from_numpy(self.pool.numpy()).view(self.L, self.R, self.P, self.rec)
+        self.mirror.copy_(src, non_blocking=False)
+
+    def close(self):
+        self.pool.close()
+
+
+class DecodeStep:
+    """Issue decode steps over all layers with the stream/event order of the pages.
+
+    ``groups`` is a list of (anchor layer, [follower layers]).  Per step t the
+    caller provides device tensors: ``sel[t]`` int32 [Lr][R][k] (Lr = anchors),
+    ``newest[t]`` int32 [R] or None, ``wb_pos[t]`` int32 [L][R] or None (rows to
+    write back first), ``new_rows[t]`` uint8 [L][R][rec] or None (the new
+    token's KV, placed in row B), and ``out`` int32 [Lr][R][k] receives the slot
+    vectors.
+    """
+
+    def __init__(self, hs, mem, groups, flags=0, num_reqs=None):
+        self.hs, self.mem, self.groups = hs, mem, groups
+        self.flags = flags
+        self.num_reqs = num_reqs
+        self.compute = torch.cuda.Stream()
+        self.backup = torch.cuda.Stream()
+        self.side = torch.cuda.Stream()
+        self.ev_wb = torch.cuda.Event()
+        self.ev_anchor = [torch.cuda.Event() for _ in groups]
+        self.ev_follow = [[torch.cuda.Event() for _ in f] for _, f in groups]
+        self.ev_step_start = torch.cuda.Event()
+        self.ev_side_done = torch.cuda.Event()
+
+    def issue(self, sel, out, newest=None, wb_pos=None, new_rows=None):
+        """Enqueue one step on the instance's streams (returns immediately)."""
+        hs, mem = self.hs, self.mem
+        cur = torch.cuda.current_stream()
+        self.ev_step_start.record(cur)
+        self.compute.wait_event(self.ev_step_start)
+        if wb_pos is not None:
+            self.backup.wait_event(self.ev_step_start)
+            hs.writeback(-1, wb_pos, self.num_reqs, stream=self.backup)
+            self.ev_wb.record(self.backup)
+            self.compute.wait_event(self.ev_wb)
+        with torch.cuda.stream(self.compute):
+            if new_rows is not None:
+                mem.hot[:, :, mem.B, :].copy_(new_rows, non_blocking=True)
+            for gi, (anchor, followers) in enumerate(self.groups):
+                f = self.flags | (H.RECORD_PLAN if followers else 0)
+                hs.resolve(anchor, sel[gi], out[gi], self.num_reqs, newest, f, stream=self.compute)
+                if followers:
+                    self.ev_anchor[gi].record(self.compute)
+                    self.side.wait_event(self.ev_anchor[gi])
+                    for fi, fl in enumerate(followers):
+                        hs.prefetch_plan(anchor, fl, self.num_reqs, stream=self.side)
+                        self.ev_follow[gi][fi].record(self.side)
+                    # the next anchor resolve rewrites the plan: it waits for the
+                    # replays of this group (only relevant within one step when
+                    # two groups share an anchor, which they do not; kept for
+                    # the next step below)
+        # a shared layer's attention would wait on its own event; at the end of
+        # the step the caller's stream waits for everything
+        for gi, (_, followers) in enumerate(self.groups):
+            for fi in range(len(followers)):
+                cur.wait_event(self.ev_follow[gi][fi])
+                self.compute.wait_event(self.ev_follow[gi][fi])
+        self.ev_side_done.record(self.compute)
+        cur.wait_event(self.ev_side_done)

@@ -1,0 +1,234 @@
+/*
+ * hisparse.h -- C ABI of the HiSparse RESOLVE hot path on GB300 (sm_103a).
+ *
+ * HiSparse keeps the authoritative KV of every decoding request in pinned host
+ * memory and only a fixed B-slot hot buffer per (request, layer) in HBM.  Each
+ * sparse layer, after its indexer picks k logical positions, runs RESOLVE:
+ * find the selections already in the hot buffer, pick LRU victims for the
+ * rest, copy the missing records from the host pool into the victims with GPU
+ * threads, and publish the position -> slot vector that sparse attention reads.
+ *
+ * Sources (cited by page title and section):
+ *   [DD]  gentlecold.top, "HiSparse 深度解析：论文、SGLang 实现与 vLLM Hybrid
+ *         HiSparse" (HiSparse deep dive): §3.2 hierarchy and metadata, §3.3
+ *         replacement policy, §3.4 request lifecycle and write-through, §3.5
+ *         RESOLVE fused kernel, §3.6 exact cross-layer prefetch, §5.2
+ *         per-request tensors and the newest slot, §5.5 swap-in kernel,
+ *         §5.6 prefetch in SGLang, §5.7 --hisparse-config fields.
+ *   [VD]  docs.vllm.ai, "HiSparse local KV offload architecture" (vLLM design
+ *         doc): "Hot lookup and LRU" and "Performance invariants".
+ *
+ * Conventions
+ *   - Every call returns HISPARSE_OK (0) or a negative HISPARSE_E* code.
+ *     Host-side argument errors are detected before any CUDA call.
+ *   - "d_" arguments are device pointers; everything else is host memory.
+ *   - Launch calls (resolve, writeback, prefetch_plan) never allocate, never
+ *     synchronise and never read device values on the host, so they can be
+ *     captured in a CUDA graph ([VD] "Performance invariants": no scalar
+ *     readback, no CPU/device round trip).
+ *   - Errors in device-side inputs never trap the GPU: the kernel records them
+ *     in a sticky status word (HISPARSE_ERR_* bits, read with
+ *     hisparse_get_status) and in a per-(layer, request) error code, and the
+ *     failing unit keeps its previous state.
+ *   - A stream argument is a cudaStream_t passed as void* (NULL = the legacy
+ *     default stream).
+ */
+#ifndef HISPARSE_H
+#define HISPARSE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- return codes ------------------------------------------------------ */
+#define HISPARSE_OK 0
+#define HISPARSE_EINVAL (-1)  /* NULL pointer, bad layer id, misaligned buffer,
+                                 record size not a multiple of 16, bad stride */
+#define HISPARSE_EBOUND (-2)  /* a size outside what the library supports
+                                 (B < k, B > 32767, shared memory too large, ...) */
+#define HISPARSE_ENOMEM (-3)  /* device or pinned host allocation failed */
+#define HISPARSE_ECUDA (-4)   /* a CUDA call failed; see hisparse_last_cuda_error */
+#define HISPARSE_EROLE (-5)   /* resolve on a shared-index layer, or a replay
+                                 pair that is not (anchor, its follower) */
+
+/* ---- device-detected error bits (status word and per-unit codes) ------- */
+#define HISPARSE_ERR_RANGE 1u /* a selected position outside [-1, P), or a
+                                 newest / write-back position outside [-1, P) */
+#define HISPARSE_ERR_DUP 2u   /* one position selected twice by one request */
+
+/* ---- resolve flags ----------------------------------------------------- */
+#define HISPARSE_RECORD_PLAN 1u /* record the miss plan for shared layers ([DD] §5.5) */
+#define HISPARSE_SKIP_IO 2u     /* the pages' no-IO oracle: metadata only, missed
+                                   rows keep stale bytes ([DD] §4.4, §5.6) */
+#define HISPARSE_FROM_MIRROR 4u /* copy missed rows from the layer's HBM mirror
+                                   of the host pool instead of the host pool */
+
+typedef struct hisparse_handle hisparse_handle;
+
+/* Sizes of one HiSparse instance ([DD] §5.7 --hisparse-config: top_k,
+ * device_buffer_size = B excluding the newest page). */
+typedef struct {
+  int32_t num_requests;     /* R: requests in the (graph-padded) decode batch, 1..8192 */
+  int32_t num_layers;       /* L: layers with a hot buffer, 1..4096 */
+  int32_t top_k;            /* k: selections per (request, layer, step), >= 1 */
+  int32_t buffer_slots;     /* B: LRU slots per (request, layer), k <= B <= 32767;
+                               row B of every hot buffer is the newest-token row */
+  int64_t host_rows;        /* P: logical positions (host rows) per (request, layer),
+                               1 <= P <= 2^31 - 1 */
+  int32_t record_bytes;     /* bytes of one position's KV in one layer; a positive
+                               multiple of 16 */
+  int32_t ctas_per_request; /* CTAs (one thread-block cluster) per request in
+                               resolve, 1..16; 0 = chosen by the library */
+  int32_t replay_ctas;      /* CTAs of the plan-replay kernel; 0 = chosen by the library */
+  const int32_t *anchor_of; /* [L] host array or NULL (= all -1): -1 if the layer runs
+                               RESOLVE itself, else the id of the anchor layer whose
+                               selection and slot table it shares ([DD] §3.6).  An
+                               anchor must itself have anchor_of == -1. */
+} hisparse_config;
+
+/* Memory of one layer.  The caller owns it and keeps it alive until
+ * hisparse_destroy.  Row (r, p) of the host pool is at
+ * host_pool + r*host_req_stride + p*host_row_stride; row (r, s) of the hot
+ * buffer, s in [0, B], is at hot + r*hot_req_stride + s*hot_row_stride.
+ * All pointers and strides must be multiples of 16 bytes, and row strides at
+ * least record_bytes. */
+typedef struct {
+  void *host_pool;          /* pinned, device-mapped host memory (hisparse_host_alloc or
+                               cudaHostAlloc / cudaHostRegister with mapping) */
+  int64_t host_req_stride;
+  int64_t host_row_stride;
+  void *hot;                /* device memory, R x (B+1) rows */
+  int64_t hot_req_stride;
+  int64_t hot_row_stride;
+  const void *mirror;       /* optional device copy of host_pool with the host pool's
+                               strides (used only with HISPARSE_FROM_MIRROR); NULL if none */
+} hisparse_layer_buffers;
+
+/* Read-only facts about an instance (for reporting). */
+typedef struct {
+  int32_t ctas_per_request; /* cluster size used by resolve */
+  int32_t threads_per_cta;
+  int32_t smem_bytes;       /* dynamic shared memory per resolve CTA */
+  int32_t hash_capacity;    /* open-addressing table entries per request */
+  int32_t replay_ctas;
+  int32_t sm_count;
+  int64_t metadata_bytes;   /* device bytes owned by the library */
+} hisparse_info;
+
+/* Create an instance.  Validates every size and buffer on the host, then
+ * allocates the library-owned metadata in device memory (slot -> position,
+ * LRU order, page table, miss plan, miss counts, error codes, status word;
+ * [DD] §5.2 tensor table) and resets every unit to its admission state: all
+ * slots empty, LRU order 0..B-1 ([DD] §5.4 request release).  Layers with
+ * anchor_of != -1 get no metadata of their own.  Synchronises the device.
+ * Errors: EINVAL, EBOUND, EROLE (bad anchor_of), ENOMEM, ECUDA. */
+int hisparse_init(const hisparse_config *cfg, const hisparse_layer_buffers *layers /* [L] */,
+                  hisparse_handle **out);
+
+/* Free the library-owned metadata (not the caller's buffers).  Synchronises. */
+int hisparse_destroy(hisparse_handle *h);
+
+/* RESOLVE one layer for requests [0, *d_num_reqs) in one launch ([DD] §3.5;
+ * [VD] "Hot lookup and LRU").  For request r:
+ *   d_sel[r*k + i]  int32 logical position, or -1 for padding;
+ *   d_newest[r]     int32 position of the newest token, bound to hot row B and
+ *                   never fetched, or -1 (d_newest may be NULL = all -1);
+ *   d_out[r*k + i]  int32 physical hot row for d_sel[r*k+i]: a slot in [0, B),
+ *                   B for the newest token, -1 for padding ([DD] §3.5 stage 5,
+ *                   top_k_device_locs aligned with the top-k order).
+ * d_num_reqs is a device int32 read by the kernel, so a graph captured at the
+ * padded batch size R serves any smaller batch ([DD] §5.5 num_real_reqs);
+ * NULL means R.  Requests at or beyond it are not touched.
+ * Replacement rule ([DD] §3.3, worked example §3.5): hits of this step become
+ * the most recent (in ascending slot order), this step's fetches come just
+ * before them (in selection-list order), and the j-th miss in list order takes
+ * the j-th least recent slot that is not a hit; empty slots are ordinary LRU
+ * entries.  On a device-detected input error (HISPARSE_ERR_*) the request's
+ * out row is all -1 and its state is unchanged.
+ * The host pool rows fetched must be complete when this runs (order any
+ * write-back before it with an event), and hot row B must already hold the
+ * newest token's KV.  flags: HISPARSE_RECORD_PLAN | HISPARSE_SKIP_IO |
+ * HISPARSE_FROM_MIRROR.  Errors: EINVAL, EROLE (layer is a follower), ECUDA. */
+int hisparse_resolve(hisparse_handle *h, int32_t layer, const int32_t *d_sel,
+                     const int32_t *d_num_reqs, const int32_t *d_newest, int32_t *d_out,
+                     uint32_t flags, void *stream);
+
+/* Write-through of the newest row ([DD] §3.4 step 4, §5.4 eager backup):
+ * for r < *d_num_reqs with d_pos[r] >= 0, copy hot row B of (layer, r) to
+ * host row d_pos[r] of (layer, r).  layer == -1 does every layer in one
+ * launch (d_pos is then [L][R]).  Positions >= P set HISPARSE_ERR_RANGE in
+ * the status word and are skipped.  Run it on a backup stream and make the
+ * compute stream wait on an event recorded after it before the next resolve
+ * that may fetch those rows, and before row B is overwritten.
+ * Errors: EINVAL, ECUDA. */
+int hisparse_writeback(hisparse_handle *h, int32_t layer, const int32_t *d_pos,
+                       const int32_t *d_num_reqs, void *stream);
+
+/* Exact prefetch for a shared-index layer ([DD] §3.6, §5.6): copy, for
+ * r < *d_num_reqs, every (position, slot) of the miss plan of the anchor's
+ * last resolve (empty unless that resolve had HISPARSE_RECORD_PLAN) from the
+ * follower's own host pool into the follower's hot buffer.  The
+ * follower's slots stay in lockstep with the anchor's, so the anchor's d_out
+ * rows are also the follower's.  Order it after the anchor's resolve (same
+ * stream or an event) and before the anchor's next resolve.
+ * Errors: EINVAL, EROLE, ECUDA. */
+int hisparse_prefetch_plan(hisparse_handle *h, int32_t anchor_layer, int32_t follower_layer,
+                           const int32_t *d_num_reqs, void *stream);
+
+/* Copy the per-request miss counts of one anchor layer's last resolve
+ * (int32 [R]) to device memory d_dst, asynchronously on `stream` (no
+ * synchronisation; graph-capturable).  Errors: EINVAL, EROLE, ECUDA. */
+int hisparse_copy_miss_counts(hisparse_handle *h, int32_t layer, int32_t *d_dst, void *stream);
+
+/* Read and clear the sticky status word (bit-OR of HISPARSE_ERR_*), and copy
+ * the per-unit codes of the last resolve ([L][R] int32, zero for followers)
+ * if unit_err_out is not NULL.  Synchronises the device: not for use inside
+ * a graph capture or a timed region. */
+int hisparse_get_status(hisparse_handle *h, uint32_t *flags_out, int32_t *unit_err_out);
+
+/* Copy one anchor layer's state to host arrays (any may be NULL):
+ * slot_pos [R][B] int32 (-1 empty), lru [R][B] int16 (least recent first),
+ * page_table [R][P] int32 (slot, or -1 = host only), miss_counts [R] int32
+ * (misses of the last resolve).  Synchronises.  Errors: EINVAL, EROLE, ECUDA. */
+int hisparse_export_state(hisparse_handle *h, int32_t layer, int32_t *slot_pos, int16_t *lru,
+                          int32_t *page_table, int32_t *miss_counts);
+
+/* Replace one anchor layer's state (checkpoint / test set-up).  The arrays
+ * are validated first: every slot_pos in [-1, P) with no position twice, lru
+ * a permutation of [0, B) per request, and page_table[p] == s exactly when
+ * slot_pos[s] == p.  Synchronises.  Errors: EINVAL, EROLE, ECUDA. */
+int hisparse_import_state(hisparse_handle *h, int32_t layer, const int32_t *slot_pos,
+                          const int16_t *lru, const int32_t *page_table);
+
+/* Copy one anchor layer's last miss plan to host arrays: count [R],
+ * pos [R][k] int32, slot [R][k] int32 (only the first count[r] entries of a
+ * row are meaningful).  Synchronises.  Errors: EINVAL, EROLE, ECUDA. */
+int hisparse_export_plan(hisparse_handle *h, int32_t layer, int32_t *count, int32_t *pos,
+                         int32_t *slot);
+
+/* Reset one anchor layer (or all layers with layer == -1) to the admission
+ * state: slots empty, LRU 0..B-1, page table all host-only ([DD] §5.4
+ * request release).  Asynchronous on `stream`.  Errors: EINVAL, EROLE, ECUDA. */
+int hisparse_reset(hisparse_handle *h, int32_t layer, void *stream);
+
+/* Fill `out` with facts about the instance. */
+int hisparse_get_info(const hisparse_handle *h, hisparse_info *out);
+
+/* Pinned, device-mapped, portable host memory for host pools (exact size, no
+ * rounding by a caching allocator).  Errors: EINVAL, ENOMEM. */
+int hisparse_host_alloc(size_t bytes, void **out);
+int hisparse_host_free(void *p);
+
+/* The cudaError_t of the last failed CUDA call made by this thread through
+ * the library (0 if none), and a static message for any return code. */
+int hisparse_last_cuda_error(void);
+const char *hisparse_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HISPARSE_H */

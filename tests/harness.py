@@ -1,0 +1,120 @@
+"""Run a workload on the CUDA path and on the oracle side by side (GPU tests).
+
+The GPU side goes only through the C ABI (``host_offload_serving_gb300``); the
+oracle side is the plain C model (``oracle.coracle``).  They share the seeded
+inputs from ``workload`` and nothing else.
+"""
+import numpy as np
+import torch
+
+from host_offload_serving_gb300 import hisparse as H
+from host_offload_serving_gb300.runtime import HiSparse, WorkloadMemory, DecodeStep
+from oracle.coracle import OracleLayer
+from workload import records as REC
+from workload.traces import all_traces
+
+
+class Run:
+    def __init__(self, w, flags=0, mirror=False, ctas_per_request=0, replay_ctas=0,
+                 num_reqs=None, oracle_bytes=True, traces=None):
+        self.w = w
+        self.flags = flags
+        dev = torch.device("cuda", 0)
+        self.mem = WorkloadMemory(w.R, w.L, w.B, w.P, w.rec, mirror=mirror)
+        REC.fill_host_pool(w, self.mem.pool.ptr, self.mem.layer_stride, self.mem.req_stride)
+        if mirror:
+            self.mem.fill_mirror()
+        self.hs = HiSparse(w.R, w.L, w.k, w.B, w.P, w.rec, self.mem.layer_buffers(),
+                           anchor_of=w.anchor_of(), ctas_per_request=ctas_per_request,
+                           replay_ctas=replay_ctas)
+        anchor_of = w.anchor_of()
+        self.groups = [(a, [l for l in range(w.L) if anchor_of[l] == a]) for a in w.anchors()]
+        tr = traces if traces is not None else all_traces(w)
+        self.sel_np = np.stack([tr[a][0] for a, _ in self.groups], axis=1)  # [T][G][R][k]
+        self.newest_np = tr[self.groups[0][0]][1] if w.write_through else None  # [T][R]
+        self.sel = torch.from_numpy(self.sel_np).to(dev)
+        self.newest = torch.from_numpy(self.newest_np).to(dev) if w.write_through else None
+        self.new_rows_np = REC.new_token_records(w)                       # [T][L][R][rec]
+        self.new_rows = torch.from_numpy(self.new_rows_np).to(dev) if w.write_through else None
+        if w.write_through:
+            wb = np.full((w.steps, w.L, w.R), -1, np.int32)
+            for t in range(1, w.steps):
+                wb[t] = self.newest_np[t - 1][None, :]
+            self.wb_np = wb
+            self.wb = torch.from_numpy(wb).to(dev)
+        self.out = torch.full((len(self.groups), w.R, w.k), -7, dtype=torch.int32, device=dev)
+        self.nreq_val = w.R if num_reqs is None else num_reqs
+        self.num_reqs = torch.tensor([self.nreq_val], dtype=torch.int32, device=dev)
+        self.step_runner = DecodeStep(self.hs, self.mem, self.groups, flags=flags,
+                                      num_reqs=self.num_reqs)
+        # oracle
+        self.oracle = {}
+        for l in range(w.L):
+            is_anchor = anchor_of[l] < 0
+            o = OracleLayer(w.R, w.k, w.B, w.P, w.rec, host=self.mem.host_view(l),
+                            host_split=w.L_ctx, keep_bytes=oracle_bytes, metadata=is_anchor)
+            if is_anchor:
+                o.reset()
+            self.oracle[l] = o
+        self.oracle_out = np.full((len(self.groups), w.R, w.k), -7, np.int32)
+        self.t = 0
+
+    # ------------------------------------------------------------------ #
+    def gpu_step(self, t):
+        self.step_runner.issue(self.sel[t], self.out,
+                               newest=self.newest[t] if self.newest is not None else None,
+                               wb_pos=self.wb[t] if (self.w.write_through and t > 0) else None,
+                               new_rows=self.new_rows[t] if self.new_rows is not None else None)
+
+    def oracle_step(self, t):
+        w = self.w
+        nr = self.nreq_val
+        io = not (self.flags & H.SKIP_IO)
+        if w.write_through:
+            for l in range(w.L):
+                if t > 0:
+                    self.oracle[l].writeback(self.wb_np[t, l], num_reqs=nr)
+                # the model writes row B of every (padded) row, like the GPU side
+                self.oracle[l].set_newest_rows(self.new_rows_np[t, l])
+        for gi, (a, fl) in enumerate(self.groups):
+            nw = self.newest_np[t] if self.newest_np is not None else None
+            out, _ = self.oracle[a].resolve(self.sel_np[t, gi], nw, num_reqs=nr, io=io)
+            self.oracle_out[gi, :nr] = out[:nr]
+            for f in fl:
+                self.oracle[a].replay_into(self.oracle[f], num_reqs=nr)
+
+    def step(self):
+        self.gpu_step(self.t)
+        self.oracle_step(self.t)
+        self.t += 1
+
+    # ------------------------------------------------------------------ #
+    def compare(self, check_bytes=True, check_page_table=True):
+        """Assert GPU == oracle on every field of every layer (synchronises)."""
+        torch.cuda.synchronize()
+        w = self.w
+        nr = self.nreq_val
+        out = self.out.cpu().numpy()
+        np.testing.assert_array_equal(out[:, :nr], self.oracle_out[:, :nr], err_msg="out slots")
+        for a, fl in self.groups:
+            sp, lru, pt, mc = self.hs.export_state(a)
+            o = self.oracle[a]
+            np.testing.assert_array_equal(sp, o.slot_pos, err_msg=f"slot_pos layer {a}")
+            np.testing.assert_array_equal(lru, o.lru, err_msg=f"lru layer {a}")
+            np.testing.assert_array_equal(mc[:nr], o.miss_count[:nr], err_msg=f"miss count {a}")
+            if check_page_table:
+                np.testing.assert_array_equal(pt, o.page_table, err_msg=f"page table {a}")
+        if check_bytes:
+            hot = self.mem.hot.cpu().numpy()
+            for l in range(w.L):
+                np.testing.assert_array_equal(hot[l], self.oracle[l].hot, err_msg=f"hot bytes {l}")
+                if w.P > w.L_ctx:
+                    tail = self.mem.host_view(l)[:, w.L_ctx:, :]
+                    np.testing.assert_array_equal(tail, self.oracle[l].host_tail,
+                                                  err_msg=f"host tail {l}")
+        flags, ue = self.hs.status()
+        assert flags == 0, f"status flags {flags}"
+
+    def close(self):
+        self.hs.close()
+        self.mem.close()

@@ -1,0 +1,253 @@
+"""CUDA path == oracle, bit for bit, through the C ABI (needs a GB300)."""
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+from host_offload_serving_gb300 import hisparse as H
+from host_offload_serving_gb300.runtime import HiSparse, WorkloadMemory
+from oracle.coracle import OracleLayer
+from workload import get, sweep_workload
+import pins
+
+pytestmark = pytest.mark.gpu
+
+
+def _instance(R, k, B, P, rec=16, ctas=0, fill=None):
+    mem = WorkloadMemory(R, 1, B, P, rec)
+    host = mem.host_view(0)
+    if fill is None:
+        host[:] = np.random.default_rng(R * 1000 + k).integers(0, 256, size=host.shape, dtype=np.uint8)
+    hs = HiSparse(R, 1, k, B, P, rec, mem.layer_buffers(), ctas_per_request=ctas)
+    return mem, hs
+
+
+def _dev(a, dtype=torch.int32):
+    return torch.from_numpy(np.ascontiguousarray(a)).to("cuda").to(dtype)
+
+
+# ---------------------------------------------------------------------- #
+def test_worked_example_b():
+    """gentlecold.top deep dive §3.5 worked example, preset through import."""
+    g = dict(pins.parse_golden("example_b_resolve.txt"))
+    B, k, P = int(g["B"]), int(g["k"]), 64
+    mem, hs = _instance(1, k, B, P)
+    sp = np.array([pins._ints(g["slot_pos"])], np.int32)
+    lru = np.array([pins._ints(g["lru"])], np.int16)
+    pt = np.full((1, P), -1, np.int32)
+    for s, p in enumerate(sp[0]):
+        pt[0, p] = s
+    assert hs.import_state(0, sp, lru, pt) == 0
+    sel = _dev(np.array([pins._ints(g["sel"])], np.int32))
+    newest = _dev(np.array([int(g["newest"])], np.int32))
+    out = torch.empty((1, k), dtype=torch.int32, device="cuda")
+    hs.resolve(0, sel, out, newest=newest, flags=H.RECORD_PLAN)
+    torch.cuda.synchronize()
+    assert out.cpu().numpy()[0].tolist() == pins._ints(g["expect_out"])
+    sp2, lru2, pt2, mc = hs.export_state(0)
+    assert lru2[0].tolist() == pins._ints(g["expect_lru"])
+    assert sp2[0].tolist() == pins._ints(g["expect_slot_pos"])
+    assert mc[0] == int(g["expect_misses"])
+    c, pp, ps = hs.export_plan(0)
+    assert c[0] == 1 and (pp[0, 0], ps[0, 0]) == (25, 0)
+    assert pt2[0, 25] == 0 and pt2[0, 10] == -1 and pt2[0, 12] == 2
+    host = mem.host_view(0)
+    assert (mem.hot[0, 0, 0].cpu().numpy() == host[0, 25]).all()
+    hs.close(); mem.close()
+
+
+def test_worked_example_a():
+    """notes.kuangjux.top §5: misses 3,1,1 at capacity 3 and 3,1,0 at capacity 4."""
+    rows = pins.parse_golden("example_a_capacity.txt")
+    steps = [pins._ints(v) for key, v in rows if key == "step"]
+    for cap, exp in ((3, [3, 1, 1]), (4, [3, 1, 0])):
+        mem, hs = _instance(1, 3, cap, 16)
+        out = torch.empty((1, 3), dtype=torch.int32, device="cuda")
+        got = []
+        for s in steps:
+            hs.resolve(0, _dev(np.array([s], np.int32)), out)
+            got.append(int(hs.export_state(0)[3][0]))
+        assert got == exp
+        hs.close(); mem.close()
+
+
+# ---------------------------------------------------------------------- #
+def _enumerate_lists(k, P):
+    """Every selection list of length k over positions [0, P) with -1 padding."""
+    out = []
+    for m in range(k + 1):
+        for vals in itertools.permutations(range(P), m):
+            for slots in itertools.combinations(range(k), m):
+                row = [-1] * k
+                for s, v in zip(slots, vals):
+                    row[s] = v
+                out.append(row)
+    return out
+
+
+@pytest.mark.parametrize("k,P,steps,extra", [(2, 4, 3, (0, 1, 2)), (3, 5, 2, (0, 1)),
+                                              (1, 4, 4, (0, 1, 2))])
+def test_exhaustive_tiny(k, P, steps, extra):
+    """All selection sequences of a tiny domain, one sequence per request."""
+    lists = _enumerate_lists(k, P)
+    seqs = list(itertools.product(range(len(lists)), repeat=steps))
+    for B in (k + e for e in extra):
+        for start in range(0, len(seqs), 8192):
+            chunk = seqs[start:start + 8192]
+            R = len(chunk)
+            sel = np.array([[lists[i] for i in s] for s in chunk], np.int32)  # [R][T][k]
+            sel = np.ascontiguousarray(sel.transpose(1, 0, 2))               # [T][R][k]
+            newest = np.where(np.arange(R) % 3 == 0, P - 1, -1).astype(np.int32)
+            mem, hs = _instance(R, k, B, P)
+            host = mem.host_view(0)
+            o = OracleLayer(R, k, B, P, 16, host=host)
+            o.reset()
+            out = torch.empty((R, k), dtype=torch.int32, device="cuda")
+            dnew = _dev(newest)
+            for t in range(steps):
+                hs.resolve(0, _dev(sel[t]), out, newest=dnew)
+                oo, e = o.resolve(sel[t], newest)
+                assert e == 0
+                np.testing.assert_array_equal(out.cpu().numpy(), oo)
+            sp, lru, pt, mc = hs.export_state(0)
+            np.testing.assert_array_equal(sp, o.slot_pos)
+            np.testing.assert_array_equal(lru, o.lru)
+            np.testing.assert_array_equal(pt, o.page_table)
+            np.testing.assert_array_equal(mc, o.miss_count)
+            np.testing.assert_array_equal(mem.hot[0].cpu().numpy()[:, :B], o.hot[:, :B])
+            hs.close(); mem.close()
+
+
+# ---------------------------------------------------------------------- #
+from harness import Run  # noqa: E402
+
+
+def _run_all(w, every=1, **kw):
+    run = Run(w, **kw)
+    try:
+        for t in range(w.steps):
+            run.step()
+            if t % every == 0 or t == w.steps - 1:
+                run.compare()
+    finally:
+        run.close()
+
+
+def test_tiny_workload_every_step():
+    _run_all(get("tiny"))
+
+
+def test_dsa_workload_full_size_every_step():
+    """8 requests x 4 layers, 128K context, k=2048, B=4096, write-through."""
+    _run_all(get("dsa"))
+
+
+def test_quest_workload_scaled():
+    """Page granularity with 32 KB records (fewer requests/layers/pages)."""
+    _run_all(get("quest").scaled(R=4, groups=2, L_ctx=2048, steps=12))
+
+
+def test_shared_workload_scaled():
+    """Anchor + 3 shared layers replaying the plan (fewer requests, shorter context)."""
+    _run_all(get("shared").scaled(R=6, groups=2, L_ctx=16384, steps=10))
+
+
+@pytest.mark.parametrize("B", [2048, 4096, 8192])
+def test_sweep_workload_scaled(B):
+    _run_all(sweep_workload(B, 0.70, L_ctx=65536).scaled(R=4, steps=6))
+
+
+@pytest.mark.parametrize("cs", [1, 2, 3, 4, 8, 16])
+def test_cluster_sizes_identical(cs):
+    _run_all(get("dsa").scaled(R=3, groups=1, L_ctx=16384, steps=5), ctas_per_request=cs)
+
+
+def test_skip_io_metadata_identical_bytes_stale():
+    _run_all(get("dsa").scaled(R=2, groups=2, L_ctx=8192, steps=5), flags=H.SKIP_IO)
+
+
+def test_from_mirror_bytes_identical():
+    _run_all(get("quest").scaled(R=2, groups=1, L_ctx=1024, steps=5), flags=H.FROM_MIRROR,
+             mirror=True)
+
+
+def test_num_reqs_padding_leaves_tail_untouched():
+    _run_all(get("dsa").scaled(R=5, groups=1, L_ctx=8192, steps=4), num_reqs=3)
+
+
+# ---------------------------------------------------------------------- #
+def test_device_detected_errors_keep_state():
+    R, k, B, P = 4, 4, 6, 32
+    mem, hs = _instance(R, k, B, P)
+    out = torch.empty((R, k), dtype=torch.int32, device="cuda")
+    good = np.array([[1, 2, 3, -1]] * R, np.int32)
+    hs.resolve(0, _dev(good), out)
+    before = hs.export_state(0)
+    bad = np.array([[4, 4, 5, -1],      # duplicate
+                    [4, 32, 5, -1],     # out of range
+                    [4, -9, 5, -1],     # out of range
+                    [7, 8, 9, 10]], np.int32)
+    hs.resolve(0, _dev(bad), out)
+    o = out.cpu().numpy()
+    assert (o[:3] == -1).all() and (o[3] >= 0).all()
+    flags, ue = hs.status()
+    assert flags == (H.ERR_DUP | H.ERR_RANGE)
+    assert ue[0].tolist() == [H.ERR_DUP, H.ERR_RANGE, H.ERR_RANGE, 0]
+    after = hs.export_state(0)
+    for r in range(3):
+        for a, b in zip(before[:3], after[:3]):      # slot_pos, lru, page table
+            np.testing.assert_array_equal(a[r], b[r])
+    assert after[3][:3].tolist() == [0, 0, 0]        # nothing fetched for failed units
+    assert hs.status()[0] == 0     # reading clears the word
+    newest = _dev(np.array([40, -1, -1, -1], np.int32))
+    hs.resolve(0, _dev(good), out, newest=newest)
+    assert hs.status()[0] == H.ERR_RANGE
+    hs.close(); mem.close()
+
+
+def test_import_rejects_inconsistent_state():
+    mem, hs = _instance(1, 2, 4, 16)
+    sp = np.array([[3, -1, 5, -1]], np.int32)
+    lru = np.array([[0, 1, 2, 3]], np.int16)
+    pt = np.full((1, 16), -1, np.int32)
+    pt[0, 3], pt[0, 5] = 0, 2
+    assert hs.import_state(0, sp, lru, pt) == 0
+    pt[0, 5] = 1
+    assert hs.import_state(0, sp, lru, pt) == H.EINVAL
+    pt[0, 5] = 2
+    assert hs.import_state(0, sp, np.array([[0, 1, 1, 3]], np.int16), pt) == H.EINVAL
+    hs.close(); mem.close()
+
+
+def test_cuda_graph_replay_equals_eager():
+    w = get("dsa").scaled(R=3, groups=2, L_ctx=16384, steps=6)
+    eager = Run(w)
+    graph = Run(w)
+    try:
+        for t in range(w.steps):
+            eager.step()
+        torch.cuda.synchronize()
+        # capture each step once, then replay it
+        g_list = []
+        s = torch.cuda.Stream()
+        for t in range(w.steps):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(s):
+                with torch.cuda.graph(g, stream=s):
+                    graph.gpu_step(t)
+            g_list.append(g)
+        torch.cuda.synchronize()
+        graph.hs.reset()
+        graph.mem.hot.zero_()
+        torch.cuda.synchronize()
+        for t in range(w.steps):
+            g_list[t].replay()
+            graph.oracle_step(t)
+        graph.compare()
+        for a, _ in eager.groups:
+            for x, y in zip(eager.hs.export_state(a), graph.hs.export_state(a)):
+                np.testing.assert_array_equal(x, y)
+    finally:
+        eager.close()
+        graph.close()

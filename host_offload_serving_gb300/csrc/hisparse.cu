@@ -27,13 +27,18 @@
 //   * No spin-waits: the only cross-CTA waits are hardware cluster barriers,
 //     and hash probing is bounded by the table size.
 #include <cuda_runtime.h>
+#include <sys/mman.h>
 
 #include <algorithm>
 #include <climits>
+#include <cstdio>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <map>
+#include <mutex>
 #include <new>
+#include <thread>
 #include <vector>
 
 #include "hisparse.h"
@@ -53,8 +58,10 @@ thread_local int g_last_cuda_error = 0;
 // Shared-memory layout of a resolve CTA (identical on host and device).
 // ---------------------------------------------------------------------------
 struct SmemLayout {
-  uint32_t key, val, sel, out, slotpos, hit, lru, newlru, missidx, victim, misc, total;
+  uint32_t key, val, sel, out, slotpos, hit, lru, newlru, missidx, victim, bkt, misc, total;
 };
+
+constexpr int kMaxBuckets = 2048;   // host-row buckets used to order the fetches
 
 __host__ __device__ inline uint32_t align16(uint32_t x) { return (x + 15u) & ~15u; }
 
@@ -71,6 +78,7 @@ __host__ __device__ inline SmemLayout smem_layout(int k, int B, int cap) {
   L.newlru = o;  o += align16(2u * B);
   L.missidx = o; o += align16(2u * k);
   L.victim = o;  o += align16(2u * k);
+  L.bkt = o;     o += align16(4u * kMaxBuckets);
   L.misc = o;    o += align16(4u * (8 + 3 * kWarps));
   L.total = o;
   return L;
@@ -84,6 +92,8 @@ enum { kMiscErr = 0, kMiscM = 1 };
 // ---------------------------------------------------------------------------
 struct ResolveArgs {
   int32_t R, k, B, cap_log2, rec16, io;
+  int32_t vec;                 // 1: sel, slot_pos and lru rows are 16-byte aligned
+  int32_t bucket_shift, nbuckets;
   int64_t P;
   const int32_t *sel, *num_reqs, *newest;
   int32_t *out;
@@ -194,13 +204,41 @@ __device__ __forceinline__ uint32_t hash_pos(int32_t p, int cap_log2) {
   return (static_cast<uint32_t>(p) * 2654435761u) >> (32 - cap_log2);
 }
 
+// Exclusive prefix sum of a[0..n), n <= 2 * kThreads, in place (all threads).
+__device__ __forceinline__ void block_exclusive_scan(int32_t *a, int n, int32_t *warp_tot) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int i0 = 2 * tid;
+  const int v0 = i0 < n ? a[i0] : 0, v1 = i0 + 1 < n ? a[i0 + 1] : 0;
+  const int sum = v0 + v1;
+  int inc = sum;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int t = __shfl_up_sync(kFull, inc, d);
+    if (lane >= d) inc += t;
+  }
+  if (lane == 31) warp_tot[warp] = inc;
+  __syncthreads();
+  const int wt = warp_tot[lane];
+  int winc = wt;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int t = __shfl_up_sync(kFull, winc, d);
+    if (lane >= d) winc += t;
+  }
+  const int excl = __shfl_sync(kFull, winc - wt, warp) + inc - sum;
+  __syncthreads();
+  if (i0 < n) a[i0] = excl;
+  if (i0 + 1 < n) a[i0 + 1] = excl + v0;
+  __syncthreads();
+}
+
 // ---------------------------------------------------------------------------
 // Leader CTA: stages 1, 2, 3 and 5 for request r.  On return (after a block
 // barrier) misc[kMiscM] holds the number of misses M and, for j < M,
 // fpos[j] / fslot[j] hold the position and victim slot of miss j.
 // ---------------------------------------------------------------------------
 template <bool kRecordPlan>
-__device__ void leader_resolve(const ResolveArgs &a, int r, unsigned char *smem,
+__device__ bool leader_resolve(const ResolveArgs &a, int r, unsigned char *smem,
                                const SmemLayout &L) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k = a.k, B = a.B, cap = 1 << a.cap_log2;
@@ -220,19 +258,39 @@ __device__ void leader_resolve(const ResolveArgs &a, int r, unsigned char *smem,
   int32_t *s_fpos = s_key;                                   // reused after stage 2
   int16_t *s_fslot = s_val;
 
-  const int32_t newest = a.newest ? a.newest[r] : -1;
   const int32_t *g_sel = a.sel + static_cast<int64_t>(r) * k;
   int32_t *g_slotpos = a.slot_pos + static_cast<int64_t>(r) * B;
   int16_t *g_lru = a.lru + static_cast<int64_t>(r) * B;
   int32_t *g_pt = a.page_table + static_cast<int64_t>(r) * P;
 
-  // ---- stage 0: load the unit's inputs, clear the hash table ----
-  for (int i = tid; i < cap; i += kThreads) s_key[i] = -1;
-  for (int i = tid; i < k; i += kThreads) s_sel[i] = g_sel[i];
-  for (int s = tid; s < B; s += kThreads) {
-    s_slotpos[s] = g_slotpos[s];
-    s_lru[s] = g_lru[s];
+  // ---- stage 0: issue every global load of the unit at once (one memory
+  //      round trip), then stage them in shared memory ----
+  const int nreq = a.num_reqs ? min(*a.num_reqs, a.R) : a.R;
+  const int32_t newest = a.newest ? a.newest[r] : -1;
+  constexpr int kV = 2;  // 16-byte vectors per thread and array in the batched path
+  int4 vs[kV], vp[kV];
+  uint4 vl[kV];
+  const int nk4 = a.vec ? k / 4 : 0, nb4 = a.vec ? B / 4 : 0, nb8 = a.vec ? B / 8 : 0;
+#pragma unroll
+  for (int u = 0; u < kV; ++u) {
+    const int i = tid + u * kThreads;
+    if (i < nk4) vs[u] = reinterpret_cast<const int4 *>(g_sel)[i];
+    if (i < nb4) vp[u] = reinterpret_cast<const int4 *>(g_slotpos)[i];
+    if (i < nb8) vl[u] = reinterpret_cast<const uint4 *>(g_lru)[i];
   }
+  if (r >= nreq) return false;  // graph padding: the whole cluster leaves together
+  for (int i = tid; i < cap; i += kThreads) s_key[i] = -1;
+#pragma unroll
+  for (int u = 0; u < kV; ++u) {
+    const int i = tid + u * kThreads;
+    if (i < nk4) reinterpret_cast<int4 *>(s_sel)[i] = vs[u];
+    if (i < nb4) reinterpret_cast<int4 *>(s_slotpos)[i] = vp[u];
+    if (i < nb8) reinterpret_cast<uint4 *>(s_lru)[i] = vl[u];
+  }
+  // whatever the batched path did not cover (unaligned rows or large k, B)
+  for (int i = 4 * min(nk4, kV * kThreads) + tid; i < k; i += kThreads) s_sel[i] = g_sel[i];
+  for (int s = 4 * min(nb4, kV * kThreads) + tid; s < B; s += kThreads) s_slotpos[s] = g_slotpos[s];
+  for (int s = 8 * min(nb8, kV * kThreads) + tid; s < B; s += kThreads) s_lru[s] = g_lru[s];
   if (tid == 0) s_misc[kMiscErr] = (newest < -1 || newest >= P) ? HISPARSE_ERR_RANGE : 0u;
   __syncthreads();
 
@@ -275,7 +333,7 @@ __device__ void leader_resolve(const ResolveArgs &a, int r, unsigned char *smem,
       s_misc[kMiscM] = 0;
     }
     __syncthreads();
-    return;
+    return true;
   }
 
   // ---- stage 2: mark each slot hit or evictable ----
@@ -368,7 +426,7 @@ __device__ void leader_resolve(const ResolveArgs &a, int r, unsigned char *smem,
   }
   __syncthreads();
 
-  // ---- stage 5 (metadata half): victims, page table, slot map, plan ----
+  // ---- stage 5 (metadata half): victims, page table, slot map ----
   for (int j = tid; j < M; j += kThreads) {
     const int i = s_missidx[j];
     const int16_t v = s_victim[j];
@@ -380,10 +438,6 @@ __device__ void leader_resolve(const ResolveArgs &a, int r, unsigned char *smem,
     g_slotpos[v] = p;
     s_fpos[j] = p;
     s_fslot[j] = v;
-    if (kRecordPlan) {
-      a.plan_pos[static_cast<int64_t>(r) * k + j] = p;
-      a.plan_slot[static_cast<int64_t>(r) * k + j] = v;
-    }
   }
   if (tid == 0) {
     s_misc[kMiscM] = static_cast<uint32_t>(M);
@@ -394,6 +448,49 @@ __device__ void leader_resolve(const ResolveArgs &a, int r, unsigned char *smem,
   __syncthreads();
   for (int i = tid; i < k; i += kThreads) a.out[static_cast<int64_t>(r) * k + i] = s_out[i];
   for (int s = tid; s < B; s += kThreads) g_lru[s] = s_newlru[s];
+
+  // ---- fetch order: misses sorted by host row ----
+  // Which slot a miss lands in is fixed above; the order in which the records
+  // are read is free.  Reading them in ascending host-row order lets records
+  // touched at the same time share GPU page-table walks, which on a large
+  // pinned pool costs far less than selection order.  Counting sort into
+  // buckets of 2^bucket_shift rows, then each entry's rank inside its bucket.
+  if (M > 1) {
+    int32_t *s_bkt = reinterpret_cast<int32_t *>(smem + L.bkt);
+    int32_t *s_bpos = s_key + cap / 2;   // cap >= 2k: second half is free
+    int16_t *s_bslot = s_val + cap / 2;
+    const int sh = a.bucket_shift, nb = a.nbuckets;
+    for (int b = tid; b < nb; b += kThreads) s_bkt[b] = 0;
+    __syncthreads();
+    for (int j = tid; j < M; j += kThreads) atomicAdd(&s_bkt[s_fpos[j] >> sh], 1);
+    __syncthreads();
+    block_exclusive_scan(s_bkt, nb, s_cnt);
+    for (int j = tid; j < M; j += kThreads) {
+      const int32_t p = s_fpos[j];
+      const int q = atomicAdd(&s_bkt[p >> sh], 1);
+      s_bpos[q] = p;
+      s_bslot[q] = s_fslot[j];
+    }
+    __syncthreads();
+    // now s_bkt[b] is the end of bucket b (and the start of bucket b + 1)
+    for (int q = tid; q < M; q += kThreads) {
+      const int32_t p = s_bpos[q];
+      const int b = p >> sh;
+      const int b0 = b ? s_bkt[b - 1] : 0, b1 = s_bkt[b];
+      int rnk = 0;
+      for (int x = b0; x < b1; ++x) rnk += s_bpos[x] < p;
+      s_fpos[b0 + rnk] = p;
+      s_fslot[b0 + rnk] = s_bslot[q];
+    }
+    __syncthreads();
+  }
+  if (kRecordPlan) {  // the plan lists the same fetches, in the same order
+    for (int j = tid; j < M; j += kThreads) {
+      a.plan_pos[static_cast<int64_t>(r) * k + j] = s_fpos[j];
+      a.plan_slot[static_cast<int64_t>(r) * k + j] = s_fslot[j];
+    }
+  }
+  return true;
 }
 
 // ---------------------------------------------------------------------------
@@ -405,15 +502,19 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
   const uint32_t cs = cluster_nctarank();
   const uint32_t rank = cluster_ctarank();
   const int r = static_cast<int>(blockIdx.x / cs);
-  const int nreq = a.num_reqs ? min(*a.num_reqs, a.R) : a.R;
-  if (r >= nreq) return;  // graph padding: the whole cluster leaves together
-
   const SmemLayout L = smem_layout(a.k, a.B, 1 << a.cap_log2);
   int32_t *s_fpos = reinterpret_cast<int32_t *>(smem + L.key);
   int16_t *s_fslot = reinterpret_cast<int16_t *>(smem + L.val);
   uint32_t *s_misc = reinterpret_cast<uint32_t *>(smem + L.misc);
 
-  if (rank == 0) leader_resolve<kRecordPlan>(a, r, smem, L);
+  // Requests at or beyond *num_reqs are graph padding: every CTA of the
+  // cluster sees the same count and leaves before any cluster barrier.
+  if (rank == 0) {
+    if (!leader_resolve<kRecordPlan>(a, r, smem, L)) return;
+  } else {
+    const int nreq = a.num_reqs ? min(*a.num_reqs, a.R) : a.R;
+    if (r >= nreq) return;
+  }
   cluster_arrive_release();
   cluster_wait_acquire();
 
@@ -575,6 +676,7 @@ struct hisparse_handle {
   uint32_t smem;
   std::vector<int32_t> anchor_of;
   std::vector<LayerDev> layers;
+  std::vector<int32_t> bucket_shift, nbuckets;  // per layer: fetch-order buckets
   std::vector<AnchorMeta> meta;
   LayerDev *d_layers = nullptr;
   uint32_t *d_status = nullptr;
@@ -649,6 +751,33 @@ int configure_resolve(hisparse_handle *h, int want_cs) {
   return HISPARSE_OK;
 }
 
+// Host pools allocated by hisparse_host_alloc through cudaHostRegister.
+std::mutex g_host_mu;
+std::map<void *, size_t> g_host_regs;
+
+// Size of a transparent huge page (0 if the kernel does not say).
+size_t thp_bytes() {
+  FILE *f = std::fopen("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size", "r");
+  if (!f) return 0;
+  unsigned long long v = 0;
+  if (std::fscanf(f, "%llu", &v) != 1) v = 0;
+  std::fclose(f);
+  return static_cast<size_t>(v);
+}
+
+// Zero-fill with a few threads so the pages are populated after the advice.
+void first_touch(void *p, size_t bytes) {
+  const unsigned n = std::max(1u, std::min(16u, std::thread::hardware_concurrency()));
+  std::vector<std::thread> th;
+  const size_t chunk = (bytes / n + 4095) & ~size_t(4095);
+  for (unsigned i = 0; i < n; ++i) {
+    const size_t b = std::min(bytes, i * chunk), e = std::min(bytes, b + chunk);
+    if (b >= e) break;
+    th.emplace_back([=] { std::memset(static_cast<char *>(p) + b, 0, e - b); });
+  }
+  for (auto &t : th) t.join();
+}
+
 }  // namespace
 
 extern "C" {
@@ -670,6 +799,28 @@ const char *hisparse_strerror(int code) {
 int hisparse_host_alloc(size_t bytes, void **out) {
   if (!out || bytes == 0) return HISPARSE_EINVAL;
   *out = nullptr;
+  // Large pools: transparent-huge-page backed memory registered with the GPU.
+  // The GPU then maps the pool with large pages, so random record fetches
+  // miss its address-translation caches far less often than with
+  // cudaHostAlloc's base-page mappings.
+  const size_t hp = thp_bytes();
+  if (hp && bytes >= hp) {
+    const size_t sz = (bytes + hp - 1) / hp * hp;
+    void *p = nullptr;
+    if (posix_memalign(&p, hp, sz) == 0) {
+      madvise(p, sz, MADV_HUGEPAGE);  // advice only: a refusal still leaves valid memory
+      first_touch(p, sz);
+      cudaError_t e = cudaHostRegister(p, sz, cudaHostRegisterMapped | cudaHostRegisterPortable);
+      if (e == cudaSuccess) {
+        std::lock_guard<std::mutex> lk(g_host_mu);
+        g_host_regs[p] = sz;
+        *out = p;
+        return HISPARSE_OK;
+      }
+      cudaGetLastError();
+      free(p);
+    }
+  }
   cudaError_t e = cudaHostAlloc(out, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
   if (e != cudaSuccess) {
     g_last_cuda_error = static_cast<int>(e);
@@ -682,6 +833,20 @@ int hisparse_host_alloc(size_t bytes, void **out) {
 
 int hisparse_host_free(void *p) {
   if (!p) return HISPARSE_EINVAL;
+  bool registered = false;
+  {
+    std::lock_guard<std::mutex> lk(g_host_mu);
+    auto it = g_host_regs.find(p);
+    if (it != g_host_regs.end()) {
+      registered = true;
+      g_host_regs.erase(it);
+    }
+  }
+  if (registered) {
+    HS_CUDA(cudaHostUnregister(p));
+    free(p);
+    return HISPARSE_OK;
+  }
   HS_CUDA(cudaFreeHost(p));
   return HISPARSE_OK;
 }
@@ -760,6 +925,18 @@ int hisparse_init(const hisparse_config *cfg, const hisparse_layer_buffers *laye
     d.hot_req_stride = b.hot_req_stride;
     d.hot_row_stride = b.hot_row_stride;
     d.mirror = static_cast<const char *>(b.mirror);
+  }
+
+  // Fetch-order buckets: about 2 MB of host rows each, at most kMaxBuckets.
+  h->bucket_shift.resize(L);
+  h->nbuckets.resize(L);
+  for (int l = 0; l < L; ++l) {
+    const int64_t rows = std::max<int64_t>(1, (int64_t(2) << 20) / layers[l].host_row_stride);
+    int sh = 0;
+    while ((int64_t(1) << (sh + 1)) <= rows) ++sh;
+    while (((P - 1) >> sh) + 1 > kMaxBuckets) ++sh;
+    h->bucket_shift[l] = sh;
+    h->nbuckets[l] = static_cast<int32_t>(((P - 1) >> sh) + 1);
   }
 
   rc = configure_resolve(h, cfg->ctas_per_request);
@@ -861,6 +1038,9 @@ int hisparse_resolve(hisparse_handle *h, int32_t layer, const int32_t *d_sel,
   ResolveArgs a;
   a.R = h->R; a.k = h->k; a.B = h->B; a.cap_log2 = h->cap_log2; a.rec16 = h->rec / 16;
   a.io = (flags & HISPARSE_SKIP_IO) ? 0 : 1;
+  a.vec = (h->k % 4 == 0 && h->B % 8 == 0 && (reinterpret_cast<uintptr_t>(d_sel) & 15u) == 0) ? 1 : 0;
+  a.bucket_shift = h->bucket_shift[layer];
+  a.nbuckets = h->nbuckets[layer];
   a.P = h->P;
   a.sel = d_sel; a.num_reqs = d_num_reqs; a.newest = d_newest; a.out = d_out;
   a.slot_pos = m.slot_pos; a.lru = m.lru; a.page_table = m.page_table;

@@ -146,7 +146,10 @@ int hisparse_destroy(hisparse_handle *h);
  * the most recent (in ascending slot order), this step's fetches come just
  * before them (in selection-list order), and the j-th miss in list order takes
  * the j-th least recent slot that is not a hit; empty slots are ordinary LRU
- * entries.  On a device-detected input error (HISPARSE_ERR_*) the request's
+ * entries.  Missed records are read from the host pool in ascending position
+ * order (which slot each one lands in is fixed by the rule above; reading them
+ * in address order lets neighbouring fetches share the GPU's page-table
+ * walks).  On a device-detected input error (HISPARSE_ERR_*) the request's
  * out row is all -1 and its state is unchanged.
  * The host pool rows fetched must be complete when this runs (order any
  * write-back before it with an event), and hot row B must already hold the
@@ -205,7 +208,10 @@ int hisparse_import_state(hisparse_handle *h, int32_t layer, const int32_t *slot
 
 /* Copy one anchor layer's last miss plan to host arrays: count [R],
  * pos [R][k] int32, slot [R][k] int32 (only the first count[r] entries of a
- * row are meaningful).  Synchronises.  Errors: EINVAL, EROLE, ECUDA. */
+ * row are meaningful).  Entries are the (position, slot) pairs fetched by the
+ * last resolve, in ascending position order -- the order the fetches were
+ * issued in (see hisparse_resolve).  Synchronises.
+ * Errors: EINVAL, EROLE, ECUDA. */
 int hisparse_export_plan(hisparse_handle *h, int32_t layer, int32_t *count, int32_t *pos,
                          int32_t *slot);
 
@@ -217,8 +223,14 @@ int hisparse_reset(hisparse_handle *h, int32_t layer, void *stream);
 /* Fill `out` with facts about the instance. */
 int hisparse_get_info(const hisparse_handle *h, hisparse_info *out);
 
-/* Pinned, device-mapped, portable host memory for host pools (exact size, no
- * rounding by a caching allocator).  Errors: EINVAL, ENOMEM. */
+/* Pinned, device-mapped, portable host memory for host pools.  A request of
+ * at least one transparent huge page is served by huge-page-advised memory
+ * registered with cudaHostRegister (zero-filled, size rounded up to whole huge
+ * pages internally): the GPU then translates the pool with large pages, and
+ * random record fetches stall far less on address translation than they do
+ * on cudaHostAlloc memory.  Smaller requests, or a refused registration, fall
+ * back to cudaHostAlloc (contents unspecified).  Free with hisparse_host_free.
+ * Errors: EINVAL, ENOMEM. */
 int hisparse_host_alloc(size_t bytes, void **out);
 int hisparse_host_free(void *p);
 

@@ -104,6 +104,14 @@ class Run:
             np.testing.assert_array_equal(mc[:nr], o.miss_count[:nr], err_msg=f"miss count {a}")
             if check_page_table:
                 np.testing.assert_array_equal(pt, o.page_table, err_msg=f"page table {a}")
+            if fl:  # the recorded plan: the same (pos, slot) fetches, by position
+                c, pp, ps = self.hs.export_plan(a)
+                for r in range(nr):
+                    got = sorted(zip(pp[r, :c[r]].tolist(), ps[r, :c[r]].tolist()))
+                    exp = sorted(zip(o.plan_pos[r, :o.plan_count[r]].tolist(),
+                                     o.plan_slot[r, :o.plan_count[r]].tolist()))
+                    assert got == exp, f"plan of layer {a} request {r}"
+                    assert [p for p, _ in zip(pp[r, :c[r]], ps[r])] == sorted(pp[r, :c[r]].tolist())
         if check_bytes:
             hot = self.mem.hot.cpu().numpy()
             for l in range(w.L):

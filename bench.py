@@ -42,6 +42,7 @@ def parse():
     ap.add_argument("--workload", default="dsa")
     ap.add_argument("--ctas", type=int, default=0, help="CTAs per request in resolve (0 = auto)")
     ap.add_argument("--replay-ctas", type=int, default=0)
+    ap.add_argument("--lookup", type=int, default=0, help="0 = page table (default), 1 = hash")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-allhit", action="store_true")
@@ -237,8 +238,9 @@ def run_ours(args):
     mem = WorkloadMemory(w.R, w.L, w.B, w.P, w.rec)
     REC.fill_host_pool(w, mem.pool.ptr, mem.layer_stride, mem.req_stride)
     hs = HiSparse(w.R, w.L, w.k, w.B, w.P, w.rec, mem.layer_buffers(), anchor_of=w.anchor_of(),
-                  ctas_per_request=args.ctas, replay_ctas=args.replay_ctas)
+                  ctas_per_request=args.ctas, replay_ctas=args.replay_ctas, lookup=args.lookup)
     info = hs.info()
+    hp_frac = mem.pool.hugepage_fraction()
     anchor_of = w.anchor_of()
     groups = [(a, [l for l in range(w.L) if anchor_of[l] == a]) for a in w.anchors()]
     G = len(groups)
@@ -381,6 +383,8 @@ def run_ours(args):
         res_flat = [x / G for x in step_ms]
         timing_note = "step graph time / anchors (includes write-back and row copy)"
     resolve_avg_ms = sum(res_flat) / len(res_flat)
+    srt = sorted(res_flat)
+    pct = lambda q: srt[min(len(srt) - 1, int(q * (len(srt) - 1) + 0.5))] * 1e3
     miss_bytes = int(miss.sum()) * w.rec
     fetch_gbs = miss_bytes / (sum(res_flat) / 1e3) / 1e9
     miss_rate = float(miss.sum()) / (args.steps * G * w.R * w.k)
@@ -497,7 +501,9 @@ def run_ours(args):
             "kernel": "resolve_kernel",
             "peak_source": "pinned cudaMemcpyAsync H2D, 1 GiB x 20, same run",
             "algorithmic_bytes_per_launch": miss_bytes / (args.steps * G),
-            "avg_launch_us": round(resolve_avg_ms * 1e3, 2), "timing": timing_note}
+            "avg_launch_us": round(resolve_avg_ms * 1e3, 2), "timing": timing_note,
+            "launch_us_p50_p90_p99_max": [round(pct(0.5), 2), round(pct(0.9), 2),
+                                          round(pct(0.99), 2), round(srt[-1] * 1e3, 2)]}
     if allhit:
         allhit["hbm_peak_gbs"] = peaks.get("hbm_gbs")
         allhit["hbm_frac"] = round(allhit["hbm_gbs"] / peaks.get("hbm_gbs"), 5)
@@ -522,7 +528,9 @@ def run_ours(args):
                        "top_k": w.k, "B": w.B, "L_ctx": w.L_ctx, "record_bytes": w.rec,
                        "write_through": w.write_through, "parallelism": f"replicas{world}",
                        "l2": "flushed (256 MB write) before every timed step",
-                       "ctas_per_request": info["ctas_per_request"]},
+                       "ctas_per_request": info["ctas_per_request"],
+                       "lookup": ["page_table", "hash"][info["lookup"]],
+                       "host_pool_hugepage_fraction": round(hp_frac, 3)},
             "roofline": roof,
             "miss_fetch_gbs": round(fetch_gbs, 2), "h2d_link_gbs": round(h2d_gbs, 2),
             "miss_rate": round(miss_rate, 4),

@@ -564,6 +564,485 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
   cluster_wait_acquire();  // the leader's memory must outlive every reader
 }
 
+// ===========================================================================
+// RESOLVE, page-table lookup (the default).  One cluster per request.
+//   workers (CTAs 1..cs-1, or CTA 0 alone when cs == 1) each take a slice of
+//     the selection list, classify every entry through the page table (padding,
+//     newest token, hit, miss), mark hit slots in a bitmap, list their misses
+//     in list order, and -- without waiting for any decision -- start reading
+//     the missed records from the host pool into registers;
+//   the leader (CTA 0) merges the slices through distributed shared memory,
+//     checks duplicates, runs the two order-stable compactions (hit slots in
+//     slot order; evictable slots in LRU order) that give every miss its
+//     victim and the new LRU order, and releases the workers, which store the
+//     staged records into their victims while the leader publishes the page
+//     table, slot map, LRU order and plan.
+// The reads from host memory thus overlap the leader's decision instead of
+// following it.  Results are identical to the hash-staged kernel above.
+// ===========================================================================
+constexpr int kStage = 4;        // 16-byte chunks a worker thread stages in registers
+constexpr int kMaxWorkers = 15;  // cluster size 16 at most
+constexpr int kGroup = 4;        // selections a worker thread classifies per load batch
+
+struct PtLayout {
+  uint32_t w_sel, w_out, w_mi, w_mp, w_hit, w_vict, w_misc, w_bkt, w_bidx, w_ord;  // worker
+  uint32_t l_lru, l_slotpos, l_hit, l_newlru, l_ev, l_mpos, l_hkey, l_misc;     // leader
+  uint32_t cnt, total;
+};
+
+__host__ __device__ inline PtLayout pt_layout(int k, int B, int ks, int hcap) {
+  PtLayout L;
+  uint32_t o = 0;
+  const uint32_t nwords = (B + 31) / 32;
+  L.w_sel = o;     o += align16(4u * ks);
+  L.w_out = o;     o += align16(4u * ks);
+  L.w_mi = o;      o += align16(4u * ks);
+  L.w_mp = o;      o += align16(4u * ks);
+  L.w_hit = o;     o += align16(4u * nwords);
+  L.w_vict = o;    o += align16(4u * ks);
+  L.w_misc = o;    o += align16(4u * 8);
+  L.w_bkt = o;     o += align16(4u * kMaxBuckets);
+  L.w_bidx = o;    o += align16(4u * ks);
+  L.w_ord = o;     o += align16(4u * ks);
+  L.l_lru = o;     o += align16(2u * B);
+  L.l_slotpos = o; o += align16(4u * B);
+  L.l_hit = o;     o += align16(4u * nwords);
+  L.l_newlru = o;  o += align16(2u * B);
+  L.l_ev = o;      o += align16(4u * k);
+  L.l_mpos = o;    o += align16(4u * k);
+  L.l_hkey = o;    o += align16(4u * hcap);
+  L.l_misc = o;    o += align16(4u * (8 + kMaxWorkers + 1));
+  L.cnt = o;       o += align16(4u * 32);
+  L.total = o;
+  return L;
+}
+
+// worker misc words / leader misc words
+enum { kWErr = 0, kWNewest = 1, kWCount = 2 };
+enum { kLErr = 0, kLM = 1, kLHits = 2, kLPrefix = 8 };
+
+struct PtArgs {
+  int32_t R, k, B, rec16, io, ks, hcap_log2;
+  int32_t bucket_shift, nbuckets;  // host-row buckets for the fetch order
+  int64_t P;
+  const int32_t *sel, *num_reqs, *newest;
+  int32_t *out;
+  int32_t *slot_pos;
+  int16_t *lru;
+  int32_t *page_table, *miss_count, *unit_err;
+  uint32_t *status;
+  int32_t *plan_pos, *plan_slot, *plan_count;
+  const char *src;
+  int64_t src_req_stride, src_row_stride;
+  char *hot;
+  int64_t hot_req_stride, hot_row_stride;
+};
+
+// Stable block-wide compaction of [0, n): emit(i, rank) for every i with
+// flag(i), rank = number of flagged elements before i.  Each warp scans one
+// contiguous segment with __ballot_sync/__popc; one barrier publishes the 32
+// warp totals, which every warp prefix-sums with shuffles.  Returns the count.
+template <class Flag, class Emit>
+__device__ __forceinline__ int block_compact(int n, Flag flag, Emit emit, int32_t *s_cnt) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int seg = ((n + kWarps * 32 - 1) / (kWarps * 32)) * 32;
+  const int i0 = warp * seg, i1 = min(n, i0 + seg);
+  int c = 0;
+  for (int b = i0; b < i1; b += 32) {
+    const int i = b + lane;
+    c += __popc(__ballot_sync(kFull, i < i1 && flag(i)));
+  }
+  if (lane == 0) s_cnt[warp] = c;
+  __syncthreads();
+  const int v = s_cnt[lane];
+  int inc = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int t = __shfl_up_sync(kFull, inc, d);
+    if (lane >= d) inc += t;
+  }
+  const int total = __shfl_sync(kFull, inc, 31);
+  int base = __shfl_sync(kFull, inc - v, warp);
+  const uint32_t lt = lanemask_lt();
+  for (int b = i0; b < i1; b += 32) {
+    const int i = b + lane;
+    const bool f = i < i1 && flag(i);
+    const uint32_t m = __ballot_sync(kFull, f);
+    if (f) emit(i, base + __popc(m & lt));
+    base += __popc(m);
+  }
+  __syncthreads();
+  return total;
+}
+
+__device__ __forceinline__ bool bit_of(const uint32_t *bits, int s) {
+  return (bits[s >> 5] >> (s & 31)) & 1u;
+}
+
+// Worker: classify selections [i0, i0 + n) of request r.
+__device__ void pt_worker_classify(const PtArgs &a, int r, int i0, int n, int32_t newest,
+                                   unsigned char *smem, const PtLayout &L) {
+  const int tid = threadIdx.x;
+  const int B = a.B;
+  const int64_t P = a.P;
+  int32_t *w_sel = reinterpret_cast<int32_t *>(smem + L.w_sel);
+  int32_t *w_out = reinterpret_cast<int32_t *>(smem + L.w_out);
+  int32_t *w_mi = reinterpret_cast<int32_t *>(smem + L.w_mi);
+  int32_t *w_mp = reinterpret_cast<int32_t *>(smem + L.w_mp);
+  uint32_t *w_hit = reinterpret_cast<uint32_t *>(smem + L.w_hit);
+  uint32_t *w_misc = reinterpret_cast<uint32_t *>(smem + L.w_misc);
+  int32_t *s_cnt = reinterpret_cast<int32_t *>(smem + L.cnt);
+  const int nwords = (B + 31) / 32;
+  for (int x = tid; x < nwords; x += kThreads) w_hit[x] = 0;
+  if (tid < 8) w_misc[tid] = 0;
+  __syncthreads();
+  const int32_t *g_sel = a.sel + static_cast<int64_t>(r) * a.k + i0;
+  const int32_t *g_pt = a.page_table + static_cast<int64_t>(r) * P;
+  for (int base = 0; base < n; base += kGroup * kThreads) {
+    int32_t p[kGroup], s[kGroup];
+#pragma unroll
+    for (int u = 0; u < kGroup; ++u) {
+      const int t = base + u * kThreads + tid;
+      p[u] = t < n ? g_sel[t] : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < kGroup; ++u) {
+      s[u] = -1;
+      if (p[u] >= 0 && p[u] < P && p[u] != newest) s[u] = g_pt[p[u]];
+    }
+#pragma unroll
+    for (int u = 0; u < kGroup; ++u) {
+      const int t = base + u * kThreads + tid;
+      if (t >= n) continue;
+      int32_t v;
+      if (p[u] == -1) {
+        v = -1;
+      } else if (p[u] < -1 || p[u] >= P) {
+        atomicOr(&w_misc[kWErr], HISPARSE_ERR_RANGE);
+        v = -1;
+      } else if (p[u] == newest) {
+        atomicAdd(&w_misc[kWNewest], 1u);
+        v = B;
+      } else if (s[u] >= 0) {
+        if (s[u] >= B) {  // a page-table entry outside [-1, B): treat the unit as failed
+          atomicOr(&w_misc[kWErr], HISPARSE_ERR_RANGE);
+          v = -1;
+        } else {
+          const uint32_t bit = 1u << (s[u] & 31);
+          if (atomicOr(&w_hit[s[u] >> 5], bit) & bit) atomicOr(&w_misc[kWErr], HISPARSE_ERR_DUP);
+          v = s[u];
+        }
+      } else {
+        v = kUnresolved;
+      }
+      w_sel[t] = p[u];
+      w_out[t] = v;
+    }
+  }
+  __syncthreads();
+  const int mw = block_compact(
+      n, [&](int t) { return w_out[t] == kUnresolved; },
+      [&](int t, int j) {
+        w_mi[j] = t;
+        w_mp[j] = w_sel[t];
+      },
+      s_cnt);
+  if (tid == 0) w_misc[kWCount] = static_cast<uint32_t>(mw);
+  // Fetch order: the slice's misses by ascending host row.  Which slot each
+  // lands in does not depend on it; reading in address order lets nearby
+  // records share the GPU's page-table walks, which matters whenever the pool
+  // is not mapped with large pages.
+  int32_t *w_ord = reinterpret_cast<int32_t *>(smem + L.w_ord);
+  if (mw > 1) {
+    int32_t *w_bkt = reinterpret_cast<int32_t *>(smem + L.w_bkt);
+    int32_t *w_bidx = reinterpret_cast<int32_t *>(smem + L.w_bidx);
+    const int sh = a.bucket_shift, nb = a.nbuckets;
+    for (int b = tid; b < nb; b += kThreads) w_bkt[b] = 0;
+    __syncthreads();
+    for (int j = tid; j < mw; j += kThreads) atomicAdd(&w_bkt[w_mp[j] >> sh], 1);
+    __syncthreads();
+    block_exclusive_scan(w_bkt, nb, s_cnt);
+    for (int j = tid; j < mw; j += kThreads) w_bidx[atomicAdd(&w_bkt[w_mp[j] >> sh], 1)] = j;
+    __syncthreads();
+    // now w_bkt[b] ends bucket b; rank each entry inside its bucket
+    for (int q = tid; q < mw; q += kThreads) {
+      const int j = w_bidx[q];
+      const int32_t p = w_mp[j];
+      const int b = p >> sh;
+      const int b0 = b ? w_bkt[b - 1] : 0, b1 = w_bkt[b];
+      int rnk = 0;
+      for (int x = b0; x < b1; ++x) rnk += w_mp[w_bidx[x]] < p;
+      w_ord[b0 + rnk] = j;
+    }
+  } else if (tid == 0) {
+    w_ord[0] = 0;
+  }
+  __syncthreads();
+}
+
+// Leader: merge the workers' slices, check duplicates, choose victims and the
+// new LRU order.  Returns nothing; results live in the leader's shared memory.
+__device__ void pt_leader_decide(const PtArgs &a, int cs, int nw, int32_t newest,
+                                 unsigned char *smem, const PtLayout &L) {
+  const int tid = threadIdx.x;
+  const int B = a.B;
+  const int nwords = (B + 31) / 32;
+  const int hcap = 1 << a.hcap_log2;
+  int16_t *l_lru = reinterpret_cast<int16_t *>(smem + L.l_lru);
+  uint32_t *l_hit = reinterpret_cast<uint32_t *>(smem + L.l_hit);
+  int16_t *l_newlru = reinterpret_cast<int16_t *>(smem + L.l_newlru);
+  int32_t *l_ev = reinterpret_cast<int32_t *>(smem + L.l_ev);
+  int32_t *l_mpos = reinterpret_cast<int32_t *>(smem + L.l_mpos);
+  int32_t *l_hkey = reinterpret_cast<int32_t *>(smem + L.l_hkey);
+  uint32_t *l_misc = reinterpret_cast<uint32_t *>(smem + L.l_misc);
+  int32_t *s_cnt = reinterpret_cast<int32_t *>(smem + L.cnt);
+  const uint32_t *w_misc0 = reinterpret_cast<const uint32_t *>(smem + L.w_misc);
+  const uint32_t *w_hit0 = reinterpret_cast<const uint32_t *>(smem + L.w_hit);
+  const int32_t *w_mp0 = reinterpret_cast<const int32_t *>(smem + L.w_mp);
+  auto wrank = [&](int w) { return static_cast<uint32_t>(cs == 1 ? 0 : w + 1); };
+
+  // per-worker counts -> prefix offsets in list order; error bits
+  if (tid == 0) {
+    uint32_t err = (newest < -1 || newest >= a.P) ? HISPARSE_ERR_RANGE : 0u;
+    uint32_t newest_seen = 0;
+    int pre = 0;
+    for (int w = 0; w < nw; ++w) {
+      err |= ld_dsmem_u32(dsmem_addr(&w_misc0[kWErr], wrank(w)));
+      newest_seen += ld_dsmem_u32(dsmem_addr(&w_misc0[kWNewest], wrank(w)));
+      l_misc[kLPrefix + w] = static_cast<uint32_t>(pre);
+      pre += static_cast<int>(ld_dsmem_u32(dsmem_addr(&w_misc0[kWCount], wrank(w))));
+    }
+    if (newest_seen > 1) err |= HISPARSE_ERR_DUP;
+    l_misc[kLPrefix + nw] = static_cast<uint32_t>(pre);
+    l_misc[kLErr] = err;
+    l_misc[kLM] = static_cast<uint32_t>(pre);
+    l_misc[kLHits] = 0;
+  }
+  __syncthreads();
+  // hit bitmap: OR of the slices; a slot hit by two slices is a duplicate
+  {
+    uint32_t dup = 0, hits = 0;
+    for (int x = tid; x < nwords; x += kThreads) {
+      uint32_t acc = 0;
+      for (int w = 0; w < nw; ++w) {
+        const uint32_t b = ld_dsmem_u32(dsmem_addr(&w_hit0[x], wrank(w)));
+        dup |= acc & b;
+        acc |= b;
+      }
+      l_hit[x] = acc;
+      hits += __popc(acc);
+    }
+    if (dup) atomicOr(&l_misc[kLErr], HISPARSE_ERR_DUP);
+    if (hits) atomicAdd(&l_misc[kLHits], hits);
+  }
+  // miss positions in list order; duplicates among misses via an
+  // open-addressing set ([DD] §3.5 stage 1's multiplicative hash)
+  for (int w = 0; w < nw; ++w) {
+    const int pre = static_cast<int>(l_misc[kLPrefix + w]);
+    const int mw = static_cast<int>(l_misc[kLPrefix + w + 1]) - pre;
+    for (int j = tid; j < mw; j += kThreads) {
+      const int32_t p = static_cast<int32_t>(ld_dsmem_u32(dsmem_addr(&w_mp0[j], wrank(w))));
+      l_mpos[pre + j] = p;
+      uint32_t h = hash_pos(p, a.hcap_log2);
+      for (int probe = 0; probe < hcap; ++probe) {
+        const int32_t prev = atomicCAS(&l_hkey[h], -1, p);
+        if (prev == -1) break;
+        if (prev == p) {
+          atomicOr(&l_misc[kLErr], HISPARSE_ERR_DUP);
+          break;
+        }
+        h = (h + 1) & (hcap - 1);
+      }
+    }
+  }
+  __syncthreads();
+  if (l_misc[kLErr]) return;  // uniform
+  const int M = static_cast<int>(l_misc[kLM]);
+  const int H = static_cast<int>(l_misc[kLHits]);
+  const int E = B - H;
+  // hits, newest last, in ascending slot order
+  block_compact(
+      B, [&](int s) { return bit_of(l_hit, s); },
+      [&](int s, int h) { l_newlru[E + h] = static_cast<int16_t>(s); }, s_cnt);
+  // evictables in LRU order: the j-th goes to the j-th miss; the rest stay oldest
+  block_compact(
+      B, [&](int j) { return !bit_of(l_hit, l_lru[j]); },
+      [&](int j, int e) {
+        const int16_t sl = l_lru[j];
+        if (e < M) l_ev[e] = sl;
+        l_newlru[e >= M ? e - M : E - M + e] = sl;
+      },
+      s_cnt);
+}
+
+// Leader: publish page table, slot map, LRU order, counts, plan.
+template <bool kRecordPlan>
+__device__ void pt_leader_publish(const PtArgs &a, int r, unsigned char *smem, const PtLayout &L) {
+  const int tid = threadIdx.x;
+  const int B = a.B, k = a.k;
+  const int64_t P = a.P;
+  const int32_t *l_slotpos = reinterpret_cast<const int32_t *>(smem + L.l_slotpos);
+  const int16_t *l_newlru = reinterpret_cast<const int16_t *>(smem + L.l_newlru);
+  const int32_t *l_ev = reinterpret_cast<const int32_t *>(smem + L.l_ev);
+  const int32_t *l_mpos = reinterpret_cast<const int32_t *>(smem + L.l_mpos);
+  const uint32_t *l_misc = reinterpret_cast<const uint32_t *>(smem + L.l_misc);
+  const uint32_t err = l_misc[kLErr];
+  if (err) {
+    if (tid == 0) {
+      a.unit_err[r] = static_cast<int32_t>(err);
+      atomicOr(a.status, err);
+      a.miss_count[r] = 0;
+      a.plan_count[r] = 0;
+    }
+    return;
+  }
+  const int M = static_cast<int>(l_misc[kLM]);
+  int32_t *g_pt = a.page_table + static_cast<int64_t>(r) * P;
+  int32_t *g_slotpos = a.slot_pos + static_cast<int64_t>(r) * B;
+  for (int g = tid; g < M; g += kThreads) {
+    const int32_t v = l_ev[g], p = l_mpos[g], old = l_slotpos[v];
+    if (old >= 0) g_pt[old] = -1;
+    g_pt[p] = v;
+    g_slotpos[v] = p;
+    if (kRecordPlan) {
+      a.plan_pos[static_cast<int64_t>(r) * k + g] = p;
+      a.plan_slot[static_cast<int64_t>(r) * k + g] = v;
+    }
+  }
+  int16_t *g_lru = a.lru + static_cast<int64_t>(r) * B;
+  for (int s = tid; s < B; s += kThreads) g_lru[s] = l_newlru[s];
+  if (tid == 0) {
+    a.miss_count[r] = M;
+    a.unit_err[r] = 0;
+    a.plan_count[r] = kRecordPlan ? M : 0;
+  }
+}
+
+template <bool kRecordPlan>
+__global__ void __launch_bounds__(kThreads, 1) resolve_pt_kernel(const PtArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int cs = static_cast<int>(cluster_nctarank());
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int r = static_cast<int>(blockIdx.x) / cs;
+  const int tid = threadIdx.x;
+  const int nw = cs == 1 ? 1 : cs - 1;
+  const bool leader = rank == 0;
+  const bool worker = cs == 1 || rank > 0;
+  const int w = cs == 1 ? 0 : rank - 1;
+  const PtLayout L = pt_layout(a.k, a.B, a.ks, 1 << a.hcap_log2);
+  const int nreq = a.num_reqs ? min(*a.num_reqs, a.R) : a.R;
+  if (r >= nreq) return;  // graph padding: every CTA of the cluster leaves
+  const int32_t newest = a.newest ? a.newest[r] : -1;
+
+  if (leader) {  // the unit's LRU order and slot map, and an empty duplicate set
+    int16_t *l_lru = reinterpret_cast<int16_t *>(smem + L.l_lru);
+    int32_t *l_slotpos = reinterpret_cast<int32_t *>(smem + L.l_slotpos);
+    int32_t *l_hkey = reinterpret_cast<int32_t *>(smem + L.l_hkey);
+    const int16_t *g_lru = a.lru + static_cast<int64_t>(r) * a.B;
+    const int32_t *g_slotpos = a.slot_pos + static_cast<int64_t>(r) * a.B;
+    for (int s = tid; s < a.B; s += kThreads) {
+      l_lru[s] = g_lru[s];
+      l_slotpos[s] = g_slotpos[s];
+    }
+    for (int i = tid; i < (1 << a.hcap_log2); i += kThreads) l_hkey[i] = -1;
+  }
+  const int i0 = w * a.ks;
+  const int n = worker ? max(0, min(a.k, i0 + a.ks) - i0) : 0;
+  if (worker) pt_worker_classify(a, r, i0, n, newest, smem, L);
+  cluster_arrive_release();  // #0: slices ready for the leader
+
+  // Workers read their misses' records into registers now, before any victim
+  // is known (cs == 1: one CTA does everything in order, nothing staged).
+  const int32_t *w_mp = reinterpret_cast<const int32_t *>(smem + L.w_mp);
+  const int32_t *w_ord = reinterpret_cast<const int32_t *>(smem + L.w_ord);
+  const uint32_t *w_misc = reinterpret_cast<const uint32_t *>(smem + L.w_misc);
+  const int mw = worker ? static_cast<int>(w_misc[kWCount]) : 0;
+  const int64_t totc = static_cast<int64_t>(mw) * a.rec16;
+  const char *src = a.src + static_cast<int64_t>(r) * a.src_req_stride;
+  char *dst = a.hot + static_cast<int64_t>(r) * a.hot_req_stride;
+  const bool stage = worker && cs > 1 && a.io;
+  uint4 v[kStage];
+#pragma unroll
+  for (int u = 0; u < kStage; ++u) {
+    const int64_t q = tid + static_cast<int64_t>(u) * kThreads;
+    if (stage && q < totc) {
+      const uint32_t q32 = static_cast<uint32_t>(q);
+      const int f = static_cast<int>(q32 / static_cast<uint32_t>(a.rec16));
+      const int o = static_cast<int>(q32 - static_cast<uint32_t>(f) * a.rec16);
+      v[u] = ld_nc_v4(src + static_cast<int64_t>(w_mp[w_ord[f]]) * a.src_row_stride + 16 * o);
+    }
+  }
+  cluster_wait_acquire();
+
+  if (leader) pt_leader_decide(a, cs, nw, newest, smem, L);
+  cluster_arrive_release();  // #1: decision ready for the workers
+  if (leader) pt_leader_publish<kRecordPlan>(a, r, smem, L);
+  cluster_wait_acquire();
+
+  if (worker) {
+    const uint32_t *l_misc = reinterpret_cast<const uint32_t *>(smem + L.l_misc);
+    const int32_t *l_ev = reinterpret_cast<const int32_t *>(smem + L.l_ev);
+    int32_t *w_vict = reinterpret_cast<int32_t *>(smem + L.w_vict);
+    const int32_t *w_out = reinterpret_cast<const int32_t *>(smem + L.w_out);
+    const int32_t *w_mi = reinterpret_cast<const int32_t *>(smem + L.w_mi);
+    const uint32_t err = ld_dsmem_u32(dsmem_addr(&l_misc[kLErr], 0));
+    if (!err) {
+      const int pre = static_cast<int>(ld_dsmem_u32(dsmem_addr(&l_misc[kLPrefix + w], 0)));
+      const uint32_t ev0 = dsmem_addr(l_ev, 0);
+      for (int j = tid; j < mw; j += kThreads)
+        w_vict[j] = static_cast<int32_t>(ld_dsmem_u32(ev0 + 4u * static_cast<uint32_t>(pre + j)));
+    }
+    __syncthreads();
+    cluster_arrive_relaxed();  // #2: done with the leader's memory
+    if (!err && a.io) {
+      // the staged chunks, then whatever did not fit in registers
+#pragma unroll
+      for (int u = 0; u < kStage; ++u) {
+        const int64_t q = tid + static_cast<int64_t>(u) * kThreads;
+        if (stage && q < totc) {
+          const uint32_t q32 = static_cast<uint32_t>(q);
+          const int f = static_cast<int>(q32 / static_cast<uint32_t>(a.rec16));
+          const int o = static_cast<int>(q32 - static_cast<uint32_t>(f) * a.rec16);
+          st_v4(dst + static_cast<int64_t>(w_vict[w_ord[f]]) * a.hot_row_stride + 16 * o, v[u]);
+        }
+      }
+      const int64_t start = stage ? static_cast<int64_t>(kStage) * kThreads : 0;
+      for (int64_t b0 = start + tid; b0 < totc; b0 += static_cast<int64_t>(kThreads) * kUnroll) {
+        uint4 x[kUnroll];
+        char *d[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          const int64_t q = b0 + static_cast<int64_t>(u) * kThreads;
+          d[u] = nullptr;
+          if (q < totc) {
+            const uint32_t q32 = static_cast<uint32_t>(q);
+            const int f = static_cast<int>(q32 / static_cast<uint32_t>(a.rec16));
+            const int o = static_cast<int>(q32 - static_cast<uint32_t>(f) * a.rec16);
+            const int j = w_ord[f];
+            x[u] = ld_nc_v4(src + static_cast<int64_t>(w_mp[j]) * a.src_row_stride + 16 * o);
+            d[u] = dst + static_cast<int64_t>(w_vict[j]) * a.hot_row_stride + 16 * o;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+          if (d[u]) st_v4(d[u], x[u]);
+      }
+    }
+    // the slice's slot vector ([DD] §3.5 stage 5: aligned with the list)
+    int32_t *g_out = a.out + static_cast<int64_t>(r) * a.k + i0;
+    for (int t = tid; t < n; t += kThreads) {
+      const int32_t val = w_out[t];
+      if (err) g_out[t] = -1;
+      else if (val != kUnresolved) g_out[t] = val;
+    }
+    if (!err)
+      for (int j = tid; j < mw; j += kThreads) g_out[w_mi[j]] = w_vict[j];
+  } else {
+    cluster_arrive_relaxed();
+  }
+  cluster_wait_acquire();  // the leader's memory outlives every reader
+}
+
 // ---------------------------------------------------------------------------
 // Write-through: grid (R, layers); copies hot row B to host row pos.
 // ---------------------------------------------------------------------------
@@ -672,7 +1151,7 @@ struct AnchorMeta {
 struct hisparse_handle {
   int32_t R, L, k, B, rec;
   int64_t P;
-  int32_t cs, cap_log2, replay_ctas, sm_count, device;
+  int32_t cs, cap_log2, replay_ctas, sm_count, device, lookup, ks;
   uint32_t smem;
   std::vector<int32_t> anchor_of;
   std::vector<LayerDev> layers;
@@ -704,21 +1183,40 @@ int layer_ok(const hisparse_handle *h, int32_t layer) {
   return HISPARSE_OK;
 }
 
+int slice_size(int k, int cs) {
+  const int nw = cs == 1 ? 1 : cs - 1;
+  return (k + nw - 1) / nw;
+}
+
+uint32_t resolve_smem(const hisparse_handle *h, int cs) {
+  if (h->lookup == HISPARSE_LOOKUP_HASH) return smem_layout(h->k, h->B, 1 << h->cap_log2).total;
+  return pt_layout(h->k, h->B, slice_size(h->k, cs), 1 << h->cap_log2).total;
+}
+
+// Choose the cluster size: as many CTAs per request as the GPU can run at once
+// for the whole batch (one wave), at most 16.
 int configure_resolve(hisparse_handle *h, int want_cs) {
-  const SmemLayout L = smem_layout(h->k, h->B, 1 << h->cap_log2);
-  h->smem = L.total;
-  if (L.total > 227u * 1024u) return HISPARSE_EBOUND;
-  const void *fns[2] = {reinterpret_cast<const void *>(&resolve_kernel<false>),
-                        reinterpret_cast<const void *>(&resolve_kernel<true>)};
+  const bool hash = h->lookup == HISPARSE_LOOKUP_HASH;
+  const void *fns[2];
+  if (hash) {
+    fns[0] = reinterpret_cast<const void *>(&resolve_kernel<false>);
+    fns[1] = reinterpret_cast<const void *>(&resolve_kernel<true>);
+  } else {
+    fns[0] = reinterpret_cast<const void *>(&resolve_pt_kernel<false>);
+    fns[1] = reinterpret_cast<const void *>(&resolve_pt_kernel<true>);
+  }
+  uint32_t smax = 0;
+  for (int cs = 1; cs <= 16; ++cs) smax = std::max(smax, resolve_smem(h, cs));
+  if (smax > 227u * 1024u) return HISPARSE_EBOUND;
   for (const void *f : fns) {
-    HS_CUDA(cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total));
+    HS_CUDA(cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smax));
     HS_CUDA(cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
   }
   auto active_clusters = [&](int cs) -> int {
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(static_cast<unsigned>(cs) * h->R);
     lc.blockDim = dim3(kThreads);
-    lc.dynamicSmemBytes = L.total;
+    lc.dynamicSmemBytes = resolve_smem(h, cs);
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = cs;
@@ -727,33 +1225,36 @@ int configure_resolve(hisparse_handle *h, int want_cs) {
     lc.attrs = at;
     lc.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void *>(&resolve_kernel<true>), &lc) !=
-        cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, fns[1], &lc) != cudaSuccess) {
       cudaGetLastError();
       return 0;
     }
     return n;
   };
+  int cs = 1;
   if (want_cs > 0) {
     if (want_cs > 16) return HISPARSE_EBOUND;
     if (active_clusters(want_cs) < 1) return HISPARSE_EBOUND;
-    h->cs = want_cs;
-    return HISPARSE_OK;
-  }
-  h->cs = 1;
-  for (int cs = 16; cs >= 2; cs >>= 1) {
-    if (cs * h->R > h->sm_count) continue;
-    if (active_clusters(cs) >= h->R) {
-      h->cs = cs;
-      break;
+    cs = want_cs;
+  } else {
+    for (int c = std::min(16, h->sm_count / h->R); c >= 2; --c) {
+      if (active_clusters(c) >= h->R) {
+        cs = c;
+        break;
+      }
     }
   }
+  h->cs = cs;
+  h->smem = resolve_smem(h, cs);
+  h->ks = slice_size(h->k, cs);
   return HISPARSE_OK;
 }
 
 // Host pools allocated by hisparse_host_alloc through cudaHostRegister.
 std::mutex g_host_mu;
 std::map<void *, size_t> g_host_regs;
+
+constexpr int kMadvCollapse = 25;  // Linux MADV_COLLAPSE (6.1+); ignored where unknown
 
 // Size of a transparent huge page (0 if the kernel does not say).
 size_t thp_bytes() {
@@ -810,6 +1311,7 @@ int hisparse_host_alloc(size_t bytes, void **out) {
     if (posix_memalign(&p, hp, sz) == 0) {
       madvise(p, sz, MADV_HUGEPAGE);  // advice only: a refusal still leaves valid memory
       first_touch(p, sz);
+      madvise(p, sz, kMadvCollapse);  // ask for huge pages now where the first touch got none
       cudaError_t e = cudaHostRegister(p, sz, cudaHostRegisterMapped | cudaHostRegisterPortable);
       if (e == cudaSuccess) {
         std::lock_guard<std::mutex> lk(g_host_mu);
@@ -828,6 +1330,28 @@ int hisparse_host_alloc(size_t bytes, void **out) {
     *out = nullptr;
     return HISPARSE_ENOMEM;
   }
+  return HISPARSE_OK;
+}
+
+int hisparse_host_hugepage_bytes(const void *p, size_t bytes, size_t *huge_out) {
+  if (!p || !huge_out) return HISPARSE_EINVAL;
+  *huge_out = 0;
+  FILE *f = std::fopen("/proc/self/smaps", "r");
+  if (!f) return HISPARSE_EINVAL;
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(p), hi = lo + bytes;
+  char line[512];
+  bool in = false;
+  unsigned long long a = 0, b = 0, kb = 0;
+  while (std::fgets(line, sizeof line, f)) {
+    if (std::sscanf(line, "%llx-%llx", &a, &b) == 2 && std::strchr(line, '-') &&
+        std::strchr(line, ' ') > std::strchr(line, '-')) {
+      in = a < hi && b > lo;  // a mapping that overlaps the range
+      continue;
+    }
+    if (in && std::sscanf(line, "AnonHugePages: %llu kB", &kb) == 1) *huge_out += kb * 1024ull;
+  }
+  std::fclose(f);
+  if (*huge_out > bytes) *huge_out = bytes;
   return HISPARSE_OK;
 }
 
@@ -865,6 +1389,8 @@ int hisparse_init(const hisparse_config *cfg, const hisparse_layer_buffers *laye
   if (static_cast<int64_t>(R) * k * (rec / 16) >= (int64_t(1) << 31)) return HISPARSE_EBOUND;
   if (cfg->ctas_per_request < 0 || cfg->ctas_per_request > 16 || cfg->replay_ctas < 0)
     return HISPARSE_EBOUND;
+  if (cfg->lookup != HISPARSE_LOOKUP_PAGE_TABLE && cfg->lookup != HISPARSE_LOOKUP_HASH)
+    return HISPARSE_EINVAL;
   std::vector<int32_t> anchor(L, -1);
   if (cfg->anchor_of) {
     for (int l = 0; l < L; ++l) anchor[l] = cfg->anchor_of[l];
@@ -890,6 +1416,7 @@ int hisparse_init(const hisparse_config *cfg, const hisparse_layer_buffers *laye
   hisparse_handle *h = new (std::nothrow) hisparse_handle();
   if (!h) return HISPARSE_ENOMEM;
   h->R = R; h->L = L; h->k = k; h->B = B; h->P = P; h->rec = rec;
+  h->lookup = cfg->lookup;
   h->anchor_of = anchor;
   int cap_log2 = 1;
   while ((1 << cap_log2) < 2 * k) ++cap_log2;
@@ -1035,20 +1562,7 @@ int hisparse_resolve(hisparse_handle *h, int32_t layer, const int32_t *d_sel,
   const LayerDev &Ld = h->layers[layer];
   const AnchorMeta &m = h->meta[layer];
   if ((flags & HISPARSE_FROM_MIRROR) && !Ld.mirror) return HISPARSE_EINVAL;
-  ResolveArgs a;
-  a.R = h->R; a.k = h->k; a.B = h->B; a.cap_log2 = h->cap_log2; a.rec16 = h->rec / 16;
-  a.io = (flags & HISPARSE_SKIP_IO) ? 0 : 1;
-  a.vec = (h->k % 4 == 0 && h->B % 8 == 0 && (reinterpret_cast<uintptr_t>(d_sel) & 15u) == 0) ? 1 : 0;
-  a.bucket_shift = h->bucket_shift[layer];
-  a.nbuckets = h->nbuckets[layer];
-  a.P = h->P;
-  a.sel = d_sel; a.num_reqs = d_num_reqs; a.newest = d_newest; a.out = d_out;
-  a.slot_pos = m.slot_pos; a.lru = m.lru; a.page_table = m.page_table;
-  a.miss_count = m.miss_count; a.unit_err = m.unit_err; a.status = h->d_status;
-  a.plan_pos = m.plan_pos; a.plan_slot = m.plan_slot; a.plan_count = m.plan_count;
-  a.src = (flags & HISPARSE_FROM_MIRROR) ? Ld.mirror : Ld.host;
-  a.src_req_stride = Ld.host_req_stride; a.src_row_stride = Ld.host_row_stride;
-  a.hot = Ld.hot; a.hot_req_stride = Ld.hot_req_stride; a.hot_row_stride = Ld.hot_row_stride;
+  const bool plan = flags & HISPARSE_RECORD_PLAN;
 
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(static_cast<unsigned>(h->cs) * h->R);
@@ -1062,8 +1576,42 @@ int hisparse_resolve(hisparse_handle *h, int32_t layer, const int32_t *d_sel,
   at[0].val.clusterDim.z = 1;
   lc.attrs = at;
   lc.numAttrs = 1;
-  cudaError_t e = (flags & HISPARSE_RECORD_PLAN) ? cudaLaunchKernelEx(&lc, resolve_kernel<true>, a)
-                                                 : cudaLaunchKernelEx(&lc, resolve_kernel<false>, a);
+  cudaError_t e;
+  if (h->lookup == HISPARSE_LOOKUP_HASH) {
+    ResolveArgs a;
+    a.R = h->R; a.k = h->k; a.B = h->B; a.cap_log2 = h->cap_log2; a.rec16 = h->rec / 16;
+    a.io = (flags & HISPARSE_SKIP_IO) ? 0 : 1;
+    a.vec = (h->k % 4 == 0 && h->B % 8 == 0 && (reinterpret_cast<uintptr_t>(d_sel) & 15u) == 0) ? 1 : 0;
+    a.bucket_shift = h->bucket_shift[layer];
+    a.nbuckets = h->nbuckets[layer];
+    a.P = h->P;
+    a.sel = d_sel; a.num_reqs = d_num_reqs; a.newest = d_newest; a.out = d_out;
+    a.slot_pos = m.slot_pos; a.lru = m.lru; a.page_table = m.page_table;
+    a.miss_count = m.miss_count; a.unit_err = m.unit_err; a.status = h->d_status;
+    a.plan_pos = m.plan_pos; a.plan_slot = m.plan_slot; a.plan_count = m.plan_count;
+    a.src = (flags & HISPARSE_FROM_MIRROR) ? Ld.mirror : Ld.host;
+    a.src_req_stride = Ld.host_req_stride; a.src_row_stride = Ld.host_row_stride;
+    a.hot = Ld.hot; a.hot_req_stride = Ld.hot_req_stride; a.hot_row_stride = Ld.hot_row_stride;
+    e = plan ? cudaLaunchKernelEx(&lc, resolve_kernel<true>, a)
+             : cudaLaunchKernelEx(&lc, resolve_kernel<false>, a);
+  } else {
+    PtArgs a;
+    a.R = h->R; a.k = h->k; a.B = h->B; a.rec16 = h->rec / 16;
+    a.io = (flags & HISPARSE_SKIP_IO) ? 0 : 1;
+    a.ks = h->ks; a.hcap_log2 = h->cap_log2;
+    a.bucket_shift = h->bucket_shift[layer];
+    a.nbuckets = h->nbuckets[layer];
+    a.P = h->P;
+    a.sel = d_sel; a.num_reqs = d_num_reqs; a.newest = d_newest; a.out = d_out;
+    a.slot_pos = m.slot_pos; a.lru = m.lru; a.page_table = m.page_table;
+    a.miss_count = m.miss_count; a.unit_err = m.unit_err; a.status = h->d_status;
+    a.plan_pos = m.plan_pos; a.plan_slot = m.plan_slot; a.plan_count = m.plan_count;
+    a.src = (flags & HISPARSE_FROM_MIRROR) ? Ld.mirror : Ld.host;
+    a.src_req_stride = Ld.host_req_stride; a.src_row_stride = Ld.host_row_stride;
+    a.hot = Ld.hot; a.hot_req_stride = Ld.hot_req_stride; a.hot_row_stride = Ld.hot_row_stride;
+    e = plan ? cudaLaunchKernelEx(&lc, resolve_pt_kernel<true>, a)
+             : cudaLaunchKernelEx(&lc, resolve_pt_kernel<false>, a);
+  }
   if (e != cudaSuccess) return cuda_fail(e);
   return HISPARSE_OK;
 }
@@ -1201,6 +1749,7 @@ int hisparse_get_info(const hisparse_handle *h, hisparse_info *out) {
   out->replay_ctas = h->replay_ctas;
   out->sm_count = h->sm_count;
   out->metadata_bytes = h->arena_bytes;
+  out->lookup = h->lookup;
   return HISPARSE_OK;
 }
 

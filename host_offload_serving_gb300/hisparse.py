@@ -13,6 +13,7 @@ from . import _build
 OK, EINVAL, EBOUND, ENOMEM, ECUDA, EROLE = 0, -1, -2, -3, -4, -5
 ERR_RANGE, ERR_DUP = 1, 2
 RECORD_PLAN, SKIP_IO, FROM_MIRROR = 1, 2, 4
+LOOKUP_PAGE_TABLE, LOOKUP_HASH = 0, 1
 
 _i32, _i64, _u32, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_void_p
 
@@ -20,7 +21,8 @@ _i32, _i64, _u32, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.
 class Config(ctypes.Structure):
     _fields_ = [("num_requests", _i32), ("num_layers", _i32), ("top_k", _i32),
                 ("buffer_slots", _i32), ("host_rows", _i64), ("record_bytes", _i32),
-                ("ctas_per_request", _i32), ("replay_ctas", _i32), ("anchor_of", _vp)]
+                ("ctas_per_request", _i32), ("replay_ctas", _i32), ("lookup", _i32),
+                ("anchor_of", _vp)]
 
 
 class LayerBuffers(ctypes.Structure):
@@ -32,7 +34,7 @@ class LayerBuffers(ctypes.Structure):
 class Info(ctypes.Structure):
     _fields_ = [("ctas_per_request", _i32), ("threads_per_cta", _i32), ("smem_bytes", _i32),
                 ("hash_capacity", _i32), ("replay_ctas", _i32), ("sm_count", _i32),
-                ("metadata_bytes", _i64)]
+                ("metadata_bytes", _i64), ("lookup", _i32)]
 
 
 # (name, restype, argtypes) of every exported symbol, in header order
@@ -52,6 +54,7 @@ SIGNATURES = [
     ("hisparse_get_info", _i32, [_vp, ctypes.POINTER(Info)]),
     ("hisparse_host_alloc", _i32, [ctypes.c_size_t, ctypes.POINTER(_vp)]),
     ("hisparse_host_free", _i32, [_vp]),
+    ("hisparse_host_hugepage_bytes", _i32, [_vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]),
     ("hisparse_last_cuda_error", _i32, []),
     ("hisparse_strerror", ctypes.c_char_p, [_i32]),
 ]
@@ -157,3 +160,9 @@ def hisparse_host_alloc(nbytes):
 
 def hisparse_host_free(p):
     return load().hisparse_host_free(p)
+
+
+def hisparse_host_hugepage_bytes(p, nbytes):
+    v = ctypes.c_size_t()
+    rc = load().hisparse_host_hugepage_bytes(p, nbytes, ctypes.byref(v))
+    return rc, v.value

@@ -35,6 +35,10 @@ class HostPool:
         self.ptr = ptr
         self.nbytes = int(nbytes)
 
+    def hugepage_fraction(self):
+        rc, huge = H.hisparse_host_hugepage_bytes(self.ptr, self.nbytes)
+        return huge / self.nbytes if rc == H.OK and self.nbytes else 0.0
+
     def numpy(self):
         buf = (ctypes.c_uint8 * self.nbytes).from_address(self.ptr)
         return np.ctypeslib.as_array(buf)
@@ -71,11 +75,11 @@ class HiSparse:
     """One instance of the C library (R requests, L layers, k, B, P, record)."""
 
     def __init__(self, R, L, k, B, P, rec, layers, anchor_of=None, ctas_per_request=0,
-                 replay_ctas=0):
+                 replay_ctas=0, lookup=0):
         self.R, self.L, self.k, self.B, self.P, self.rec = R, L, k, B, P, rec
         self.anchor_of = list(anchor_of) if anchor_of is not None else [-1] * L
         self._anchor_arr = (ctypes.c_int32 * L)(*self.anchor_of)
-        cfg = H.Config(R, L, k, B, P, rec, ctas_per_request, replay_ctas,
+        cfg = H.Config(R, L, k, B, P, rec, ctas_per_request, replay_ctas, lookup,
                        ctypes.cast(self._anchor_arr, ctypes.c_void_p))
         rc, h = H.hisparse_init(cfg, layers)
         H.check(rc, "hisparse_init")

@@ -66,6 +66,10 @@ extern "C" {
 #define HISPARSE_FROM_MIRROR 4u /* copy missed rows from the layer's HBM mirror
                                    of the host pool instead of the host pool */
 
+/* ---- lookup strategies (hisparse_config.lookup) ------------------------- */
+#define HISPARSE_LOOKUP_PAGE_TABLE 0
+#define HISPARSE_LOOKUP_HASH 1
+
 typedef struct hisparse_handle hisparse_handle;
 
 /* Sizes of one HiSparse instance ([DD] §5.7 --hisparse-config: top_k,
@@ -83,6 +87,13 @@ typedef struct {
   int32_t ctas_per_request; /* CTAs (one thread-block cluster) per request in
                                resolve, 1..16; 0 = chosen by the library */
   int32_t replay_ctas;      /* CTAs of the plan-replay kernel; 0 = chosen by the library */
+  int32_t lookup;           /* how RESOLVE finds the resident selections:
+                               HISPARSE_LOOKUP_PAGE_TABLE (0, default): worker CTAs read
+                               the page table, mark hits and start the missed-record
+                               reads while the leader CTA chooses victims;
+                               HISPARSE_LOOKUP_HASH (1): one CTA stages the selection in
+                               a shared-memory hash and probes every slot ([DD] §3.5
+                               stages 1-2), then the cluster fetches.  Same results. */
   const int32_t *anchor_of; /* [L] host array or NULL (= all -1): -1 if the layer runs
                                RESOLVE itself, else the id of the anchor layer whose
                                selection and slot table it shares ([DD] §3.6).  An
@@ -116,6 +127,7 @@ typedef struct {
   int32_t replay_ctas;
   int32_t sm_count;
   int64_t metadata_bytes;   /* device bytes owned by the library */
+  int32_t lookup;           /* HISPARSE_LOOKUP_* in use */
 } hisparse_info;
 
 /* Create an instance.  Validates every size and buffer on the host, then
@@ -146,11 +158,10 @@ int hisparse_destroy(hisparse_handle *h);
  * the most recent (in ascending slot order), this step's fetches come just
  * before them (in selection-list order), and the j-th miss in list order takes
  * the j-th least recent slot that is not a hit; empty slots are ordinary LRU
- * entries.  Missed records are read from the host pool in ascending position
- * order (which slot each one lands in is fixed by the rule above; reading them
- * in address order lets neighbouring fetches share the GPU's page-table
- * walks).  On a device-detected input error (HISPARSE_ERR_*) the request's
- * out row is all -1 and its state is unchanged.
+ * entries.  Which slot each missed record lands in is fixed by this rule; the
+ * order the records are read in is not part of the result.  On a
+ * device-detected input error (HISPARSE_ERR_*) the request's out row is all
+ * -1 and its state is unchanged.
  * The host pool rows fetched must be complete when this runs (order any
  * write-back before it with an event), and hot row B must already hold the
  * newest token's KV.  flags: HISPARSE_RECORD_PLAN | HISPARSE_SKIP_IO |
@@ -209,8 +220,8 @@ int hisparse_import_state(hisparse_handle *h, int32_t layer, const int32_t *slot
 /* Copy one anchor layer's last miss plan to host arrays: count [R],
  * pos [R][k] int32, slot [R][k] int32 (only the first count[r] entries of a
  * row are meaningful).  Entries are the (position, slot) pairs fetched by the
- * last resolve, in ascending position order -- the order the fetches were
- * issued in (see hisparse_resolve).  Synchronises.
+ * last resolve: in list order with HISPARSE_LOOKUP_PAGE_TABLE, in ascending
+ * position with HISPARSE_LOOKUP_HASH.  Synchronises.
  * Errors: EINVAL, EROLE, ECUDA. */
 int hisparse_export_plan(hisparse_handle *h, int32_t layer, int32_t *count, int32_t *pos,
                          int32_t *slot);
@@ -233,6 +244,13 @@ int hisparse_get_info(const hisparse_handle *h, hisparse_info *out);
  * Errors: EINVAL, ENOMEM. */
 int hisparse_host_alloc(size_t bytes, void **out);
 int hisparse_host_free(void *p);
+
+/* Bytes of [p, p + bytes) that the host kernel backs with transparent huge
+ * pages (from /proc/self/smaps; whole mappings that overlap the range are
+ * counted, capped at `bytes`).  A pool with few huge pages still works but
+ * costs the GPU more address-translation work per fetched record.
+ * Errors: EINVAL. */
+int hisparse_host_hugepage_bytes(const void *p, size_t bytes, size_t *huge_out);
 
 /* The cudaError_t of the last failed CUDA call made by this thread through
  * the library (0 if none), and a static message for any return code. */

@@ -16,7 +16,7 @@ from workload.traces import all_traces
 
 class Run:
     def __init__(self, w, flags=0, mirror=False, ctas_per_request=0, replay_ctas=0,
-                 num_reqs=None, oracle_bytes=True, traces=None):
+                 num_reqs=None, oracle_bytes=True, traces=None, lookup=0):
         self.w = w
         self.flags = flags
         dev = torch.device("cuda", 0)
@@ -26,7 +26,7 @@ class Run:
             self.mem.fill_mirror()
         self.hs = HiSparse(w.R, w.L, w.k, w.B, w.P, w.rec, self.mem.layer_buffers(),
                            anchor_of=w.anchor_of(), ctas_per_request=ctas_per_request,
-                           replay_ctas=replay_ctas)
+                           replay_ctas=replay_ctas, lookup=lookup)
         anchor_of = w.anchor_of()
         self.groups = [(a, [l for l in range(w.L) if anchor_of[l] == a]) for a in w.anchors()]
         tr = traces if traces is not None else all_traces(w)
@@ -111,7 +111,6 @@ class Run:
                     exp = sorted(zip(o.plan_pos[r, :o.plan_count[r]].tolist(),
                                      o.plan_slot[r, :o.plan_count[r]].tolist()))
                     assert got == exp, f"plan of layer {a} request {r}"
-                    assert [p for p, _ in zip(pp[r, :c[r]], ps[r])] == sorted(pp[r, :c[r]].tolist())
         if check_bytes:
             hot = self.mem.hot.cpu().numpy()
             for l in range(w.L):

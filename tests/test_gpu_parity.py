@@ -14,12 +14,15 @@ import pins
 pytestmark = pytest.mark.gpu
 
 
-def _instance(R, k, B, P, rec=16, ctas=0, fill=None):
+LOOKUPS = [H.LOOKUP_PAGE_TABLE, H.LOOKUP_HASH]
+
+
+def _instance(R, k, B, P, rec=16, ctas=0, fill=None, lookup=H.LOOKUP_PAGE_TABLE):
     mem = WorkloadMemory(R, 1, B, P, rec)
     host = mem.host_view(0)
     if fill is None:
         host[:] = np.random.default_rng(R * 1000 + k).integers(0, 256, size=host.shape, dtype=np.uint8)
-    hs = HiSparse(R, 1, k, B, P, rec, mem.layer_buffers(), ctas_per_request=ctas)
+    hs = HiSparse(R, 1, k, B, P, rec, mem.layer_buffers(), ctas_per_request=ctas, lookup=lookup)
     return mem, hs
 
 
@@ -28,11 +31,12 @@ def _dev(a, dtype=torch.int32):
 
 
 # ---------------------------------------------------------------------- #
-def test_worked_example_b():
+@pytest.mark.parametrize("lookup", LOOKUPS)
+def test_worked_example_b(lookup):
     """gentlecold.top deep dive §3.5 worked example, preset through import."""
     g = dict(pins.parse_golden("example_b_resolve.txt"))
     B, k, P = int(g["B"]), int(g["k"]), 64
-    mem, hs = _instance(1, k, B, P)
+    mem, hs = _instance(1, k, B, P, lookup=lookup)
     sp = np.array([pins._ints(g["slot_pos"])], np.int32)
     lru = np.array([pins._ints(g["lru"])], np.int16)
     pt = np.full((1, P), -1, np.int32)
@@ -57,12 +61,13 @@ def test_worked_example_b():
     hs.close(); mem.close()
 
 
-def test_worked_example_a():
+@pytest.mark.parametrize("lookup", LOOKUPS)
+def test_worked_example_a(lookup):
     """notes.kuangjux.top §5: misses 3,1,1 at capacity 3 and 3,1,0 at capacity 4."""
     rows = pins.parse_golden("example_a_capacity.txt")
     steps = [pins._ints(v) for key, v in rows if key == "step"]
     for cap, exp in ((3, [3, 1, 1]), (4, [3, 1, 0])):
-        mem, hs = _instance(1, 3, cap, 16)
+        mem, hs = _instance(1, 3, cap, 16, lookup=lookup)
         out = torch.empty((1, 3), dtype=torch.int32, device="cuda")
         got = []
         for s in steps:
@@ -86,9 +91,10 @@ def _enumerate_lists(k, P):
     return out
 
 
+@pytest.mark.parametrize("lookup", LOOKUPS)
 @pytest.mark.parametrize("k,P,steps,extra", [(2, 4, 3, (0, 1, 2)), (3, 5, 2, (0, 1)),
                                               (1, 4, 4, (0, 1, 2))])
-def test_exhaustive_tiny(k, P, steps, extra):
+def test_exhaustive_tiny(k, P, steps, extra, lookup):
     """All selection sequences of a tiny domain, one sequence per request."""
     lists = _enumerate_lists(k, P)
     seqs = list(itertools.product(range(len(lists)), repeat=steps))
@@ -99,7 +105,7 @@ def test_exhaustive_tiny(k, P, steps, extra):
             sel = np.array([[lists[i] for i in s] for s in chunk], np.int32)  # [R][T][k]
             sel = np.ascontiguousarray(sel.transpose(1, 0, 2))               # [T][R][k]
             newest = np.where(np.arange(R) % 3 == 0, P - 1, -1).astype(np.int32)
-            mem, hs = _instance(R, k, B, P)
+            mem, hs = _instance(R, k, B, P, lookup=lookup, ctas=1 + (R % 3 == 1))
             host = mem.host_view(0)
             o = OracleLayer(R, k, B, P, 16, host=host)
             o.reset()
@@ -138,9 +144,10 @@ def test_tiny_workload_every_step():
     _run_all(get("tiny"))
 
 
-def test_dsa_workload_full_size_every_step():
+@pytest.mark.parametrize("lookup", LOOKUPS)
+def test_dsa_workload_full_size_every_step(lookup):
     """8 requests x 4 layers, 128K context, k=2048, B=4096, write-through."""
-    _run_all(get("dsa"))
+    _run_all(get("dsa"), lookup=lookup)
 
 
 def test_quest_workload_scaled():
@@ -158,13 +165,16 @@ def test_sweep_workload_scaled(B):
     _run_all(sweep_workload(B, 0.70, L_ctx=65536).scaled(R=4, steps=6))
 
 
+@pytest.mark.parametrize("lookup", LOOKUPS)
 @pytest.mark.parametrize("cs", [1, 2, 3, 4, 8, 16])
-def test_cluster_sizes_identical(cs):
-    _run_all(get("dsa").scaled(R=3, groups=1, L_ctx=16384, steps=5), ctas_per_request=cs)
+def test_cluster_sizes_identical(cs, lookup):
+    _run_all(get("dsa").scaled(R=3, groups=1, L_ctx=16384, steps=5), ctas_per_request=cs,
+             lookup=lookup)
 
 
-def test_skip_io_metadata_identical_bytes_stale():
-    _run_all(get("dsa").scaled(R=2, groups=2, L_ctx=8192, steps=5), flags=H.SKIP_IO)
+@pytest.mark.parametrize("lookup", LOOKUPS)
+def test_skip_io_metadata_identical_bytes_stale(lookup):
+    _run_all(get("dsa").scaled(R=2, groups=2, L_ctx=8192, steps=5), flags=H.SKIP_IO, lookup=lookup)
 
 
 def test_from_mirror_bytes_identical():
@@ -177,9 +187,11 @@ def test_num_reqs_padding_leaves_tail_untouched():
 
 
 # ---------------------------------------------------------------------- #
-def test_device_detected_errors_keep_state():
+@pytest.mark.parametrize("lookup", LOOKUPS)
+@pytest.mark.parametrize("cs", [1, 3])
+def test_device_detected_errors_keep_state(lookup, cs):
     R, k, B, P = 4, 4, 6, 32
-    mem, hs = _instance(R, k, B, P)
+    mem, hs = _instance(R, k, B, P, lookup=lookup, ctas=cs)
     out = torch.empty((R, k), dtype=torch.int32, device="cuda")
     good = np.array([[1, 2, 3, -1]] * R, np.int32)
     hs.resolve(0, _dev(good), out)

@@ -112,17 +112,30 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
 
 
-def profile_traffic(kernel_file):
-    """Per-launch DRAM traffic recorded by an ncu capture of the current kernel source."""
-    p = os.path.join(ROOT, "profiles", "resolve_traffic.json")
-    if not os.path.exists(p):
+def profile_traffic(kernel_file, kernel):
+    """Per-launch traffic of `kernel` from the ncu summaries under profiles/.
+
+    A summary line of the form
+      machine: kernel=<name> sha256=<kernel source sha256> dram_bytes_per_launch=<n> sysmem_bytes_per_launch=<n>
+    counts only while the kernel source still has that hash (the counters are
+    stale once the kernel changes).
+    """
+    sha = hashlib.sha256(open(kernel_file, "rb").read()).hexdigest()
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
         return None
-    with open(p) as fh:
-        d = json.load(fh)
-    src = open(kernel_file, "rb").read()
-    if d.get("source_sha256") != hashlib.sha256(src).hexdigest():
-        return None  # the kernel changed since the counters were taken
-    return d
+    for name in sorted(os.listdir(pdir)):
+        if not name.endswith(".md"):
+            continue
+        for line in open(os.path.join(pdir, name), encoding="utf-8"):
+            if not line.startswith("machine:"):
+                continue
+            kv = dict(x.split("=", 1) for x in line.split()[1:] if "=" in x)
+            if kv.get("kernel") == kernel and kv.get("sha256") == sha:
+                return {"dram_bytes_per_launch": float(kv["dram_bytes_per_launch"]),
+                        "sysmem_bytes_per_launch": float(kv["sysmem_bytes_per_launch"]),
+                        "source": name}
+    return None
 
 
 # --------------------------------------------------------------------------- #
@@ -228,7 +241,8 @@ def run_ours(args):
     w = get(args.workload)
     if w.write_through:
         w = w.scaled(steps=max(w.steps, args.warmup + args.steps))
-    w = w.scaled(seed=w.seed + 1000 * rank)     # each replica its own requests
+    from host_offload_serving_gb300.replicas import replica_seed, max_over_ranks, job_throughput
+    w = w.scaled(seed=replica_seed(w.seed, rank))     # each replica its own requests
     T = args.warmup + args.steps
     if not w.write_through and T > w.steps:
         w = w.scaled(steps=T)
@@ -368,13 +382,8 @@ def run_ours(args):
     total_ms = sum(step_ms)
     sel_per_step = G * w.R * w.k
     value_local = sel_per_step * args.steps / (total_ms / 1e3)
-    if dist is not None:
-        tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms_max = float(tt.item())
-    else:
-        total_ms_max = total_ms
-    value = sel_per_step * args.steps * world / (total_ms_max / 1e3)
+    total_ms_max = max_over_ranks(total_ms, dist, dev)
+    value = job_throughput(sel_per_step * args.steps, total_ms_max / 1e3, world)
 
     if res_ms is not None:
         res_flat = [x for r in res_ms for x in r]
@@ -494,11 +503,14 @@ def run_ours(args):
 
     peaks, peak_src = measured_peaks()
     kernel_src = os.path.join(ROOT, "host_offload_serving_gb300", "csrc", "hisparse.cu")
-    prof = profile_traffic(kernel_src)
+    kname = "resolve_pt_kernel" if args.lookup == 0 else "resolve_kernel"
+    prof = profile_traffic(kernel_src, kname)
     roof = {"bound": "host_link", "achieved": round(fetch_gbs, 2), "peak": round(h2d_gbs, 2),
             "unit": "GB/s", "frac": round(fetch_gbs / h2d_gbs, 4),
             "traffic": prof["dram_bytes_per_launch"] if prof else None,
-            "kernel": "resolve_kernel",
+            "traffic_sysmem": prof["sysmem_bytes_per_launch"] if prof else None,
+            "traffic_source": prof["source"] if prof else None,
+            "kernel": kname,
             "peak_source": "pinned cudaMemcpyAsync H2D, 1 GiB x 20, same run",
             "algorithmic_bytes_per_launch": miss_bytes / (args.steps * G),
             "avg_launch_us": round(resolve_avg_ms * 1e3, 2), "timing": timing_note,

@@ -1,0 +1,98 @@
+"""The C ABI library on a machine without a GPU: it loads, exports every
+declared symbol, and rejects bad arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from host_offload_serving_gb300 import hisparse as H
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "hisparse.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(hisparse_[a-z_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = H.load()
+    names = declared_functions()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(lib, n), n
+    bound = {n for n, _, _ in H.SIGNATURES}
+    assert set(names) == bound, set(names) ^ bound
+
+
+def test_strerror_and_codes():
+    lib = H.load()
+    assert lib.hisparse_strerror(0) == b"ok"
+    for code in (H.EINVAL, H.EBOUND, H.ENOMEM, H.ECUDA, H.EROLE):
+        assert lib.hisparse_strerror(code) not in (b"ok", b"unknown error")
+    assert lib.hisparse_strerror(-99) == b"unknown error"
+
+
+def _cfg(R=2, L=1, k=4, B=8, P=100, rec=1152, cs=0, rc=0, lookup=0, anchor=None):
+    arr = None
+    if anchor is not None:
+        arr = (ctypes.c_int32 * len(anchor))(*anchor)
+    c = H.Config(R, L, k, B, P, rec, cs, rc, lookup, ctypes.cast(arr, ctypes.c_void_p) if arr else None)
+    c._keep = arr
+    return c
+
+
+def _bufs(L=1, host=0x1000, hot=0x2000, rs=1152 * 100, row=1152, hrs=1152 * 9, hrow=1152):
+    return [H.LayerBuffers(host, rs, row, hot, hrs, hrow, None) for _ in range(L)]
+
+
+@pytest.mark.parametrize("kw,bufkw,code", [
+    (dict(B=2, k=4), {}, H.EBOUND),                     # B < k
+    (dict(B=40000, k=4), {}, H.EBOUND),                 # int16 LRU order
+    (dict(rec=1000), dict(row=1008, hrow=1008), H.EINVAL),  # record not a multiple of 16
+    (dict(R=0), {}, H.EINVAL),
+    (dict(R=9000), {}, H.EBOUND),
+    (dict(P=0), {}, H.EINVAL),
+    (dict(cs=17), {}, H.EBOUND),
+    (dict(lookup=7), {}, H.EINVAL),
+    (dict(L=3, anchor=[-1, 0, 1]), dict(L=3), H.EROLE),   # anchor of an anchor
+    (dict(L=2, anchor=[1, 1]), dict(L=2), H.EROLE),       # own anchor
+    (dict(L=2, anchor=[-1, 5]), dict(L=2), H.EROLE),      # out of range
+    ({}, dict(host=0x1004), H.EINVAL),                   # misaligned host pool
+    ({}, dict(hot=0), H.EINVAL),                         # NULL hot buffer
+    ({}, dict(row=1000), H.EINVAL),                      # row stride < record
+    ({}, dict(rs=1152 * 100 + 8), H.EINVAL),             # stride not a multiple of 16
+])
+def test_init_rejects_on_host(kw, bufkw, code):
+    L = kw.get("L", 1)
+    rc, h = H.hisparse_init(_cfg(**kw), _bufs(**bufkw) if "L" in bufkw else _bufs(L=L, **bufkw))
+    assert rc == code and h is None
+
+
+def test_init_without_gpu_reports_cuda_error_not_crash():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    rc, h = H.hisparse_init(_cfg(), _bufs())
+    assert rc in (H.ECUDA, H.EINVAL) and h is None
+
+
+def test_calls_on_null_handle_are_rejected():
+    lib = H.load()
+    assert lib.hisparse_resolve(None, 0, 1, None, None, 1, 0, None) == H.EINVAL
+    assert lib.hisparse_writeback(None, 0, 1, None, None) == H.EINVAL
+    assert lib.hisparse_prefetch_plan(None, 0, 1, None, None) == H.EINVAL
+    assert lib.hisparse_reset(None, 0, None) == H.EINVAL
+    assert lib.hisparse_destroy(None) == H.EINVAL
+    f = ctypes.c_uint32()
+    assert lib.hisparse_get_status(None, ctypes.byref(f), None) == H.EINVAL
+    assert H.hisparse_host_alloc(0)[0] == H.EINVAL
+
+
+def test_hugepage_query_on_ordinary_memory():
+    a = np.zeros(1 << 20, np.uint8)
+    rc, huge = H.hisparse_host_hugepage_bytes(a.ctypes.data, a.nbytes)
+    assert rc == H.OK and 0 <= huge <= a.nbytes

@@ -255,6 +255,18 @@ def run_ours(args):
                   ctas_per_request=args.ctas, replay_ctas=args.replay_ctas, lookup=args.lookup)
     info = hs.info()
     hp_frac = mem.pool.hugepage_fraction()
+
+    def thp_splits():
+        d = {}
+        try:
+            for line in open("/proc/vmstat"):
+                k, v = line.split()
+                if k in ("thp_split_page", "thp_split_pmd"):
+                    d[k] = int(v)
+        except OSError:
+            pass
+        return d
+    splits0 = thp_splits()
     anchor_of = w.anchor_of()
     groups = [(a, [l for l in range(w.L) if anchor_of[l] == a]) for a in w.anchors()]
     G = len(groups)
@@ -283,17 +295,12 @@ def run_ours(args):
                      wb_pos=wb[t] if (wb is not None and t > 0) else None,
                      new_rows=new_rows[t] if new_rows is not None else None)
 
-    clocks = Clocks(local)
-    clocks.__enter__()
-    t_wait = time.time()
-    while not clocks.samples and time.time() - t_wait < 5:
-        time.sleep(0.05)
-
     # Every step is captured once as a CUDA graph -- the form the pages deploy
     # RESOLVE in (gentlecold.top deep dive §3.5: captured in the decode CUDA
     # graph) -- so the timed region measures GPU work, not Python launch
-    # overhead.  Timing events sit inside the graphs around every RESOLVE
-    # launch, on the stream it runs on.
+    # overhead.  The headline pass replays plain graphs; a second pass over the
+    # same steps replays graphs with timing events around every RESOLVE and
+    # write-back launch, on the stream each runs on.
     def timing_event():
         try:
             return torch.cuda.Event(enable_timing=True, external=True), True
@@ -301,38 +308,48 @@ def run_ours(args):
             return torch.cuda.Event(enable_timing=True), False
 
     cap = torch.cuda.Stream()
-    graphs, rev = [], []
-    ext_ok = True
-    orig_resolve = hs.resolve
-    for t in range(T):
-        evs = []
-        for _ in groups:
-            a0, ok0 = timing_event()
-            a1, ok1 = timing_event()
-            ext_ok = ext_ok and ok0 and ok1
-            evs.append((a0, a1))
+
+    def capture(t, instrument):
+        """Graph of step t; with `instrument`, timing events around every
+        RESOLVE and write-back launch and a copy of the miss counts."""
+        evs, wev = [], []
         box = [0]
+        orig_resolve, orig_wb = hs.resolve, hs.writeback
 
-        def timed_resolve(layer, *a, _evs=evs, _box=box, **kw):
-            gi = _box[0]
+        def timed_resolve(layer, *a, **kw):
             st = kw.get("stream")
-            if ext_ok:
-                _evs[gi][0].record(st)
+            e0, e1 = timing_event()[0], timing_event()[0]
+            e0.record(st)
             orig_resolve(layer, *a, **kw)
-            if ext_ok:
-                _evs[gi][1].record(st)
-            _box[0] += 1
+            e1.record(st)
+            evs.append((e0, e1))
 
-        hs.resolve = timed_resolve
+        def timed_wb(layer, *a, **kw):
+            st = kw.get("stream")
+            e0, e1 = timing_event()[0], timing_event()[0]
+            e0.record(st)
+            orig_wb(layer, *a, **kw)
+            e1.record(st)
+            wev.append((e0, e1))
+
+        if instrument:
+            hs.resolve, hs.writeback = timed_resolve, timed_wb
         g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(cap):
-            with torch.cuda.graph(g, stream=cap):
-                issue(t)
-                for gi, (a, _) in enumerate(groups):
-                    hs.copy_miss_counts(a, miss_hist[t, gi], stream=torch.cuda.current_stream())
-        hs.resolve = orig_resolve
-        graphs.append(g)
-        rev.append(evs)
+        try:
+            with torch.cuda.stream(cap):
+                with torch.cuda.graph(g, stream=cap):
+                    issue(t)
+                    if instrument:
+                        for gi, (a, _) in enumerate(groups):
+                            hs.copy_miss_counts(a, miss_hist[t, gi],
+                                                stream=torch.cuda.current_stream())
+        finally:
+            hs.resolve, hs.writeback = orig_resolve, orig_wb
+        return g, evs, wev
+
+    ext_ok = timing_event()[1]
+    plain = [capture(t, False)[0] for t in range(T)]
+    instr = [capture(t, ext_ok) for t in range(T)] if ext_ok else None
     torch.cuda.synchronize()
 
     clocks = Clocks(local)
@@ -341,13 +358,12 @@ def run_ours(args):
     while not clocks.samples and time.time() - t_wait < 5:
         time.sleep(0.05)
 
-    # ---- warm-up ----
+    # ---- pass 1 (the headline): W warm-up steps, then exactly K timed steps,
+    #      L2 flushed before each (the flush also keeps the GPU busy while the
+    #      host enqueues the replay) ----
     for t in range(args.warmup):
-        graphs[t].replay()
+        plain[t].replay()
     torch.cuda.synchronize()
-
-    # ---- timed: K steps, L2 flushed before each (the flush also keeps the GPU
-    #      busy while the host enqueues the replay) ----
     cur = torch.cuda.current_stream()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
@@ -359,7 +375,7 @@ def run_ours(args):
         t = args.warmup + i
         flush.fill_(i & 0xFF)
         ev[i][0].record(cur)
-        graphs[t].replay()
+        plain[t].replay()
         ev[i][1].record(cur)
         launches += G + (1 if (wb is not None and t > 0) else 0) + sum(len(f) for _, f in groups)
     torch.cuda.synchronize()
@@ -368,16 +384,35 @@ def run_ours(args):
     time.sleep(0.25)               # one more clock sample after the timed region
     clocks.__exit__()
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    if ext_ok:
-        res_ms = [[a.elapsed_time(b) for a, b in rev[args.warmup + i]] for i in range(args.steps)]
-    else:
-        res_ms = None
     flags, _ = hs.status()
-    miss = miss_hist[args.warmup:].cpu().numpy().astype(np.int64)       # [K][G][R]
 
     verify = None
     if args.verify:
         verify = verify_against_oracle(w, hs, mem, groups, traces, args.warmup + args.steps)
+
+    # ---- pass 2 (per-kernel durations for the roofline): the same steps from
+    #      the admission state, with events inside the graphs around every
+    #      RESOLVE and write-back launch ----
+    hs.reset()
+    mem.hot.zero_()
+    torch.cuda.synchronize()
+    res_ms = wb_ms = None
+    if instr is not None:
+        for t in range(T):
+            if t >= args.warmup:
+                flush.fill_(t & 0xFF)
+            instr[t][0].replay()
+            torch.cuda.synchronize()
+        res_ms = [[a.elapsed_time(b) for a, b in instr[args.warmup + i][1]] for i in range(args.steps)]
+        wb_ms = [a.elapsed_time(b) for i in range(args.steps) for a, b in instr[args.warmup + i][2]]
+    else:   # no in-graph timing events in this torch: count misses eagerly
+        for t in range(T):
+            plain[t].replay()
+            for gi, (a, _) in enumerate(groups):
+                hs.copy_miss_counts(a, miss_hist[t, gi], stream=cur)
+        torch.cuda.synchronize()
+    flags |= hs.status()[0]
+    miss = miss_hist[args.warmup:].cpu().numpy().astype(np.int64)       # [K][G][R]
 
     total_ms = sum(step_ms)
     sel_per_step = G * w.R * w.k
@@ -387,7 +422,8 @@ def run_ours(args):
 
     if res_ms is not None:
         res_flat = [x for r in res_ms for x in r]
-        timing_note = "events inside the step graphs around every RESOLVE launch"
+        timing_note = ("events inside the step graphs around every RESOLVE launch "
+                       "(second pass over the same steps)")
     else:   # this torch cannot put timing events inside a graph
         res_flat = [x / G for x in step_ms]
         timing_note = "step graph time / anchors (includes write-back and row copy)"
@@ -515,7 +551,8 @@ def run_ours(args):
             "algorithmic_bytes_per_launch": miss_bytes / (args.steps * G),
             "avg_launch_us": round(resolve_avg_ms * 1e3, 2), "timing": timing_note,
             "launch_us_p50_p90_p99_max": [round(pct(0.5), 2), round(pct(0.9), 2),
-                                          round(pct(0.99), 2), round(srt[-1] * 1e3, 2)]}
+                                          round(pct(0.99), 2), round(srt[-1] * 1e3, 2)],
+            "writeback_us_avg": round(1e3 * sum(wb_ms) / len(wb_ms), 2) if wb_ms else None}
     if allhit:
         allhit["hbm_peak_gbs"] = peaks.get("hbm_gbs")
         allhit["hbm_frac"] = round(allhit["hbm_gbs"] / peaks.get("hbm_gbs"), 5)
@@ -528,6 +565,9 @@ def run_ours(args):
         cpu.pop("seconds", None)
         cpu.pop("steps", None)
 
+    hp_frac_end = mem.pool.hugepage_fraction()
+    s1 = thp_splits()
+    splits_run = {k: s1[k] - splits0.get(k, 0) for k in s1}
     hs.close()
     mem.close()
     if rank == 0:
@@ -542,7 +582,9 @@ def run_ours(args):
                        "l2": "flushed (256 MB write) before every timed step",
                        "ctas_per_request": info["ctas_per_request"],
                        "lookup": ["page_table", "hash"][info["lookup"]],
-                       "host_pool_hugepage_fraction": round(hp_frac, 3)},
+                       "host_pool_hugepage_fraction": round(hp_frac, 3),
+                       "host_pool_hugepage_fraction_end": round(hp_frac_end, 3),
+                       "host_thp_splits_during_run": splits_run},
             "roofline": roof,
             "miss_fetch_gbs": round(fetch_gbs, 2), "h2d_link_gbs": round(h2d_gbs, 2),
             "miss_rate": round(miss_rate, 4),

@@ -612,7 +612,7 @@ __host__ __device__ inline PtLayout pt_layout(int k, int B, int ks, int hcap) {
   L.l_mpos = o;    o += align16(4u * k);
   L.l_hkey = o;    o += align16(4u * hcap);
   L.l_misc = o;    o += align16(4u * (8 + kMaxWorkers + 1));
-  L.cnt = o;       o += align16(4u * 32);
+  L.cnt = o;       o += align16(4u * 64);
   L.total = o;
   return L;
 }
@@ -673,6 +673,51 @@ __device__ __forceinline__ int block_compact(int n, Flag flag, Emit emit, int32_
   }
   __syncthreads();
   return total;
+}
+
+// Two stable compactions of [0, n) in one pass (one barrier for both):
+// emitA(i, rank) for flagA, emitB(i, rank) for flagB.  s_cnt holds 64 ints.
+template <class FlagA, class EmitA, class FlagB, class EmitB>
+__device__ __forceinline__ void block_compact2(int n, FlagA flagA, EmitA emitA, FlagB flagB,
+                                               EmitB emitB, int32_t *s_cnt) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int seg = ((n + kWarps * 32 - 1) / (kWarps * 32)) * 32;
+  const int i0 = warp * seg, i1 = min(n, i0 + seg);
+  int ca = 0, cb = 0;
+  for (int b = i0; b < i1; b += 32) {
+    const int i = b + lane;
+    const bool in = i < i1;
+    ca += __popc(__ballot_sync(kFull, in && flagA(i)));
+    cb += __popc(__ballot_sync(kFull, in && flagB(i)));
+  }
+  if (lane == 0) {
+    s_cnt[warp] = ca;
+    s_cnt[32 + warp] = cb;
+  }
+  __syncthreads();
+  const int va = s_cnt[lane], vb = s_cnt[32 + lane];
+  int ia = va, ib = vb;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int ta = __shfl_up_sync(kFull, ia, d), tb = __shfl_up_sync(kFull, ib, d);
+    if (lane >= d) {
+      ia += ta;
+      ib += tb;
+    }
+  }
+  int ba = __shfl_sync(kFull, ia - va, warp), bb = __shfl_sync(kFull, ib - vb, warp);
+  const uint32_t lt = lanemask_lt();
+  for (int b = i0; b < i1; b += 32) {
+    const int i = b + lane;
+    const bool in = i < i1;
+    const bool fa = in && flagA(i), fb = in && flagB(i);
+    const uint32_t ma = __ballot_sync(kFull, fa), mb = __ballot_sync(kFull, fb);
+    if (fa) emitA(i, ba + __popc(ma & lt));
+    if (fb) emitB(i, bb + __popc(mb & lt));
+    ba += __popc(ma);
+    bb += __popc(mb);
+  }
+  __syncthreads();
 }
 
 __device__ __forceinline__ bool bit_of(const uint32_t *bits, int s) {
@@ -784,7 +829,7 @@ __device__ void pt_worker_classify(const PtArgs &a, int r, int i0, int n, int32_
 // new LRU order.  Returns nothing; results live in the leader's shared memory.
 __device__ void pt_leader_decide(const PtArgs &a, int cs, int nw, int32_t newest,
                                  unsigned char *smem, const PtLayout &L) {
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31;
   const int B = a.B;
   const int nwords = (B + 31) / 32;
   const int hcap = 1 << a.hcap_log2;
@@ -801,72 +846,85 @@ __device__ void pt_leader_decide(const PtArgs &a, int cs, int nw, int32_t newest
   const int32_t *w_mp0 = reinterpret_cast<const int32_t *>(smem + L.w_mp);
   auto wrank = [&](int w) { return static_cast<uint32_t>(cs == 1 ? 0 : w + 1); };
 
-  // per-worker counts -> prefix offsets in list order; error bits
-  if (tid == 0) {
-    uint32_t err = (newest < -1 || newest >= a.P) ? HISPARSE_ERR_RANGE : 0u;
-    uint32_t newest_seen = 0;
-    int pre = 0;
-    for (int w = 0; w < nw; ++w) {
-      err |= ld_dsmem_u32(dsmem_addr(&w_misc0[kWErr], wrank(w)));
-      newest_seen += ld_dsmem_u32(dsmem_addr(&w_misc0[kWNewest], wrank(w)));
-      l_misc[kLPrefix + w] = static_cast<uint32_t>(pre);
-      pre += static_cast<int>(ld_dsmem_u32(dsmem_addr(&w_misc0[kWCount], wrank(w))));
+  // Every read of a worker's shared memory below is issued by a different
+  // thread, so the cluster's distributed-shared-memory latency is paid once
+  // per phase, not once per worker.
+  // (1) per-worker counts -> prefix offsets in list order; error bits (warp 0)
+  if (tid < 32) {
+    uint32_t err = 0, seen = 0;
+    int cnt = 0;
+    if (lane < nw) {
+      err = ld_dsmem_u32(dsmem_addr(&w_misc0[kWErr], wrank(lane)));
+      seen = ld_dsmem_u32(dsmem_addr(&w_misc0[kWNewest], wrank(lane)));
+      cnt = static_cast<int>(ld_dsmem_u32(dsmem_addr(&w_misc0[kWCount], wrank(lane))));
     }
-    if (newest_seen > 1) err |= HISPARSE_ERR_DUP;
-    l_misc[kLPrefix + nw] = static_cast<uint32_t>(pre);
-    l_misc[kLErr] = err;
-    l_misc[kLM] = static_cast<uint32_t>(pre);
-    l_misc[kLHits] = 0;
+    int inc = cnt;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int t = __shfl_up_sync(kFull, inc, d);
+      if (lane >= d) inc += t;
+      err |= __shfl_xor_sync(kFull, err, d);
+      seen += __shfl_xor_sync(kFull, seen, d);
+    }
+    if (lane < nw) l_misc[kLPrefix + lane] = static_cast<uint32_t>(inc - cnt);
+    if (lane == 31) {
+      if (newest < -1 || newest >= a.P) err |= HISPARSE_ERR_RANGE;
+      if (seen > 1) err |= HISPARSE_ERR_DUP;
+      l_misc[kLPrefix + nw] = static_cast<uint32_t>(inc);
+      l_misc[kLErr] = err;
+      l_misc[kLM] = static_cast<uint32_t>(inc);
+      l_misc[kLHits] = 0;
+    }
   }
+  for (int x = tid; x < nwords; x += kThreads) l_hit[x] = 0;
   __syncthreads();
-  // hit bitmap: OR of the slices; a slot hit by two slices is a duplicate
+  // (2) hit bitmap: OR of the slices (a slot hit by two slices is a duplicate),
+  //     and the miss positions in list order, with duplicates among misses
+  //     caught by an open-addressing set ([DD] §3.5 stage 1's hash).
   {
-    uint32_t dup = 0, hits = 0;
-    for (int x = tid; x < nwords; x += kThreads) {
-      uint32_t acc = 0;
-      for (int w = 0; w < nw; ++w) {
-        const uint32_t b = ld_dsmem_u32(dsmem_addr(&w_hit0[x], wrank(w)));
-        dup |= acc & b;
-        acc |= b;
-      }
-      l_hit[x] = acc;
-      hits += __popc(acc);
+    uint32_t dup = 0;
+    for (int idx = tid; idx < nw * nwords; idx += kThreads) {
+      const int w = idx / nwords, x = idx - w * nwords;
+      const uint32_t b = ld_dsmem_u32(dsmem_addr(&w_hit0[x], wrank(w)));
+      if (b) dup |= atomicOr(&l_hit[x], b) & b;
     }
-    if (dup) atomicOr(&l_misc[kLErr], HISPARSE_ERR_DUP);
-    if (hits) atomicAdd(&l_misc[kLHits], hits);
-  }
-  // miss positions in list order; duplicates among misses via an
-  // open-addressing set ([DD] §3.5 stage 1's multiplicative hash)
-  for (int w = 0; w < nw; ++w) {
-    const int pre = static_cast<int>(l_misc[kLPrefix + w]);
-    const int mw = static_cast<int>(l_misc[kLPrefix + w + 1]) - pre;
-    for (int j = tid; j < mw; j += kThreads) {
+    const int M = static_cast<int>(l_misc[kLM]);
+    for (int g = tid; g < M; g += kThreads) {
+      int w = 0;
+      while (w + 1 < nw && static_cast<int>(l_misc[kLPrefix + w + 1]) <= g) ++w;
+      const int j = g - static_cast<int>(l_misc[kLPrefix + w]);
       const int32_t p = static_cast<int32_t>(ld_dsmem_u32(dsmem_addr(&w_mp0[j], wrank(w))));
-      l_mpos[pre + j] = p;
+      l_mpos[g] = p;
       uint32_t h = hash_pos(p, a.hcap_log2);
       for (int probe = 0; probe < hcap; ++probe) {
         const int32_t prev = atomicCAS(&l_hkey[h], -1, p);
         if (prev == -1) break;
         if (prev == p) {
-          atomicOr(&l_misc[kLErr], HISPARSE_ERR_DUP);
+          dup = 1;
           break;
         }
         h = (h + 1) & (hcap - 1);
       }
     }
+    if (dup) atomicOr(&l_misc[kLErr], HISPARSE_ERR_DUP);
   }
   __syncthreads();
   if (l_misc[kLErr]) return;  // uniform
+  // (3) hit count, then one pass that compacts hits (slot order) and
+  //     evictables (LRU order) together
+  {
+    int hits = 0;
+    for (int x = tid; x < nwords; x += kThreads) hits += __popc(l_hit[x]);
+    if (hits) atomicAdd(&l_misc[kLHits], static_cast<uint32_t>(hits));
+  }
+  __syncthreads();
   const int M = static_cast<int>(l_misc[kLM]);
   const int H = static_cast<int>(l_misc[kLHits]);
   const int E = B - H;
-  // hits, newest last, in ascending slot order
-  block_compact(
+  block_compact2(
       B, [&](int s) { return bit_of(l_hit, s); },
-      [&](int s, int h) { l_newlru[E + h] = static_cast<int16_t>(s); }, s_cnt);
-  // evictables in LRU order: the j-th goes to the j-th miss; the rest stay oldest
-  block_compact(
-      B, [&](int j) { return !bit_of(l_hit, l_lru[j]); },
+      [&](int s, int h) { l_newlru[E + h] = static_cast<int16_t>(s); },
+      [&](int j) { return !bit_of(l_hit, l_lru[j]); },
       [&](int j, int e) {
         const int16_t sl = l_lru[j];
         if (e < M) l_ev[e] = sl;
@@ -1312,6 +1370,11 @@ int hisparse_host_alloc(size_t bytes, void **out) {
       madvise(p, sz, MADV_HUGEPAGE);  // advice only: a refusal still leaves valid memory
       first_touch(p, sz);
       madvise(p, sz, kMadvCollapse);  // ask for huge pages now where the first touch got none
+      // A fork() of this process would split every pinned huge page of the
+      // pool into base pages in the parent (pinned pages cannot be shared
+      // copy-on-write), and the GPU would then stall on translation misses.
+      // Children never need the pool.
+      madvise(p, sz, MADV_DONTFORK);
       cudaError_t e = cudaHostRegister(p, sz, cudaHostRegisterMapped | cudaHostRegisterPortable);
       if (e == cudaSuccess) {
         std::lock_guard<std::mutex> lk(g_host_mu);

@@ -239,8 +239,10 @@ int hisparse_get_info(const hisparse_handle *h, hisparse_info *out);
  * registered with cudaHostRegister (zero-filled, size rounded up to whole huge
  * pages internally): the GPU then translates the pool with large pages, and
  * random record fetches stall far less on address translation than they do
- * on cudaHostAlloc memory.  Smaller requests, or a refused registration, fall
- * back to cudaHostAlloc (contents unspecified).  Free with hisparse_host_free.
+ * on cudaHostAlloc memory.  Such a pool is excluded from fork() children
+ * (MADV_DONTFORK): a fork would otherwise split its pinned huge pages in the
+ * parent.  Smaller requests, or a refused registration, fall back to
+ * cudaHostAlloc (contents unspecified).  Free with hisparse_host_free.
  * Errors: EINVAL, ENOMEM. */
 int hisparse_host_alloc(size_t bytes, void **out);
 int hisparse_host_free(void *p);

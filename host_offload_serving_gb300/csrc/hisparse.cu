@@ -122,6 +122,7 @@ struct WritebackArgs {
   int32_t layer0, R, B, rec16;
   int64_t P;
   const int32_t *pos;          // [nl][R]
+  const char *new_rows;        // [nl][R][rec16 * 16] or null
   const int32_t *num_reqs;
   uint32_t *status;
 };
@@ -726,7 +727,8 @@ __device__ __forceinline__ bool bit_of(const uint32_t *bits, int s) {
 
 // Worker: classify selections [i0, i0 + n) of request r.
 __device__ void pt_worker_classify(const PtArgs &a, int r, int i0, int n, int32_t newest,
-                                   unsigned char *smem, const PtLayout &L) {
+                                   const int32_t (&first)[kGroup], unsigned char *smem,
+                                   const PtLayout &L) {
   const int tid = threadIdx.x;
   const int B = a.B;
   const int64_t P = a.P;
@@ -748,7 +750,7 @@ __device__ void pt_worker_classify(const PtArgs &a, int r, int i0, int n, int32_
 #pragma unroll
     for (int u = 0; u < kGroup; ++u) {
       const int t = base + u * kThreads + tid;
-      p[u] = t < n ? g_sel[t] : -1;
+      p[u] = base == 0 ? first[u] : (t < n ? g_sel[t] : -1);
     }
 #pragma unroll
     for (int u = 0; u < kGroup; ++u) {
@@ -988,9 +990,20 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_pt_kernel(const PtArgs a)
   const bool worker = cs == 1 || rank > 0;
   const int w = cs == 1 ? 0 : rank - 1;
   const PtLayout L = pt_layout(a.k, a.B, a.ks, 1 << a.hcap_log2);
+  const int i0 = w * a.ks;
+  const int n = worker ? max(0, min(a.k, i0 + a.ks) - i0) : 0;
+  // The first loads of every role go out together with the batch-size and
+  // newest-position reads (all are in bounds for any r < R); the padding check
+  // then costs no extra memory round trip.
+  int32_t first[kGroup];
+#pragma unroll
+  for (int u = 0; u < kGroup; ++u) {
+    const int t = u * kThreads + tid;
+    first[u] = (worker && t < n) ? a.sel[static_cast<int64_t>(r) * a.k + i0 + t] : -1;
+  }
+  const int32_t newest = a.newest ? a.newest[r] : -1;
   const int nreq = a.num_reqs ? min(*a.num_reqs, a.R) : a.R;
   if (r >= nreq) return;  // graph padding: every CTA of the cluster leaves
-  const int32_t newest = a.newest ? a.newest[r] : -1;
 
   if (leader) {  // the unit's LRU order and slot map, and an empty duplicate set
     int16_t *l_lru = reinterpret_cast<int16_t *>(smem + L.l_lru);
@@ -998,15 +1011,20 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_pt_kernel(const PtArgs a)
     int32_t *l_hkey = reinterpret_cast<int32_t *>(smem + L.l_hkey);
     const int16_t *g_lru = a.lru + static_cast<int64_t>(r) * a.B;
     const int32_t *g_slotpos = a.slot_pos + static_cast<int64_t>(r) * a.B;
-    for (int s = tid; s < a.B; s += kThreads) {
-      l_lru[s] = g_lru[s];
-      l_slotpos[s] = g_slotpos[s];
+    if (a.B % 8 == 0) {  // 16-byte rows: one vector load per 8 LRU / 4 slot entries
+      for (int c = tid; c < a.B / 8; c += kThreads)
+        reinterpret_cast<uint4 *>(l_lru)[c] = reinterpret_cast<const uint4 *>(g_lru)[c];
+      for (int c = tid; c < a.B / 4; c += kThreads)
+        reinterpret_cast<int4 *>(l_slotpos)[c] = reinterpret_cast<const int4 *>(g_slotpos)[c];
+    } else {
+      for (int s = tid; s < a.B; s += kThreads) {
+        l_lru[s] = g_lru[s];
+        l_slotpos[s] = g_slotpos[s];
+      }
     }
     for (int i = tid; i < (1 << a.hcap_log2); i += kThreads) l_hkey[i] = -1;
   }
-  const int i0 = w * a.ks;
-  const int n = worker ? max(0, min(a.k, i0 + a.ks) - i0) : 0;
-  if (worker) pt_worker_classify(a, r, i0, n, newest, smem, L);
+  if (worker) pt_worker_classify(a, r, i0, n, newest, first, smem, L);
   cluster_arrive_release();  // #0: slices ready for the leader
 
   // Workers read their misses' records into registers now, before any victim
@@ -1109,17 +1127,21 @@ __global__ void __launch_bounds__(128) writeback_kernel(const WritebackArgs a) {
   const int nreq = a.num_reqs ? min(*a.num_reqs, a.R) : a.R;
   if (r >= nreq) return;
   const int32_t p = a.pos[static_cast<int64_t>(li) * a.R + r];
-  if (p < 0) return;
-  if (p >= a.P) {
-    if (threadIdx.x == 0) atomicOr(a.status, HISPARSE_ERR_RANGE);
-    return;
-  }
   const LayerDev &Ld = a.layers[a.layer0 + li];
-  const uint4 *s = reinterpret_cast<const uint4 *>(Ld.hot + static_cast<int64_t>(r) * Ld.hot_req_stride +
-                                                   static_cast<int64_t>(a.B) * Ld.hot_row_stride);
+  uint4 *row = reinterpret_cast<uint4 *>(Ld.hot + static_cast<int64_t>(r) * Ld.hot_req_stride +
+                                         static_cast<int64_t>(a.B) * Ld.hot_row_stride);
+  const bool wb = p >= 0 && p < a.P;
+  if (p >= a.P && threadIdx.x == 0) atomicOr(a.status, HISPARSE_ERR_RANGE);
   uint4 *d = reinterpret_cast<uint4 *>(Ld.host_w + static_cast<int64_t>(r) * Ld.host_req_stride +
-                                       static_cast<int64_t>(p) * Ld.host_row_stride);
-  for (int c = threadIdx.x; c < a.rec16; c += blockDim.x) st_v4(d + c, s[c]);
+                                       static_cast<int64_t>(wb ? p : 0) * Ld.host_row_stride);
+  const uint4 *nr = a.new_rows ? reinterpret_cast<const uint4 *>(
+                                     a.new_rows + (static_cast<int64_t>(li) * a.R + r) * a.rec16 * 16)
+                               : nullptr;
+  // each thread moves its own chunks: old row B out first, then the new token in
+  for (int c = threadIdx.x; c < a.rec16; c += blockDim.x) {
+    if (wb) st_v4(d + c, row[c]);
+    if (nr) row[c] = nr[c];
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -1356,13 +1378,18 @@ const char *hisparse_strerror(int code) {
 }
 
 int hisparse_host_alloc(size_t bytes, void **out) {
+  return hisparse_host_alloc_kind(bytes, HISPARSE_HOST_HUGE, out);
+}
+
+int hisparse_host_alloc_kind(size_t bytes, int32_t kind, void **out) {
   if (!out || bytes == 0) return HISPARSE_EINVAL;
+  if (kind != HISPARSE_HOST_HUGE && kind != HISPARSE_HOST_PINNED) return HISPARSE_EINVAL;
   *out = nullptr;
   // Large pools: transparent-huge-page backed memory registered with the GPU.
   // The GPU then maps the pool with large pages, so random record fetches
   // miss its address-translation caches far less often than with
   // cudaHostAlloc's base-page mappings.
-  const size_t hp = thp_bytes();
+  const size_t hp = kind == HISPARSE_HOST_HUGE ? thp_bytes() : 0;
   if (hp && bytes >= hp) {
     const size_t sz = (bytes + hp - 1) / hp * hp;
     void *p = nullptr;
@@ -1680,14 +1707,16 @@ int hisparse_resolve(hisparse_handle *h, int32_t layer, const int32_t *d_sel,
 }
 
 int hisparse_writeback(hisparse_handle *h, int32_t layer, const int32_t *d_pos,
-                       const int32_t *d_num_reqs, void *stream) {
+                       const void *d_new_rows, const int32_t *d_num_reqs, void *stream) {
   if (!h || !d_pos) return HISPARSE_EINVAL;
   if (layer != -1 && layer_ok(h, layer)) return HISPARSE_EINVAL;
+  if (d_new_rows && !aligned16(d_new_rows)) return HISPARSE_EINVAL;
   WritebackArgs a;
   a.layers = h->d_layers;
   a.layer0 = layer == -1 ? 0 : layer;
   a.R = h->R; a.B = h->B; a.rec16 = h->rec / 16; a.P = h->P;
   a.pos = d_pos; a.num_reqs = d_num_reqs; a.status = h->d_status;
+  a.new_rows = static_cast<const char *>(d_new_rows);
   const dim3 grid(h->R, layer == -1 ? h->L : 1);
   writeback_kernel<<<grid, 128, 0, static_cast<cudaStream_t>(stream)>>>(a);
   HS_CUDA(cudaGetLastError());

@@ -14,6 +14,7 @@ OK, EINVAL, EBOUND, ENOMEM, ECUDA, EROLE = 0, -1, -2, -3, -4, -5
 ERR_RANGE, ERR_DUP = 1, 2
 RECORD_PLAN, SKIP_IO, FROM_MIRROR = 1, 2, 4
 LOOKUP_PAGE_TABLE, LOOKUP_HASH = 0, 1
+HOST_HUGE, HOST_PINNED = 0, 1
 
 _i32, _i64, _u32, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_void_p
 
@@ -43,7 +44,7 @@ SIGNATURES = [
                              ctypes.POINTER(_vp)]),
     ("hisparse_destroy", _i32, [_vp]),
     ("hisparse_resolve", _i32, [_vp, _i32, _vp, _vp, _vp, _vp, _u32, _vp]),
-    ("hisparse_writeback", _i32, [_vp, _i32, _vp, _vp, _vp]),
+    ("hisparse_writeback", _i32, [_vp, _i32, _vp, _vp, _vp, _vp]),
     ("hisparse_prefetch_plan", _i32, [_vp, _i32, _i32, _vp, _vp]),
     ("hisparse_copy_miss_counts", _i32, [_vp, _i32, _vp, _vp]),
     ("hisparse_get_status", _i32, [_vp, ctypes.POINTER(_u32), _vp]),
@@ -54,6 +55,7 @@ SIGNATURES = [
     ("hisparse_get_info", _i32, [_vp, ctypes.POINTER(Info)]),
     ("hisparse_host_alloc", _i32, [ctypes.c_size_t, ctypes.POINTER(_vp)]),
     ("hisparse_host_free", _i32, [_vp]),
+    ("hisparse_host_alloc_kind", _i32, [ctypes.c_size_t, _i32, ctypes.POINTER(_vp)]),
     ("hisparse_host_hugepage_bytes", _i32, [_vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]),
     ("hisparse_last_cuda_error", _i32, []),
     ("hisparse_strerror", ctypes.c_char_p, [_i32]),
@@ -112,8 +114,8 @@ def hisparse_resolve(h, layer, d_sel, d_num_reqs, d_newest, d_out, flags, stream
     return load().hisparse_resolve(h, layer, d_sel, d_num_reqs, d_newest, d_out, flags, stream)
 
 
-def hisparse_writeback(h, layer, d_pos, d_num_reqs, stream):
-    return load().hisparse_writeback(h, layer, d_pos, d_num_reqs, stream)
+def hisparse_writeback(h, layer, d_pos, d_new_rows, d_num_reqs, stream):
+    return load().hisparse_writeback(h, layer, d_pos, d_new_rows, d_num_reqs, stream)
 
 
 def hisparse_prefetch_plan(h, anchor_layer, follower_layer, d_num_reqs, stream):
@@ -155,6 +157,12 @@ def hisparse_get_info(h):
 def hisparse_host_alloc(nbytes):
     p = _vp()
     rc = load().hisparse_host_alloc(nbytes, ctypes.byref(p))
+    return rc, p.value
+
+
+def hisparse_host_alloc_kind(nbytes, kind):
+    p = _vp()
+    rc = load().hisparse_host_alloc_kind(nbytes, kind, ctypes.byref(p))
     return rc, p.value
 
 

@@ -29,9 +29,9 @@ from . import hisparse as H
 class HostPool:
     """Pinned + mapped host memory of exactly ``nbytes`` (freed by ``close``)."""
 
-    def __init__(self, nbytes):
-        rc, ptr = H.hisparse_host_alloc(int(nbytes))
-        H.check(rc, f"hisparse_host_alloc({nbytes})")
+    def __init__(self, nbytes, kind=H.HOST_HUGE):
+        rc, ptr = H.hisparse_host_alloc_kind(int(nbytes), kind)
+        H.check(rc, f"hisparse_host_alloc_kind({nbytes}, {kind})")
         self.ptr = ptr
         self.nbytes = int(nbytes)
 
@@ -90,9 +90,9 @@ class HiSparse:
         H.check(H.hisparse_resolve(self.h, layer, _ptr(sel), _ptr(num_reqs), _ptr(newest),
                                    _ptr(out), flags, _stream(stream)), "hisparse_resolve")
 
-    def writeback(self, layer, pos, num_reqs=None, stream=None):
-        H.check(H.hisparse_writeback(self.h, layer, _ptr(pos), _ptr(num_reqs), _stream(stream)),
-                "hisparse_writeback")
+    def writeback(self, layer, pos, num_reqs=None, stream=None, new_rows=None):
+        H.check(H.hisparse_writeback(self.h, layer, _ptr(pos), _ptr(new_rows), _ptr(num_reqs),
+                                     _stream(stream)), "hisparse_writeback")
 
     def prefetch_plan(self, anchor, follower, num_reqs=None, stream=None):
         H.check(H.hisparse_prefetch_plan(self.h, anchor, follower, _ptr(num_reqs),
@@ -154,11 +154,11 @@ class WorkloadMemory:
     Hot buffer of layer l: ``hot[l]`` (uint8 [R][B+1][rec], device).
     """
 
-    def __init__(self, R, L, B, P, rec, device="cuda", mirror=False):
+    def __init__(self, R, L, B, P, rec, device="cuda", mirror=False, pool_kind=H.HOST_HUGE):
         self.R, self.L, self.B, self.P, self.rec = R, L, B, P, rec
         self.req_stride = P * rec
         self.layer_stride = R * P * rec
-        self.pool = HostPool(L * self.layer_stride)
+        self.pool = HostPool(L * self.layer_stride, kind=pool_kind)
         self.hot = torch.zeros((L, R, B + 1, rec), dtype=torch.uint8, device=device)
         self.mirror = None
         if mirror:
@@ -211,6 +211,10 @@ class DecodeStep:
         self.ev_follow = [[torch.cuda.Event() for _ in f] for _, f in groups]
         self.ev_step_start = torch.cuda.Event()
         self.ev_side_done = torch.cuda.Event()
+        self._nopos = torch.full((hs.L, hs.R), -1, dtype=torch.int32, device=mem.hot.device)
+
+    def _no_pos(self):
+        return self._nopos
 
     def issue(self, sel, out, newest=None, wb_pos=None, new_rows=None):
         """Enqueue one step on the instance's streams (returns immediately)."""
@@ -218,14 +222,15 @@ class DecodeStep:
         cur = torch.cuda.current_stream()
         self.ev_step_start.record(cur)
         self.compute.wait_event(self.ev_step_start)
-        if wb_pos is not None:
+        if wb_pos is not None or new_rows is not None:
+            # one launch writes row B of every layer through to the host and
+            # then places the new token's KV there ([DD] §3.4 step 4)
             self.backup.wait_event(self.ev_step_start)
-            hs.writeback(-1, wb_pos, self.num_reqs, stream=self.backup)
+            pos = wb_pos if wb_pos is not None else self._no_pos()
+            hs.writeback(-1, pos, self.num_reqs, stream=self.backup, new_rows=new_rows)
             self.ev_wb.record(self.backup)
             self.compute.wait_event(self.ev_wb)
         with torch.cuda.stream(self.compute):
-            if new_rows is not None:
-                mem.hot[:, :, mem.B, :].copy_(new_rows, non_blocking=True)
             for gi, (anchor, followers) in enumerate(self.groups):
                 f = self.flags | (H.RECORD_PLAN if followers else 0)
                 hs.resolve(anchor, sel[gi], out[gi], self.num_reqs, newest, f, stream=self.compute)

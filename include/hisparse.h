@@ -172,14 +172,16 @@ int hisparse_resolve(hisparse_handle *h, int32_t layer, const int32_t *d_sel,
 
 /* Write-through of the newest row ([DD] §3.4 step 4, §5.4 eager backup):
  * for r < *d_num_reqs with d_pos[r] >= 0, copy hot row B of (layer, r) to
- * host row d_pos[r] of (layer, r).  layer == -1 does every layer in one
- * launch (d_pos is then [L][R]).  Positions >= P set HISPARSE_ERR_RANGE in
- * the status word and are skipped.  Run it on a backup stream and make the
- * compute stream wait on an event recorded after it before the next resolve
- * that may fetch those rows, and before row B is overwritten.
+ * host row d_pos[r] of (layer, r); then, if d_new_rows is not NULL, place the
+ * new token's KV (d_new_rows, device, [R][record_bytes] per layer, 16-byte
+ * aligned) in row B -- the old row is always read before it is replaced.
+ * layer == -1 does every layer in one launch (d_pos is then [L][R] and
+ * d_new_rows [L][R][record_bytes]).  Positions >= P set HISPARSE_ERR_RANGE in
+ * the status word and are not written back.  Make every resolve that may
+ * fetch those rows wait for this launch (same stream or an event).
  * Errors: EINVAL, ECUDA. */
 int hisparse_writeback(hisparse_handle *h, int32_t layer, const int32_t *d_pos,
-                       const int32_t *d_num_reqs, void *stream);
+                       const void *d_new_rows, const int32_t *d_num_reqs, void *stream);
 
 /* Exact prefetch for a shared-index layer ([DD] §3.6, §5.6): copy, for
  * r < *d_num_reqs, every (position, slot) of the miss plan of the anchor's
@@ -246,6 +248,20 @@ int hisparse_get_info(const hisparse_handle *h, hisparse_info *out);
  * Errors: EINVAL, ENOMEM. */
 int hisparse_host_alloc(size_t bytes, void **out);
 int hisparse_host_free(void *p);
+
+/* Host-pool kinds for hisparse_host_alloc_kind. */
+#define HISPARSE_HOST_HUGE 0   /* huge-page-backed, registered (hisparse_host_alloc) */
+#define HISPARSE_HOST_PINNED 1 /* cudaHostAlloc: driver-pinned base pages */
+
+/* hisparse_host_alloc with an explicit kind.  HUGE maps the pool with few,
+ * large translations, which is fastest for random record fetches; on a host
+ * whose GPU driver migrates GPU-hot host pages (ATS access-counter migration)
+ * such a pool can have huge pages split under it while it is in use, and the
+ * GPU then stalls in fault service.  PINNED memory is never migrated or split
+ * but costs a translation miss per first-touched 64 KB page.  The operator-side
+ * remedy for HUGE is to disable the driver's access-counter migration.
+ * Errors: EINVAL, ENOMEM. */
+int hisparse_host_alloc_kind(size_t bytes, int32_t kind, void **out);
 
 /* Bytes of [p, p + bytes) that the host kernel backs with transparent huge
  * pages (from /proc/self/smaps; whole mappings that overlap the range are

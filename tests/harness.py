@@ -16,11 +16,11 @@ from workload.traces import all_traces
 
 class Run:
     def __init__(self, w, flags=0, mirror=False, ctas_per_request=0, replay_ctas=0,
-                 num_reqs=None, oracle_bytes=True, traces=None, lookup=0):
+                 num_reqs=None, oracle_bytes=True, traces=None, lookup=0, pool_kind=0):
         self.w = w
         self.flags = flags
         dev = torch.device("cuda", 0)
-        self.mem = WorkloadMemory(w.R, w.L, w.B, w.P, w.rec, mirror=mirror)
+        self.mem = WorkloadMemory(w.R, w.L, w.B, w.P, w.rec, mirror=mirror, pool_kind=pool_kind)
         REC.fill_host_pool(w, self.mem.pool.ptr, self.mem.layer_stride, self.mem.req_stride)
         if mirror:
             self.mem.fill_mirror()
@@ -74,8 +74,9 @@ class Run:
             for l in range(w.L):
                 if t > 0:
                     self.oracle[l].writeback(self.wb_np[t, l], num_reqs=nr)
-                # the model writes row B of every (padded) row, like the GPU side
-                self.oracle[l].set_newest_rows(self.new_rows_np[t, l])
+                # the write-back launch places the new token's KV in row B of
+                # every live request
+                self.oracle[l].set_newest_rows(self.new_rows_np[t, l], num_reqs=nr)
         for gi, (a, fl) in enumerate(self.groups):
             nw = self.newest_np[t] if self.newest_np is not None else None
             out, _ = self.oracle[a].resolve(self.sel_np[t, gi], nw, num_reqs=nr, io=io)

@@ -83,7 +83,7 @@ def test_init_without_gpu_reports_cuda_error_not_crash():
 def test_calls_on_null_handle_are_rejected():
     lib = H.load()
     assert lib.hisparse_resolve(None, 0, 1, None, None, 1, 0, None) == H.EINVAL
-    assert lib.hisparse_writeback(None, 0, 1, None, None) == H.EINVAL
+    assert lib.hisparse_writeback(None, 0, 1, None, None, None) == H.EINVAL
     assert lib.hisparse_prefetch_plan(None, 0, 1, None, None) == H.EINVAL
     assert lib.hisparse_reset(None, 0, None) == H.EINVAL
     assert lib.hisparse_destroy(None) == H.EINVAL

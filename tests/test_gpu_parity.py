@@ -182,6 +182,11 @@ def test_from_mirror_bytes_identical():
              mirror=True)
 
 
+def test_cudahostalloc_pool():
+    """The same results from a driver-pinned (cudaHostAlloc) host pool."""
+    _run_all(get("dsa").scaled(R=3, groups=2, L_ctx=65536, steps=6), pool_kind=H.HOST_PINNED)
+
+
 def test_num_reqs_padding_leaves_tail_untouched():
     _run_all(get("dsa").scaled(R=5, groups=1, L_ctx=8192, steps=4), num_reqs=3)
 

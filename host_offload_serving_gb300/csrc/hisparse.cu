@@ -588,10 +588,11 @@ constexpr int kGroup = 4;        // selections a worker thread classifies per lo
 struct PtLayout {
   uint32_t w_sel, w_out, w_mi, w_mp, w_hit, w_vict, w_misc, w_bkt, w_bidx, w_ord;  // worker
   uint32_t l_lru, l_slotpos, l_hit, l_newlru, l_ev, l_mpos, l_hkey, l_misc;     // leader
+  uint32_t l_prevrow;                                                             // leader
   uint32_t cnt, total;
 };
 
-__host__ __device__ inline PtLayout pt_layout(int k, int B, int ks, int hcap) {
+__host__ __device__ inline PtLayout pt_layout(int k, int B, int ks, int hcap, int rec) {
   PtLayout L;
   uint32_t o = 0;
   const uint32_t nwords = (B + 31) / 32;
@@ -614,6 +615,7 @@ __host__ __device__ inline PtLayout pt_layout(int k, int B, int ks, int hcap) {
   L.l_hkey = o;    o += align16(4u * hcap);
   L.l_misc = o;    o += align16(4u * (8 + kMaxWorkers + 1));
   L.cnt = o;       o += align16(4u * 64);
+  L.l_prevrow = o; o += align16(static_cast<uint32_t>(rec));
   L.total = o;
   return L;
 }
@@ -625,6 +627,15 @@ enum { kLErr = 0, kLM = 1, kLHits = 2, kLPrefix = 8 };
 struct PtArgs {
   int32_t R, k, B, rec16, io, ks, hcap_log2;
   int32_t bucket_shift, nbuckets;  // host-row buckets for the fetch order
+  // Fused write-through (hisparse_resolve_step): the previous token's row B
+  // goes to host row prev_pos[r], then new_rows[r] replaces it.  With
+  // prev_from_row the previous token, if selected, is filled from row B
+  // (which is what the host row now holds) instead of being read back.
+  const int32_t *prev_pos;
+  const char *new_rows;
+  char *host_w;
+  int64_t host_req_stride, host_row_stride;
+  int32_t prev_from_row;
   int64_t P;
   const int32_t *sel, *num_reqs, *newest;
   int32_t *out;
@@ -937,7 +948,8 @@ __device__ void pt_leader_decide(const PtArgs &a, int cs, int nw, int32_t newest
 
 // Leader: publish page table, slot map, LRU order, counts, plan.
 template <bool kRecordPlan>
-__device__ void pt_leader_publish(const PtArgs &a, int r, unsigned char *smem, const PtLayout &L) {
+__device__ void pt_leader_publish(const PtArgs &a, int r, int32_t skip_pos, unsigned char *smem,
+                                  const PtLayout &L) {
   const int tid = threadIdx.x;
   const int B = a.B, k = a.k;
   const int64_t P = a.P;
@@ -959,6 +971,21 @@ __device__ void pt_leader_publish(const PtArgs &a, int r, unsigned char *smem, c
   const int M = static_cast<int>(l_misc[kLM]);
   int32_t *g_pt = a.page_table + static_cast<int64_t>(r) * P;
   int32_t *g_slotpos = a.slot_pos + static_cast<int64_t>(r) * B;
+  if (skip_pos >= 0 && a.io) {  // the previous token's record, from the kept row B
+    __shared__ int32_t s_prev_victim;
+    if (tid == 0) s_prev_victim = -1;
+    __syncthreads();
+    for (int g = tid; g < M; g += kThreads)
+      if (l_mpos[g] == skip_pos) s_prev_victim = l_ev[g];
+    __syncthreads();
+    const int32_t pv = s_prev_victim;
+    if (pv >= 0) {
+      const uint4 *keep = reinterpret_cast<const uint4 *>(smem + L.l_prevrow);
+      uint4 *row = reinterpret_cast<uint4 *>(a.hot + static_cast<int64_t>(r) * a.hot_req_stride +
+                                             static_cast<int64_t>(pv) * a.hot_row_stride);
+      for (int c = tid; c < a.rec16; c += kThreads) st_v4(row + c, keep[c]);
+    }
+  }
   for (int g = tid; g < M; g += kThreads) {
     const int32_t v = l_ev[g], p = l_mpos[g], old = l_slotpos[v];
     if (old >= 0) g_pt[old] = -1;
@@ -978,6 +1005,85 @@ __device__ void pt_leader_publish(const PtArgs &a, int r, unsigned char *smem, c
   }
 }
 
+// Worker, after the leader's decision: fetch victims' indices, store the
+// staged records (and read + store the rest), write the slice's slot vector.
+// With a cluster this also arrives at barrier #2 once the leader's memory is
+// no longer needed.
+__device__ void pt_worker_finish(const PtArgs &a, int r, int w, int i0, int n, int32_t skip_pos,
+                                 bool staged, const uint4 *v, const char *src, char *dst,
+                                 unsigned char *smem, const PtLayout &L) {
+  const int tid = threadIdx.x;
+  const bool cluster = v != nullptr;
+  const uint32_t *l_misc = reinterpret_cast<const uint32_t *>(smem + L.l_misc);
+  const int32_t *l_ev = reinterpret_cast<const int32_t *>(smem + L.l_ev);
+  int32_t *w_vict = reinterpret_cast<int32_t *>(smem + L.w_vict);
+  const int32_t *w_out = reinterpret_cast<const int32_t *>(smem + L.w_out);
+  const int32_t *w_mi = reinterpret_cast<const int32_t *>(smem + L.w_mi);
+  const int32_t *w_mp = reinterpret_cast<const int32_t *>(smem + L.w_mp);
+  const int32_t *w_ord = reinterpret_cast<const int32_t *>(smem + L.w_ord);
+  const uint32_t *w_misc = reinterpret_cast<const uint32_t *>(smem + L.w_misc);
+  const int mw = static_cast<int>(w_misc[kWCount]);
+  const int64_t totc = static_cast<int64_t>(mw) * a.rec16;
+  const uint32_t err = ld_dsmem_u32(dsmem_addr(&l_misc[kLErr], 0));
+  if (!err) {
+    const int pre = static_cast<int>(ld_dsmem_u32(dsmem_addr(&l_misc[kLPrefix + w], 0)));
+    const uint32_t ev0 = dsmem_addr(l_ev, 0);
+    for (int j = tid; j < mw; j += kThreads)
+      w_vict[j] = static_cast<int32_t>(ld_dsmem_u32(ev0 + 4u * static_cast<uint32_t>(pre + j)));
+  }
+  __syncthreads();
+  if (cluster) cluster_arrive_relaxed();  // #2: done with the leader's memory
+  if (!err && a.io) {
+    int64_t start = 0;
+    if (staged) {
+#pragma unroll
+      for (int u = 0; u < kStage; ++u) {
+        const int64_t q = tid + static_cast<int64_t>(u) * kThreads;
+        if (q < totc) {
+          const uint32_t q32 = static_cast<uint32_t>(q);
+          const int f = static_cast<int>(q32 / static_cast<uint32_t>(a.rec16));
+          const int o = static_cast<int>(q32 - static_cast<uint32_t>(f) * a.rec16);
+          if (w_mp[w_ord[f]] != skip_pos)
+            st_v4(dst + static_cast<int64_t>(w_vict[w_ord[f]]) * a.hot_row_stride + 16 * o, v[u]);
+        }
+      }
+      start = static_cast<int64_t>(kStage) * kThreads;
+    }
+    // whatever was not staged, in host-row order
+    for (int64_t b0 = start + tid; b0 < totc; b0 += static_cast<int64_t>(kThreads) * kUnroll) {
+      uint4 x[kUnroll];
+      char *d[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int64_t q = b0 + static_cast<int64_t>(u) * kThreads;
+        d[u] = nullptr;
+        if (q < totc) {
+          const uint32_t q32 = static_cast<uint32_t>(q);
+          const int f = static_cast<int>(q32 / static_cast<uint32_t>(a.rec16));
+          const int o = static_cast<int>(q32 - static_cast<uint32_t>(f) * a.rec16);
+          const int j = w_ord[f];
+          if (w_mp[j] != skip_pos) {
+            x[u] = ld_nc_v4(src + static_cast<int64_t>(w_mp[j]) * a.src_row_stride + 16 * o);
+            d[u] = dst + static_cast<int64_t>(w_vict[j]) * a.hot_row_stride + 16 * o;
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u)
+        if (d[u]) st_v4(d[u], x[u]);
+    }
+  }
+  // the slice's slot vector ([DD] §3.5 stage 5: aligned with the list)
+  int32_t *g_out = a.out + static_cast<int64_t>(r) * a.k + i0;
+  for (int t = tid; t < n; t += kThreads) {
+    const int32_t val = w_out[t];
+    if (err) g_out[t] = -1;
+    else if (val != kUnresolved) g_out[t] = val;
+  }
+  if (!err)
+    for (int j = tid; j < mw; j += kThreads) g_out[w_mi[j]] = w_vict[j];
+}
+
 template <bool kRecordPlan>
 __global__ void __launch_bounds__(kThreads, 1) resolve_pt_kernel(const PtArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
@@ -989,7 +1095,7 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_pt_kernel(const PtArgs a)
   const bool leader = rank == 0;
   const bool worker = cs == 1 || rank > 0;
   const int w = cs == 1 ? 0 : rank - 1;
-  const PtLayout L = pt_layout(a.k, a.B, a.ks, 1 << a.hcap_log2);
+  const PtLayout L = pt_layout(a.k, a.B, a.ks, 1 << a.hcap_log2, a.rec16 * 16);
   const int i0 = w * a.ks;
   const int n = worker ? max(0, min(a.k, i0 + a.ks) - i0) : 0;
   // The first loads of every role go out together with the batch-size and
@@ -1002,8 +1108,32 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_pt_kernel(const PtArgs a)
     first[u] = (worker && t < n) ? a.sel[static_cast<int64_t>(r) * a.k + i0 + t] : -1;
   }
   const int32_t newest = a.newest ? a.newest[r] : -1;
+  const int32_t prev = a.prev_pos ? a.prev_pos[r] : -1;
   const int nreq = a.num_reqs ? min(*a.num_reqs, a.R) : a.R;
   if (r >= nreq) return;  // graph padding: every CTA of the cluster leaves
+  // the previous token's record, when filled from row B, is not read from the host
+  const int32_t skip_pos = (a.prev_from_row && prev >= 0) ? prev : -2;
+
+  if (leader && (a.prev_pos || a.new_rows)) {
+    // fused write-through ([DD] §3.4 step 4): row B -> host row prev, then the
+    // new token's KV -> row B; each thread reads a chunk before replacing it
+    uint4 *rowb = reinterpret_cast<uint4 *>(a.hot + static_cast<int64_t>(r) * a.hot_req_stride +
+                                            static_cast<int64_t>(a.B) * a.hot_row_stride);
+    uint4 *keep = reinterpret_cast<uint4 *>(smem + L.l_prevrow);
+    const bool wb = prev >= 0 && prev < a.P;
+    if (prev >= a.P && tid == 0) atomicOr(a.status, HISPARSE_ERR_RANGE);
+    uint4 *hrow = reinterpret_cast<uint4 *>(a.host_w + static_cast<int64_t>(r) * a.host_req_stride +
+                                            static_cast<int64_t>(wb ? prev : 0) * a.host_row_stride);
+    const uint4 *nrow = a.new_rows ? reinterpret_cast<const uint4 *>(
+                                         a.new_rows + static_cast<int64_t>(r) * a.rec16 * 16)
+                                   : nullptr;
+    for (int c = tid; c < a.rec16; c += kThreads) {
+      const uint4 v = rowb[c];
+      keep[c] = v;
+      if (wb) st_v4(hrow + c, v);
+      if (nrow) rowb[c] = nrow[c];
+    }
+  }
 
   if (leader) {  // the unit's LRU order and slot map, and an empty duplicate set
     int16_t *l_lru = reinterpret_cast<int16_t *>(smem + L.l_lru);
@@ -1024,19 +1154,40 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_pt_kernel(const PtArgs a)
     }
     for (int i = tid; i < (1 << a.hcap_log2); i += kThreads) l_hkey[i] = -1;
   }
-  if (worker) pt_worker_classify(a, r, i0, n, newest, first, smem, L);
-  cluster_arrive_release();  // #0: slices ready for the leader
+  const char *src = a.src + static_cast<int64_t>(r) * a.src_req_stride;
+  char *dst = a.hot + static_cast<int64_t>(r) * a.hot_req_stride;
 
-  // Workers read their misses' records into registers now, before any victim
-  // is known (cs == 1: one CTA does everything in order, nothing staged).
+  if (cs == 1) {
+    // one CTA plays every role in order; nothing to overlap, nothing staged
+    pt_worker_classify(a, r, i0, n, newest, first, smem, L);
+    pt_leader_decide(a, cs, nw, newest, smem, L);
+    __syncthreads();
+    pt_leader_publish<kRecordPlan>(a, r, skip_pos, smem, L);
+    __syncthreads();
+    pt_worker_finish(a, r, w, i0, n, skip_pos, false, nullptr, src, dst, smem, L);
+    return;
+  }
+  if (leader) {
+    cluster_arrive_release();  // #0 (nothing of ours to publish yet)
+    cluster_wait_acquire();    //    the slices are ready
+    pt_leader_decide(a, cs, nw, newest, smem, L);
+    cluster_arrive_release();  // #1: the decision, for the workers
+    pt_leader_publish<kRecordPlan>(a, r, skip_pos, smem, L);
+    cluster_wait_acquire();
+    cluster_arrive_relaxed();  // #2
+    cluster_wait_acquire();    //    the workers are done with this CTA's memory
+    return;
+  }
+  // worker
+  pt_worker_classify(a, r, i0, n, newest, first, smem, L);
+  cluster_arrive_release();  // #0: the slice, for the leader
+  // Read this slice's missed records into registers now, before any victim is
+  // known: the reads fly while the leader decides.
   const int32_t *w_mp = reinterpret_cast<const int32_t *>(smem + L.w_mp);
   const int32_t *w_ord = reinterpret_cast<const int32_t *>(smem + L.w_ord);
   const uint32_t *w_misc = reinterpret_cast<const uint32_t *>(smem + L.w_misc);
-  const int mw = worker ? static_cast<int>(w_misc[kWCount]) : 0;
-  const int64_t totc = static_cast<int64_t>(mw) * a.rec16;
-  const char *src = a.src + static_cast<int64_t>(r) * a.src_req_stride;
-  char *dst = a.hot + static_cast<int64_t>(r) * a.hot_req_stride;
-  const bool stage = worker && cs > 1 && a.io;
+  const int64_t totc = static_cast<int64_t>(w_misc[kWCount]) * a.rec16;
+  const bool stage = a.io;
   uint4 v[kStage];
 #pragma unroll
   for (int u = 0; u < kStage; ++u) {
@@ -1045,78 +1196,15 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_pt_kernel(const PtArgs a)
       const uint32_t q32 = static_cast<uint32_t>(q);
       const int f = static_cast<int>(q32 / static_cast<uint32_t>(a.rec16));
       const int o = static_cast<int>(q32 - static_cast<uint32_t>(f) * a.rec16);
-      v[u] = ld_nc_v4(src + static_cast<int64_t>(w_mp[w_ord[f]]) * a.src_row_stride + 16 * o);
+      const int32_t pm = w_mp[w_ord[f]];
+      if (pm != skip_pos) v[u] = ld_nc_v4(src + static_cast<int64_t>(pm) * a.src_row_stride + 16 * o);
     }
   }
   cluster_wait_acquire();
-
-  if (leader) pt_leader_decide(a, cs, nw, newest, smem, L);
-  cluster_arrive_release();  // #1: decision ready for the workers
-  if (leader) pt_leader_publish<kRecordPlan>(a, r, smem, L);
-  cluster_wait_acquire();
-
-  if (worker) {
-    const uint32_t *l_misc = reinterpret_cast<const uint32_t *>(smem + L.l_misc);
-    const int32_t *l_ev = reinterpret_cast<const int32_t *>(smem + L.l_ev);
-    int32_t *w_vict = reinterpret_cast<int32_t *>(smem + L.w_vict);
-    const int32_t *w_out = reinterpret_cast<const int32_t *>(smem + L.w_out);
-    const int32_t *w_mi = reinterpret_cast<const int32_t *>(smem + L.w_mi);
-    const uint32_t err = ld_dsmem_u32(dsmem_addr(&l_misc[kLErr], 0));
-    if (!err) {
-      const int pre = static_cast<int>(ld_dsmem_u32(dsmem_addr(&l_misc[kLPrefix + w], 0)));
-      const uint32_t ev0 = dsmem_addr(l_ev, 0);
-      for (int j = tid; j < mw; j += kThreads)
-        w_vict[j] = static_cast<int32_t>(ld_dsmem_u32(ev0 + 4u * static_cast<uint32_t>(pre + j)));
-    }
-    __syncthreads();
-    cluster_arrive_relaxed();  // #2: done with the leader's memory
-    if (!err && a.io) {
-      // the staged chunks, then whatever did not fit in registers
-#pragma unroll
-      for (int u = 0; u < kStage; ++u) {
-        const int64_t q = tid + static_cast<int64_t>(u) * kThreads;
-        if (stage && q < totc) {
-          const uint32_t q32 = static_cast<uint32_t>(q);
-          const int f = static_cast<int>(q32 / static_cast<uint32_t>(a.rec16));
-          const int o = static_cast<int>(q32 - static_cast<uint32_t>(f) * a.rec16);
-          st_v4(dst + static_cast<int64_t>(w_vict[w_ord[f]]) * a.hot_row_stride + 16 * o, v[u]);
-        }
-      }
-      const int64_t start = stage ? static_cast<int64_t>(kStage) * kThreads : 0;
-      for (int64_t b0 = start + tid; b0 < totc; b0 += static_cast<int64_t>(kThreads) * kUnroll) {
-        uint4 x[kUnroll];
-        char *d[kUnroll];
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-          const int64_t q = b0 + static_cast<int64_t>(u) * kThreads;
-          d[u] = nullptr;
-          if (q < totc) {
-            const uint32_t q32 = static_cast<uint32_t>(q);
-            const int f = static_cast<int>(q32 / static_cast<uint32_t>(a.rec16));
-            const int o = static_cast<int>(q32 - static_cast<uint32_t>(f) * a.rec16);
-            const int j = w_ord[f];
-            x[u] = ld_nc_v4(src + static_cast<int64_t>(w_mp[j]) * a.src_row_stride + 16 * o);
-            d[u] = dst + static_cast<int64_t>(w_vict[j]) * a.hot_row_stride + 16 * o;
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u)
-          if (d[u]) st_v4(d[u], x[u]);
-      }
-    }
-    // the slice's slot vector ([DD] §3.5 stage 5: aligned with the list)
-    int32_t *g_out = a.out + static_cast<int64_t>(r) * a.k + i0;
-    for (int t = tid; t < n; t += kThreads) {
-      const int32_t val = w_out[t];
-      if (err) g_out[t] = -1;
-      else if (val != kUnresolved) g_out[t] = val;
-    }
-    if (!err)
-      for (int j = tid; j < mw; j += kThreads) g_out[w_mi[j]] = w_vict[j];
-  } else {
-    cluster_arrive_relaxed();
-  }
-  cluster_wait_acquire();  // the leader's memory outlives every reader
+  cluster_arrive_release();  // #1
+  cluster_wait_acquire();    //    the leader's decision is visible
+  pt_worker_finish(a, r, w, i0, n, skip_pos, stage, v, src, dst, smem, L);
+  cluster_wait_acquire();    // #2 completes: the leader may leave
 }
 
 // ---------------------------------------------------------------------------
@@ -1270,7 +1358,7 @@ int slice_size(int k, int cs) {
 
 uint32_t resolve_smem(const hisparse_handle *h, int cs) {
   if (h->lookup == HISPARSE_LOOKUP_HASH) return smem_layout(h->k, h->B, 1 << h->cap_log2).total;
-  return pt_layout(h->k, h->B, slice_size(h->k, cs), 1 << h->cap_log2).total;
+  return pt_layout(h->k, h->B, slice_size(h->k, cs), 1 << h->cap_log2, h->rec).total;
 }
 
 // Choose the cluster size: as many CTAs per request as the GPU can run at once
@@ -1645,7 +1733,16 @@ int hisparse_reset(hisparse_handle *h, int32_t layer, void *stream) {
 int hisparse_resolve(hisparse_handle *h, int32_t layer, const int32_t *d_sel,
                      const int32_t *d_num_reqs, const int32_t *d_newest, int32_t *d_out,
                      uint32_t flags, void *stream) {
+  return hisparse_resolve_step(h, layer, d_sel, d_num_reqs, d_newest, nullptr, nullptr, d_out,
+                               flags, stream);
+}
+
+int hisparse_resolve_step(hisparse_handle *h, int32_t layer, const int32_t *d_sel,
+                          const int32_t *d_num_reqs, const int32_t *d_newest,
+                          const int32_t *d_prev_pos, const void *d_new_rows, int32_t *d_out,
+                          uint32_t flags, void *stream) {
   if (layer_ok(h, layer)) return HISPARSE_EINVAL;
+  if (d_new_rows && !aligned16(d_new_rows)) return HISPARSE_EINVAL;
   if (!d_sel || !d_out) return HISPARSE_EINVAL;
   if (flags & ~(HISPARSE_RECORD_PLAN | HISPARSE_SKIP_IO | HISPARSE_FROM_MIRROR)) return HISPARSE_EINVAL;
   if (h->anchor_of[layer] != -1) return HISPARSE_EROLE;
@@ -1668,6 +1765,11 @@ int hisparse_resolve(hisparse_handle *h, int32_t layer, const int32_t *d_sel,
   lc.numAttrs = 1;
   cudaError_t e;
   if (h->lookup == HISPARSE_LOOKUP_HASH) {
+    if (d_prev_pos || d_new_rows) {  // the hash kernel has no fused write-through
+      if (!d_prev_pos) return HISPARSE_EINVAL;
+      const int rc = hisparse_writeback(h, layer, d_prev_pos, d_new_rows, d_num_reqs, stream);
+      if (rc != HISPARSE_OK) return rc;
+    }
     ResolveArgs a;
     a.R = h->R; a.k = h->k; a.B = h->B; a.cap_log2 = h->cap_log2; a.rec16 = h->rec / 16;
     a.io = (flags & HISPARSE_SKIP_IO) ? 0 : 1;
@@ -1691,6 +1793,12 @@ int hisparse_resolve(hisparse_handle *h, int32_t layer, const int32_t *d_sel,
     a.ks = h->ks; a.hcap_log2 = h->cap_log2;
     a.bucket_shift = h->bucket_shift[layer];
     a.nbuckets = h->nbuckets[layer];
+    a.prev_pos = d_prev_pos;
+    a.new_rows = static_cast<const char *>(d_new_rows);
+    a.host_w = Ld.host_w;
+    a.host_req_stride = Ld.host_req_stride;
+    a.host_row_stride = Ld.host_row_stride;
+    a.prev_from_row = (d_prev_pos && !(flags & HISPARSE_FROM_MIRROR)) ? 1 : 0;
     a.P = h->P;
     a.sel = d_sel; a.num_reqs = d_num_reqs; a.newest = d_newest; a.out = d_out;
     a.slot_pos = m.slot_pos; a.lru = m.lru; a.page_table = m.page_table;

@@ -90,6 +90,12 @@ class HiSparse:
         H.check(H.hisparse_resolve(self.h, layer, _ptr(sel), _ptr(num_reqs), _ptr(newest),
                                    _ptr(out), flags, _stream(stream)), "hisparse_resolve")
 
+    def resolve_step(self, layer, sel, out, num_reqs=None, newest=None, prev_pos=None,
+                     new_rows=None, flags=0, stream=None):
+        H.check(H.hisparse_resolve_step(self.h, layer, _ptr(sel), _ptr(num_reqs), _ptr(newest),
+                                        _ptr(prev_pos), _ptr(new_rows), _ptr(out), flags,
+                                        _stream(stream)), "hisparse_resolve_step")
+
     def writeback(self, layer, pos, num_reqs=None, stream=None, new_rows=None):
         H.check(H.hisparse_writeback(self.h, layer, _ptr(pos), _ptr(new_rows), _ptr(num_reqs),
                                      _stream(stream)), "hisparse_writeback")
@@ -197,12 +203,20 @@ class DecodeStep:
     write back first), ``new_rows[t]`` uint8 [L][R][rec] or None (the new
     token's KV, placed in row B), and ``out`` int32 [Lr][R][k] receives the slot
     vectors.
+
+    ``fused=True`` (default) writes each anchor's previous token through, and
+    installs its new token, inside that anchor's RESOLVE launch
+    (``hisparse_resolve_step``); shared-index layers get a write-back launch on
+    the side stream ahead of their replays.  ``fused=False`` issues one
+    ``hisparse_writeback`` for every layer on a backup stream first, as the
+    pages describe (gentlecold.top "HiSparse 深度解析" §5.4).
     """
 
-    def __init__(self, hs, mem, groups, flags=0, num_reqs=None):
+    def __init__(self, hs, mem, groups, flags=0, num_reqs=None, fused=True):
         self.hs, self.mem, self.groups = hs, mem, groups
         self.flags = flags
         self.num_reqs = num_reqs
+        self.fused = fused
         self.compute = torch.cuda.Stream()
         self.backup = torch.cuda.Stream()
         self.side = torch.cuda.Stream()
@@ -218,32 +232,36 @@ class DecodeStep:
 
     def issue(self, sel, out, newest=None, wb_pos=None, new_rows=None):
         """Enqueue one step on the instance's streams (returns immediately)."""
-        hs, mem = self.hs, self.mem
+        hs = self.hs
         cur = torch.cuda.current_stream()
         self.ev_step_start.record(cur)
         self.compute.wait_event(self.ev_step_start)
-        if wb_pos is not None or new_rows is not None:
+        through = wb_pos is not None or new_rows is not None
+        pos = wb_pos if wb_pos is not None else self._no_pos()
+        if through and not self.fused:
             # one launch writes row B of every layer through to the host and
             # then places the new token's KV there ([DD] §3.4 step 4)
             self.backup.wait_event(self.ev_step_start)
-            pos = wb_pos if wb_pos is not None else self._no_pos()
             hs.writeback(-1, pos, self.num_reqs, stream=self.backup, new_rows=new_rows)
             self.ev_wb.record(self.backup)
             self.compute.wait_event(self.ev_wb)
-        with torch.cuda.stream(self.compute):
-            for gi, (anchor, followers) in enumerate(self.groups):
-                f = self.flags | (H.RECORD_PLAN if followers else 0)
+        for gi, (anchor, followers) in enumerate(self.groups):
+            f = self.flags | (H.RECORD_PLAN if followers else 0)
+            if through and self.fused:
+                hs.resolve_step(anchor, sel[gi], out[gi], self.num_reqs, newest, pos[anchor],
+                                new_rows[anchor] if new_rows is not None else None, f,
+                                stream=self.compute)
+            else:
                 hs.resolve(anchor, sel[gi], out[gi], self.num_reqs, newest, f, stream=self.compute)
-                if followers:
-                    self.ev_anchor[gi].record(self.compute)
-                    self.side.wait_event(self.ev_anchor[gi])
-                    for fi, fl in enumerate(followers):
-                        hs.prefetch_plan(anchor, fl, self.num_reqs, stream=self.side)
-                        self.ev_follow[gi][fi].record(self.side)
-                    # the next anchor resolve rewrites the plan: it waits for the
-                    # replays of this group (only relevant within one step when
-                    # two groups share an anchor, which they do not; kept for
-                    # the next step below)
+            if followers:
+                self.ev_anchor[gi].record(self.compute)
+                self.side.wait_event(self.ev_anchor[gi])
+                for fi, fl in enumerate(followers):
+                    if through and self.fused:   # the shared layer's own write-through first
+                        hs.writeback(fl, pos[fl:fl + 1], self.num_reqs, stream=self.side,
+                                     new_rows=new_rows[fl] if new_rows is not None else None)
+                    hs.prefetch_plan(anchor, fl, self.num_reqs, stream=self.side)
+                    self.ev_follow[gi][fi].record(self.side)
         # a shared layer's attention would wait on its own event; at the end of
         # the step the caller's stream waits for everything
         for gi, (_, followers) in enumerate(self.groups):

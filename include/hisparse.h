@@ -170,6 +170,20 @@ int hisparse_resolve(hisparse_handle *h, int32_t layer, const int32_t *d_sel,
                      const int32_t *d_num_reqs, const int32_t *d_newest, int32_t *d_out,
                      uint32_t flags, void *stream);
 
+/* hisparse_writeback(h, layer, d_prev_pos, d_new_rows, d_num_reqs) followed by
+ * hisparse_resolve(h, layer, ...) for one layer that runs RESOLVE, in one
+ * launch and with identical results: row B of each request is written to
+ * host row d_prev_pos[r] (skipped for -1), d_new_rows (device [R][record_bytes],
+ * may be NULL) replaces it, and then the layer is resolved -- a previous
+ * token that is selected again is filled from the row B just written back
+ * rather than read back over the host link.  With HISPARSE_LOOKUP_HASH this
+ * is two launches (d_prev_pos must then be given).  Shared-index layers keep
+ * using hisparse_writeback.  Errors: as hisparse_resolve and hisparse_writeback. */
+int hisparse_resolve_step(hisparse_handle *h, int32_t layer, const int32_t *d_sel,
+                          const int32_t *d_num_reqs, const int32_t *d_newest,
+                          const int32_t *d_prev_pos, const void *d_new_rows, int32_t *d_out,
+                          uint32_t flags, void *stream);
+
 /* Write-through of the newest row ([DD] §3.4 step 4, §5.4 eager backup):
  * for r < *d_num_reqs with d_pos[r] >= 0, copy hot row B of (layer, r) to
  * host row d_pos[r] of (layer, r); then, if d_new_rows is not NULL, place the

@@ -16,7 +16,8 @@ from workload.traces import all_traces
 
 class Run:
     def __init__(self, w, flags=0, mirror=False, ctas_per_request=0, replay_ctas=0,
-                 num_reqs=None, oracle_bytes=True, traces=None, lookup=0, pool_kind=0):
+                 num_reqs=None, oracle_bytes=True, traces=None, lookup=0, pool_kind=0,
+                 fused=True):
         self.w = w
         self.flags = flags
         dev = torch.device("cuda", 0)
@@ -46,7 +47,7 @@ class Run:
         self.nreq_val = w.R if num_reqs is None else num_reqs
         self.num_reqs = torch.tensor([self.nreq_val], dtype=torch.int32, device=dev)
         self.step_runner = DecodeStep(self.hs, self.mem, self.groups, flags=flags,
-                                      num_reqs=self.num_reqs)
+                                      num_reqs=self.num_reqs, fused=fused)
         # oracle
         self.oracle = {}
         for l in range(w.L):

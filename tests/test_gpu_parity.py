@@ -146,8 +146,20 @@ def test_tiny_workload_every_step():
 
 @pytest.mark.parametrize("lookup", LOOKUPS)
 def test_dsa_workload_full_size_every_step(lookup):
-    """8 requests x 4 layers, 128K context, k=2048, B=4096, write-through."""
+    """8 requests x 4 layers, 128K context, k=2048, B=4096, write-through
+    fused into RESOLVE."""
     _run_all(get("dsa"), lookup=lookup)
+
+
+@pytest.mark.parametrize("lookup", LOOKUPS)
+def test_separate_writeback_launch(lookup):
+    """The write-through as its own launch on a backup stream (the pages' order)."""
+    _run_all(get("dsa").scaled(R=4, groups=2, L_ctx=32768, steps=8), lookup=lookup, fused=False)
+
+
+def test_write_through_with_shared_layers():
+    """Write-through on anchors (fused) and on shared layers (own launch)."""
+    _run_all(get("shared").scaled(R=3, groups=2, L_ctx=8192, steps=6, write_through=True))
 
 
 def test_quest_workload_scaled():

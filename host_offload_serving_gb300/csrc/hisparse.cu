@@ -948,11 +948,29 @@ __device__ void pt_leader_decide(const PtArgs &a, int cs, int nw, int32_t newest
 
 // Leader: publish page table, slot map, LRU order, counts, plan.
 template <bool kRecordPlan>
-__device__ void pt_leader_publish(const PtArgs &a, int r, int32_t skip_pos, unsigned char *smem,
-                                  const PtLayout &L) {
+__device__ void pt_leader_publish(const PtArgs &a, int r, int32_t prev, int32_t skip_pos,
+                                  unsigned char *smem, const PtLayout &L) {
   const int tid = threadIdx.x;
   const int B = a.B, k = a.k;
   const int64_t P = a.P;
+  if (a.prev_pos || a.new_rows) {
+    // fused write-through, second half: the kept row B -> host row prev, and
+    // the new token's KV -> row B (no one reads row B during this kernel)
+    const uint4 *keep = reinterpret_cast<const uint4 *>(smem + L.l_prevrow);
+    uint4 *rowb = reinterpret_cast<uint4 *>(a.hot + static_cast<int64_t>(r) * a.hot_req_stride +
+                                            static_cast<int64_t>(B) * a.hot_row_stride);
+    const bool wb = prev >= 0 && prev < P;
+    if (prev >= P && tid == 0) atomicOr(a.status, HISPARSE_ERR_RANGE);
+    uint4 *hrow = reinterpret_cast<uint4 *>(a.host_w + static_cast<int64_t>(r) * a.host_req_stride +
+                                            static_cast<int64_t>(wb ? prev : 0) * a.host_row_stride);
+    const uint4 *nrow = a.new_rows ? reinterpret_cast<const uint4 *>(
+                                         a.new_rows + static_cast<int64_t>(r) * a.rec16 * 16)
+                                   : nullptr;
+    for (int c = tid; c < a.rec16; c += kThreads) {
+      if (wb) st_v4(hrow + c, keep[c]);
+      if (nrow) rowb[c] = nrow[c];
+    }
+  }
   const int32_t *l_slotpos = reinterpret_cast<const int32_t *>(smem + L.l_slotpos);
   const int16_t *l_newlru = reinterpret_cast<const int16_t *>(smem + L.l_newlru);
   const int32_t *l_ev = reinterpret_cast<const int32_t *>(smem + L.l_ev);
@@ -1115,24 +1133,12 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_pt_kernel(const PtArgs a)
   const int32_t skip_pos = (a.prev_from_row && prev >= 0) ? prev : -2;
 
   if (leader && (a.prev_pos || a.new_rows)) {
-    // fused write-through ([DD] §3.4 step 4): row B -> host row prev, then the
-    // new token's KV -> row B; each thread reads a chunk before replacing it
-    uint4 *rowb = reinterpret_cast<uint4 *>(a.hot + static_cast<int64_t>(r) * a.hot_req_stride +
-                                            static_cast<int64_t>(a.B) * a.hot_row_stride);
+    // fused write-through ([DD] §3.4 step 4), first half: keep the previous
+    // token's row B; it goes to the host and is replaced after the decision
+    const uint4 *rowb = reinterpret_cast<const uint4 *>(
+        a.hot + static_cast<int64_t>(r) * a.hot_req_stride + static_cast<int64_t>(a.B) * a.hot_row_stride);
     uint4 *keep = reinterpret_cast<uint4 *>(smem + L.l_prevrow);
-    const bool wb = prev >= 0 && prev < a.P;
-    if (prev >= a.P && tid == 0) atomicOr(a.status, HISPARSE_ERR_RANGE);
-    uint4 *hrow = reinterpret_cast<uint4 *>(a.host_w + static_cast<int64_t>(r) * a.host_req_stride +
-                                            static_cast<int64_t>(wb ? prev : 0) * a.host_row_stride);
-    const uint4 *nrow = a.new_rows ? reinterpret_cast<const uint4 *>(
-                                         a.new_rows + static_cast<int64_t>(r) * a.rec16 * 16)
-                                   : nullptr;
-    for (int c = tid; c < a.rec16; c += kThreads) {
-      const uint4 v = rowb[c];
-      keep[c] = v;
-      if (wb) st_v4(hrow + c, v);
-      if (nrow) rowb[c] = nrow[c];
-    }
+    for (int c = tid; c < a.rec16; c += kThreads) keep[c] = rowb[c];
   }
 
   if (leader) {  // the unit's LRU order and slot map, and an empty duplicate set
@@ -1162,17 +1168,17 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_pt_kernel(const PtArgs a)
     pt_worker_classify(a, r, i0, n, newest, first, smem, L);
     pt_leader_decide(a, cs, nw, newest, smem, L);
     __syncthreads();
-    pt_leader_publish<kRecordPlan>(a, r, skip_pos, smem, L);
+    pt_leader_publish<kRecordPlan>(a, r, prev, skip_pos, smem, L);
     __syncthreads();
     pt_worker_finish(a, r, w, i0, n, skip_pos, false, nullptr, src, dst, smem, L);
     return;
   }
   if (leader) {
-    cluster_arrive_release();  // #0 (nothing of ours to publish yet)
+    cluster_arrive_relaxed();  // #0 (nothing of ours to publish yet)
     cluster_wait_acquire();    //    the slices are ready
     pt_leader_decide(a, cs, nw, newest, smem, L);
     cluster_arrive_release();  // #1: the decision, for the workers
-    pt_leader_publish<kRecordPlan>(a, r, skip_pos, smem, L);
+    pt_leader_publish<kRecordPlan>(a, r, prev, skip_pos, smem, L);
     cluster_wait_acquire();
     cluster_arrive_relaxed();  // #2
     cluster_wait_acquire();    //    the workers are done with this CTA's memory

@@ -124,9 +124,11 @@ def profile_traffic(kernel_file, kernel):
     """Per-launch traffic of `kernel` from the ncu summaries under profiles/.
 
     A summary line of the form
-      machine: kernel=<name> sha256=<kernel source sha256> dram_bytes_per_launch=<n> sysmem_bytes_per_launch=<n>
+      machine: kernel=<name> sha256=<kernel source sha256> dram_bytes_per_launch=<n> sysmem_bytes_per_launch=<n> [algorithmic_bytes_per_launch=<n>]
     counts only while the kernel source still has that hash (the counters are
-    stale once the kernel changes).
+    stale once the kernel changes).  The captured launch's own miss bytes come
+    with it: a launch's host-link traffic is in proportion to its misses, so the
+    two are compared as a ratio.
     """
     sha = hashlib.sha256(open(kernel_file, "rb").read()).hexdigest()
     pdir = os.path.join(ROOT, "profiles")
@@ -142,6 +144,8 @@ def profile_traffic(kernel_file, kernel):
             if kv.get("kernel") == kernel and kv.get("sha256") == sha:
                 return {"dram_bytes_per_launch": float(kv["dram_bytes_per_launch"]),
                         "sysmem_bytes_per_launch": float(kv["sysmem_bytes_per_launch"]),
+                        "algorithmic_bytes": (float(kv["algorithmic_bytes_per_launch"])
+                                              if "algorithmic_bytes_per_launch" in kv else None),
                         "source": name}
     return None
 
@@ -605,6 +609,7 @@ def run_ours(args):
             "traffic": prof["dram_bytes_per_launch"] if prof else None,
             "traffic_sysmem": prof["sysmem_bytes_per_launch"] if prof else None,
             "traffic_source": prof["source"] if prof else None,
+            "traffic_launch_algorithmic_bytes": prof["algorithmic_bytes"] if prof else None,
             "kernel": kname,
             "peak_source": "pinned cudaMemcpyAsync H2D, 1 GiB x 20, best of 3 rounds, same run",
             "algorithmic_bytes_per_launch": miss_bytes / (args.steps * G),

@@ -584,6 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
 constexpr int kStage = 4;        // 16-byte chunks a worker thread stages in registers
 constexpr int kMaxWorkers = 15;  // cluster size 16 at most
 constexpr int kGroup = 4;        // selections a worker thread classifies per load batch
+constexpr int kRankSortMax = 128;  // up to this many misses a slice is ordered by direct ranking
 
 struct PtLayout {
   uint32_t w_sel, w_out, w_mi, w_mp, w_hit, w_vict, w_misc, w_bkt, w_bidx, w_ord;  // worker
@@ -811,7 +812,29 @@ __device__ void pt_worker_classify(const PtArgs &a, int r, int i0, int n, int32_
   // records share the GPU's page-table walks, which matters whenever the pool
   // is not mapped with large pages.
   int32_t *w_ord = reinterpret_cast<int32_t *>(smem + L.w_ord);
-  if (mw > 1) {
+  // Ties (equal rows) only occur in a failing unit; they are broken by list
+  // index so that w_ord is always a permutation of [0, mw).
+  if (mw <= 32) {
+    if (tid < 32) {  // one warp: each lane ranks its miss against the others
+      const int32_t key = tid < mw ? w_mp[tid] : 0;
+      int rnk = 0;
+      for (int i = 0; i < mw; ++i) {
+        const int32_t ki = __shfl_sync(kFull, key, i);
+        rnk += ki < key || (ki == key && i < tid);
+      }
+      if (tid < mw) w_ord[rnk] = tid;
+    }
+  } else if (mw <= kRankSortMax) {
+    for (int j = tid; j < mw; j += kThreads) {  // rank against every miss (broadcast reads)
+      const int32_t key = w_mp[j];
+      int rnk = 0;
+      for (int i = 0; i < mw; ++i) {
+        const int32_t ki = w_mp[i];
+        rnk += ki < key || (ki == key && i < j);
+      }
+      w_ord[rnk] = j;
+    }
+  } else {  // counting sort into row buckets, then a rank inside each bucket
     int32_t *w_bkt = reinterpret_cast<int32_t *>(smem + L.w_bkt);
     int32_t *w_bidx = reinterpret_cast<int32_t *>(smem + L.w_bidx);
     const int sh = a.bucket_shift, nb = a.nbuckets;
@@ -829,11 +852,12 @@ __device__ void pt_worker_classify(const PtArgs &a, int r, int i0, int n, int32_
       const int b = p >> sh;
       const int b0 = b ? w_bkt[b - 1] : 0, b1 = w_bkt[b];
       int rnk = 0;
-      for (int x = b0; x < b1; ++x) rnk += w_mp[w_bidx[x]] < p;
+      for (int x = b0; x < b1; ++x) {
+        const int32_t px = w_mp[w_bidx[x]];
+        rnk += px < p || (px == p && x < q);
+      }
       w_ord[b0 + rnk] = j;
     }
-  } else if (tid == 0) {
-    w_ord[0] = 0;
   }
   __syncthreads();
 }
@@ -953,23 +977,12 @@ __device__ void pt_leader_publish(const PtArgs &a, int r, int32_t prev, int32_t 
   const int tid = threadIdx.x;
   const int B = a.B, k = a.k;
   const int64_t P = a.P;
-  if (a.prev_pos || a.new_rows) {
-    // fused write-through, second half: the kept row B -> host row prev, and
-    // the new token's KV -> row B (no one reads row B during this kernel)
+  if (a.prev_pos && prev >= 0 && prev < P) {
+    // fused write-through, second half: the kept row B -> host row prev
     const uint4 *keep = reinterpret_cast<const uint4 *>(smem + L.l_prevrow);
-    uint4 *rowb = reinterpret_cast<uint4 *>(a.hot + static_cast<int64_t>(r) * a.hot_req_stride +
-                                            static_cast<int64_t>(B) * a.hot_row_stride);
-    const bool wb = prev >= 0 && prev < P;
-    if (prev >= P && tid == 0) atomicOr(a.status, HISPARSE_ERR_RANGE);
     uint4 *hrow = reinterpret_cast<uint4 *>(a.host_w + static_cast<int64_t>(r) * a.host_req_stride +
-                                            static_cast<int64_t>(wb ? prev : 0) * a.host_row_stride);
-    const uint4 *nrow = a.new_rows ? reinterpret_cast<const uint4 *>(
-                                         a.new_rows + static_cast<int64_t>(r) * a.rec16 * 16)
-                                   : nullptr;
-    for (int c = tid; c < a.rec16; c += kThreads) {
-      if (wb) st_v4(hrow + c, keep[c]);
-      if (nrow) rowb[c] = nrow[c];
-    }
+                                            static_cast<int64_t>(prev) * a.host_row_stride);
+    for (int c = tid; c < a.rec16; c += kThreads) st_v4(hrow + c, keep[c]);
   }
   const int32_t *l_slotpos = reinterpret_cast<const int32_t *>(smem + L.l_slotpos);
   const int16_t *l_newlru = reinterpret_cast<const int16_t *>(smem + L.l_newlru);
@@ -1023,8 +1036,8 @@ __device__ void pt_leader_publish(const PtArgs &a, int r, int32_t prev, int32_t 
   }
 }
 
-// Worker, after the leader's decision: fetch victims' indices, store the
-// staged records (and read + store the rest), write the slice's slot vector.
+// Worker, after the leader's decision: fetch victims' indices, write the
+// slice's slot vector, store the staged records (and read + store the rest).
 // With a cluster this also arrives at barrier #2 once the leader's memory is
 // no longer needed.
 __device__ void pt_worker_finish(const PtArgs &a, int r, int w, int i0, int n, int32_t skip_pos,
@@ -1091,7 +1104,8 @@ __device__ void pt_worker_finish(const PtArgs &a, int r, int w, int i0, int n, i
         if (d[u]) st_v4(d[u], x[u]);
     }
   }
-  // the slice's slot vector ([DD] §3.5 stage 5: aligned with the list)
+  // the slice's slot vector ([DD] §3.5 stage 5: aligned with the list); it
+  // needs no record bytes, so it goes out before the staged loads land
   int32_t *g_out = a.out + static_cast<int64_t>(r) * a.k + i0;
   for (int t = tid; t < n; t += kThreads) {
     const int32_t val = w_out[t];
@@ -1100,6 +1114,55 @@ __device__ void pt_worker_finish(const PtArgs &a, int r, int w, int i0, int n, i
   }
   if (!err)
     for (int j = tid; j < mw; j += kThreads) g_out[w_mi[j]] = w_vict[j];
+}
+
+// Leader: the unit's LRU order and slot map into shared memory, and an empty
+// duplicate set.  `sp0` is this thread's first 16-byte piece of the slot map
+// when it was read ahead (vector rows only).
+__device__ void pt_leader_load_state(const PtArgs &a, int r, bool have_sp0, int4 sp0,
+                                     unsigned char *smem, const PtLayout &L) {
+  const int tid = threadIdx.x;
+  int16_t *l_lru = reinterpret_cast<int16_t *>(smem + L.l_lru);
+  int32_t *l_slotpos = reinterpret_cast<int32_t *>(smem + L.l_slotpos);
+  int32_t *l_hkey = reinterpret_cast<int32_t *>(smem + L.l_hkey);
+  const int16_t *g_lru = a.lru + static_cast<int64_t>(r) * a.B;
+  const int32_t *g_slotpos = a.slot_pos + static_cast<int64_t>(r) * a.B;
+  if (a.B % 8 == 0) {  // 16-byte rows: one vector per 8 LRU / 4 slot entries
+    const int4 *g_lru16 = reinterpret_cast<const int4 *>(g_lru);
+    const int4 *g_sp16 = reinterpret_cast<const int4 *>(g_slotpos);
+    int4 *l_lru16 = reinterpret_cast<int4 *>(l_lru);
+    int4 *l_sp16 = reinterpret_cast<int4 *>(l_slotpos);
+    for (int c = tid; c < a.B / 4; c += kThreads)
+      l_sp16[c] = (have_sp0 && c == tid) ? sp0 : g_sp16[c];
+    for (int c = tid; c < a.B / 8; c += kThreads) l_lru16[c] = g_lru16[c];
+  } else {
+    for (int s = tid; s < a.B; s += kThreads) {
+      l_lru[s] = g_lru[s];
+      l_slotpos[s] = g_slotpos[s];
+    }
+  }
+  for (int i = tid; i < (1 << a.hcap_log2); i += kThreads) l_hkey[i] = -1;
+}
+
+// Leader, fused write-through ([DD] §3.4 step 4), first half: keep the
+// previous token's row B in shared memory and put the new token's KV in its
+// place.  The kept row goes to host row prev in pt_leader_publish, after the
+// decision, so that no release on the way there waits for host stores.
+__device__ void pt_leader_write_through(const PtArgs &a, int r, int32_t prev, unsigned char *smem,
+                                        const PtLayout &L) {
+  if (!a.prev_pos && !a.new_rows) return;
+  const int tid = threadIdx.x;
+  uint4 *rowb = reinterpret_cast<uint4 *>(a.hot + static_cast<int64_t>(r) * a.hot_req_stride +
+                                          static_cast<int64_t>(a.B) * a.hot_row_stride);
+  const uint4 *nrow = a.new_rows ? reinterpret_cast<const uint4 *>(
+                                       a.new_rows + static_cast<int64_t>(r) * a.rec16 * 16)
+                                 : nullptr;
+  uint4 *keep = reinterpret_cast<uint4 *>(smem + L.l_prevrow);
+  if (prev >= a.P && tid == 0) atomicOr(a.status, HISPARSE_ERR_RANGE);
+  for (int c = tid; c < a.rec16; c += kThreads) {
+    keep[c] = rowb[c];
+    if (nrow) rowb[c] = nrow[c];
+  }
 }
 
 template <bool kRecordPlan>
@@ -1118,12 +1181,21 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_pt_kernel(const PtArgs a)
   const int n = worker ? max(0, min(a.k, i0 + a.ks) - i0) : 0;
   // The first loads of every role go out together with the batch-size and
   // newest-position reads (all are in bounds for any r < R); the padding check
-  // then costs no extra memory round trip.
-  int32_t first[kGroup];
+  // then costs no extra memory round trip.  Workers read their first
+  // selections, the leader its first 16-byte pieces of the LRU row and the
+  // slot map.
+  static_assert(kGroup == 4, "a leader keeps one 16-byte slot-map piece in first[]");
+  int32_t first[kGroup] = {-1, -1, -1, -1};
+  const bool sp_ahead = !worker && a.B % 8 == 0 && tid < a.B / 4;
+  if (worker) {
 #pragma unroll
-  for (int u = 0; u < kGroup; ++u) {
-    const int t = u * kThreads + tid;
-    first[u] = (worker && t < n) ? a.sel[static_cast<int64_t>(r) * a.k + i0 + t] : -1;
+    for (int u = 0; u < kGroup; ++u) {
+      const int t = u * kThreads + tid;
+      first[u] = t < n ? a.sel[static_cast<int64_t>(r) * a.k + i0 + t] : -1;
+    }
+  } else if (sp_ahead) {
+    const int4 v = reinterpret_cast<const int4 *>(a.slot_pos + static_cast<int64_t>(r) * a.B)[tid];
+    first[0] = v.x; first[1] = v.y; first[2] = v.z; first[3] = v.w;
   }
   const int32_t newest = a.newest ? a.newest[r] : -1;
   const int32_t prev = a.prev_pos ? a.prev_pos[r] : -1;
@@ -1132,39 +1204,13 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_pt_kernel(const PtArgs a)
   // the previous token's record, when filled from row B, is not read from the host
   const int32_t skip_pos = (a.prev_from_row && prev >= 0) ? prev : -2;
 
-  if (leader && (a.prev_pos || a.new_rows)) {
-    // fused write-through ([DD] §3.4 step 4), first half: keep the previous
-    // token's row B; it goes to the host and is replaced after the decision
-    const uint4 *rowb = reinterpret_cast<const uint4 *>(
-        a.hot + static_cast<int64_t>(r) * a.hot_req_stride + static_cast<int64_t>(a.B) * a.hot_row_stride);
-    uint4 *keep = reinterpret_cast<uint4 *>(smem + L.l_prevrow);
-    for (int c = tid; c < a.rec16; c += kThreads) keep[c] = rowb[c];
-  }
-
-  if (leader) {  // the unit's LRU order and slot map, and an empty duplicate set
-    int16_t *l_lru = reinterpret_cast<int16_t *>(smem + L.l_lru);
-    int32_t *l_slotpos = reinterpret_cast<int32_t *>(smem + L.l_slotpos);
-    int32_t *l_hkey = reinterpret_cast<int32_t *>(smem + L.l_hkey);
-    const int16_t *g_lru = a.lru + static_cast<int64_t>(r) * a.B;
-    const int32_t *g_slotpos = a.slot_pos + static_cast<int64_t>(r) * a.B;
-    if (a.B % 8 == 0) {  // 16-byte rows: one vector load per 8 LRU / 4 slot entries
-      for (int c = tid; c < a.B / 8; c += kThreads)
-        reinterpret_cast<uint4 *>(l_lru)[c] = reinterpret_cast<const uint4 *>(g_lru)[c];
-      for (int c = tid; c < a.B / 4; c += kThreads)
-        reinterpret_cast<int4 *>(l_slotpos)[c] = reinterpret_cast<const int4 *>(g_slotpos)[c];
-    } else {
-      for (int s = tid; s < a.B; s += kThreads) {
-        l_lru[s] = g_lru[s];
-        l_slotpos[s] = g_slotpos[s];
-      }
-    }
-    for (int i = tid; i < (1 << a.hcap_log2); i += kThreads) l_hkey[i] = -1;
-  }
   const char *src = a.src + static_cast<int64_t>(r) * a.src_req_stride;
   char *dst = a.hot + static_cast<int64_t>(r) * a.hot_req_stride;
 
   if (cs == 1) {
     // one CTA plays every role in order; nothing to overlap, nothing staged
+    pt_leader_load_state(a, r, false, make_int4(0, 0, 0, 0), smem, L);
+    pt_leader_write_through(a, r, prev, smem, L);
     pt_worker_classify(a, r, i0, n, newest, first, smem, L);
     pt_leader_decide(a, cs, nw, newest, smem, L);
     __syncthreads();
@@ -1174,7 +1220,13 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_pt_kernel(const PtArgs a)
     return;
   }
   if (leader) {
-    cluster_arrive_relaxed();  // #0 (nothing of ours to publish yet)
+    // #0: the leader publishes nothing here, so it arrives at once and reads
+    // its state while the workers classify their slices
+    cluster_arrive_relaxed();
+    pt_leader_load_state(a, r, sp_ahead, make_int4(first[0], first[1], first[2], first[3]), smem,
+                         L);
+    pt_leader_write_through(a, r, prev, smem, L);
+    __syncthreads();
     cluster_wait_acquire();    //    the slices are ready
     pt_leader_decide(a, cs, nw, newest, smem, L);
     cluster_arrive_release();  // #1: the decision, for the workers
@@ -1207,7 +1259,7 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_pt_kernel(const PtArgs a)
     }
   }
   cluster_wait_acquire();
-  cluster_arrive_release();  // #1
+  cluster_arrive_relaxed();  // #1: nothing new to publish; the staged loads stay in flight
   cluster_wait_acquire();    //    the leader's decision is visible
   pt_worker_finish(a, r, w, i0, n, skip_pos, stage, v, src, dst, smem, L);
   cluster_wait_acquire();    // #2 completes: the leader may leave
@@ -1239,60 +1291,81 @@ __global__ void __launch_bounds__(128) writeback_kernel(const WritebackArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// Plan replay for a shared-index layer ([DD] §3.6, §5.6): a small fixed grid
-// walks the flattened (request, miss, 16-byte chunk) space.
+// Plan replay for a shared-index layer ([DD] §3.6, §5.6).  The plan's records
+// (every request's, back to back) are split evenly over a small grid; a CTA
+// resolves a batch of its records to source and destination rows once, into
+// shared memory, then streams the batch's 16-byte chunks with kReplayDepth
+// host loads in flight per thread.  Nothing on the load path waits on a global
+// read of the plan.
 // ---------------------------------------------------------------------------
 constexpr int kReplayThreads = 512;
+constexpr int kReplayBatch = 512;  // plan records resolved to rows per round
+constexpr int kReplayDepth = 8;    // 16-byte host loads in flight per thread
+
+__host__ __device__ inline int replay_pref_bytes(int R) { return ((R + 1) * 4 + 15) & ~15; }
 
 __global__ void __launch_bounds__(kReplayThreads) replay_kernel(const ReplayArgs a) {
-  extern __shared__ int32_t s_pref[];  // [R + 1] exclusive prefix of plan counts
+  extern __shared__ __align__(16) unsigned char rsm[];
+  int32_t *s_pref = reinterpret_cast<int32_t *>(rsm);  // [R + 1] exclusive prefix of plan counts
+  int64_t *s_src = reinterpret_cast<int64_t *>(rsm + replay_pref_bytes(a.R));  // [kReplayBatch]
+  int64_t *s_dst = s_src + kReplayBatch;
+  const int tid = threadIdx.x;
   const int nreq = a.num_reqs ? min(*a.num_reqs, a.R) : a.R;
-  if (threadIdx.x < 32) {
+  if (tid < 32) {
     int run = 0;
     for (int r0 = 0; r0 < nreq; r0 += 32) {
-      const int r = r0 + threadIdx.x;
+      const int r = r0 + tid;
       int v = r < nreq ? a.plan_count[r] : 0, inc = v;
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
         const int t = __shfl_up_sync(kFull, inc, d);
-        if ((int)threadIdx.x >= d) inc += t;
+        if (tid >= d) inc += t;
       }
       if (r < nreq) s_pref[r] = run + inc - v;
       run += __shfl_sync(kFull, inc, 31);
     }
-    if (threadIdx.x == 0) s_pref[nreq] = run;
+    if (tid == 0) s_pref[nreq] = run;
   }
   __syncthreads();
-  const int64_t total = static_cast<int64_t>(s_pref[nreq]) * a.rec16;
-  const int64_t T = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; base < total;
-       base += T * kUnroll) {
-    uint4 v[kUnroll];
-    char *d[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int64_t c = base + u * T;
-      d[u] = nullptr;
-      if (c < total) {
-        const uint32_t c32 = static_cast<uint32_t>(c);
-        const int m = static_cast<int>(c32 / static_cast<uint32_t>(a.rec16));
-        const int o = static_cast<int>(c32 - static_cast<uint32_t>(m) * a.rec16);
-        int lo = 0, hi = nreq - 1;  // last r with s_pref[r] <= m
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (s_pref[mid] <= m) lo = mid; else hi = mid - 1;
-        }
-        const int j = m - s_pref[lo];
-        const int64_t pk = static_cast<int64_t>(lo) * a.k + j;
-        v[u] = ld_nc_v4(a.src + static_cast<int64_t>(lo) * a.src_req_stride +
-                        static_cast<int64_t>(a.plan_pos[pk]) * a.src_row_stride + 16 * o);
-        d[u] = a.hot + static_cast<int64_t>(lo) * a.hot_req_stride +
-               static_cast<int64_t>(a.plan_slot[pk]) * a.hot_row_stride + 16 * o;
+  const int M = s_pref[nreq];
+  const int m0 = static_cast<int>(static_cast<int64_t>(M) * blockIdx.x / gridDim.x);
+  const int m1 = static_cast<int>(static_cast<int64_t>(M) * (blockIdx.x + 1) / gridDim.x);
+  const uint32_t rec16 = static_cast<uint32_t>(a.rec16);
+  for (int b0 = m0; b0 < m1; b0 += kReplayBatch) {
+    const int nb = min(kReplayBatch, m1 - b0);
+    for (int i = tid; i < nb; i += kReplayThreads) {
+      const int m = b0 + i;
+      int lo = 0, hi = nreq - 1;  // the request: last r with s_pref[r] <= m
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_pref[mid] <= m) lo = mid; else hi = mid - 1;
       }
+      const int64_t pk = static_cast<int64_t>(lo) * a.k + (m - s_pref[lo]);
+      s_src[i] = static_cast<int64_t>(lo) * a.src_req_stride +
+                 static_cast<int64_t>(a.plan_pos[pk]) * a.src_row_stride;
+      s_dst[i] = static_cast<int64_t>(lo) * a.hot_req_stride +
+                 static_cast<int64_t>(a.plan_slot[pk]) * a.hot_row_stride;
     }
+    __syncthreads();
+    const uint32_t n = static_cast<uint32_t>(nb) * rec16;
+    for (uint32_t q0 = tid; q0 < n; q0 += kReplayThreads * kReplayDepth) {
+      uint4 v[kReplayDepth];
+      char *d[kReplayDepth];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u)
-      if (d[u]) st_v4(d[u], v[u]);
+      for (int u = 0; u < kReplayDepth; ++u) {
+        const uint32_t q = q0 + u * kReplayThreads;
+        d[u] = nullptr;
+        if (q < n) {
+          const uint32_t i = q / rec16, o = q - i * rec16;
+          v[u] = ld_nc_v4(a.src + s_src[i] + 16 * o);
+          d[u] = a.hot + s_dst[i] + 16 * o;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kReplayDepth; ++u)
+        if (d[u]) st_v4(d[u], v[u]);
+    }
+    __syncthreads();
   }
 }
 
@@ -1849,7 +1922,7 @@ int hisparse_prefetch_plan(hisparse_handle *h, int32_t anchor_layer, int32_t fol
   a.plan_pos = m.plan_pos; a.plan_slot = m.plan_slot; a.plan_count = m.plan_count;
   a.src = Lf.host; a.src_req_stride = Lf.host_req_stride; a.src_row_stride = Lf.host_row_stride;
   a.hot = Lf.hot; a.hot_req_stride = Lf.hot_req_stride; a.hot_row_stride = Lf.hot_row_stride;
-  const size_t smem = sizeof(int32_t) * (h->R + 1);
+  const size_t smem = replay_pref_bytes(h->R) + 2 * sizeof(int64_t) * kReplayBatch;
   replay_kernel<<<h->replay_ctas, kReplayThreads, smem, static_cast<cudaStream_t>(stream)>>>(a);
   HS_CUDA(cudaGetLastError());
   return HISPARSE_OK;

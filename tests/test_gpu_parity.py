@@ -235,6 +235,43 @@ def test_device_detected_errors_keep_state(lookup, cs):
     hs.close(); mem.close()
 
 
+@pytest.mark.parametrize("cs", [1, 2])
+@pytest.mark.parametrize("m", [20, 100, 500])
+def test_duplicate_among_one_slices_misses(cs, m):
+    """A repeated position whose two copies are both misses of the same slice
+    fails the unit with its admission state untouched, whichever way the slice
+    orders its fetch list (one warp, direct ranks, row buckets); the same list
+    without the repeat then resolves exactly as the oracle does."""
+    R, k, B, P, rec = 1, 512, 1024, 8192, 16
+    mem, hs = _instance(R, k, B, P, rec=rec, ctas=cs)
+    out = torch.empty((R, k), dtype=torch.int32, device="cuda")
+    pos = np.random.default_rng(m).choice(P, size=m, replace=False).astype(np.int32)
+    bad = np.full((R, k), -1, np.int32)
+    bad[0, :m] = pos
+    bad[0, m - 1] = pos[0]
+    hs.resolve(0, _dev(bad), out)
+    flags, ue = hs.status()
+    assert flags == H.ERR_DUP and ue[0].tolist() == [H.ERR_DUP]
+    assert (out.cpu().numpy() == -1).all()
+    sp, lru, pt, mc = hs.export_state(0)
+    assert (sp == -1).all() and (pt == -1).all() and mc.tolist() == [0]
+    assert lru[0].tolist() == list(range(B))
+    good = bad.copy()
+    good[0, m - 1] = -1
+    hs.resolve(0, _dev(good), out)
+    ora = OracleLayer(R, k, B, P, rec, host=mem.host_view(0))
+    o_out, o_err = ora.resolve(good)
+    assert hs.status()[0] == 0 and not np.any(o_err)
+    np.testing.assert_array_equal(out.cpu().numpy(), o_out)
+    sp, lru, pt, mc = hs.export_state(0)
+    np.testing.assert_array_equal(sp, ora.slot_pos)
+    np.testing.assert_array_equal(lru, ora.lru)
+    np.testing.assert_array_equal(pt, ora.page_table)
+    np.testing.assert_array_equal(mc, ora.miss_count)
+    np.testing.assert_array_equal(mem.hot[0].cpu().numpy()[:, :B], ora.hot[:, :B])
+    hs.close(); mem.close()
+
+
 def test_import_rejects_inconsistent_state():
     mem, hs = _instance(1, 2, 4, 16)
     sp = np.array([[3, -1, 5, -1]], np.int32)

@@ -171,6 +171,12 @@ __device__ __forceinline__ uint32_t ld_dsmem_u32(uint32_t addr) {
   asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
   return v;
 }
+__device__ __forceinline__ void st_dsmem_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void fence_acq_rel_cluster() {
+  asm volatile("fence.acq_rel.cluster;" ::: "memory");
+}
 __device__ __forceinline__ uint4 ld_dsmem_v4(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -622,7 +628,7 @@ __host__ __device__ inline PtLayout pt_layout(int k, int B, int ks, int hcap, in
 }
 
 // worker misc words / leader misc words
-enum { kWErr = 0, kWNewest = 1, kWCount = 2 };
+enum { kWErr = 0, kWNewest = 1, kWCount = 2, kWLeadErr = 3 };
 enum { kLErr = 0, kLM = 1, kLHits = 2, kLPrefix = 8 };
 
 struct PtArgs {
@@ -947,27 +953,75 @@ __device__ void pt_leader_decide(const PtArgs &a, int cs, int nw, int32_t newest
   }
   __syncthreads();
   if (l_misc[kLErr]) return;  // uniform
-  // (3) hit count, then one pass that compacts hits (slot order) and
-  //     evictables (LRU order) together
-  {
-    int hits = 0;
-    for (int x = tid; x < nwords; x += kThreads) hits += __popc(l_hit[x]);
-    if (hits) atomicAdd(&l_misc[kLHits], static_cast<uint32_t>(hits));
-  }
-  __syncthreads();
+  // (3) one block-wide pass compacts the hits (slot order) and the evictables
+  //     (LRU order) together.  Thread t owns slots and LRU positions
+  //     [t*per, t*per + per); one exclusive scan of the packed per-thread
+  //     counts (hits << 16 | evictables; both < 2^15) gives every thread its
+  //     output ranks and every warp the hit total H.
   const int M = static_cast<int>(l_misc[kLM]);
-  const int H = static_cast<int>(l_misc[kLHits]);
+  const int per = (B + kThreads - 1) / kThreads;  // <= 32 since B <= 32767
+  const int j0 = min(B, tid * per), j1 = min(B, j0 + per);
+  uint32_t ma = 0, mb = 0;  // bit i: slot j0+i is hit / LRU entry j0+i is evictable
+  for (int j = j0; j < j1; ++j) {
+    ma |= static_cast<uint32_t>(bit_of(l_hit, j)) << (j - j0);
+    mb |= static_cast<uint32_t>(!bit_of(l_hit, l_lru[j])) << (j - j0);
+  }
+  const uint32_t v = (static_cast<uint32_t>(__popc(ma)) << 16) | static_cast<uint32_t>(__popc(mb));
+  uint32_t inc = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t t = __shfl_up_sync(kFull, inc, d);
+    if (lane >= d) inc += t;
+  }
+  if (lane == 31) s_cnt[tid >> 5] = static_cast<int32_t>(inc);
+  __syncthreads();
+  const uint32_t wt = static_cast<uint32_t>(s_cnt[lane]);
+  uint32_t winc = wt;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t t = __shfl_up_sync(kFull, winc, d);
+    if (lane >= d) winc += t;
+  }
+  const uint32_t total = __shfl_sync(kFull, winc, 31);
+  const uint32_t base = __shfl_sync(kFull, winc - wt, tid >> 5) + inc - v;
+  const int H = static_cast<int>(total >> 16);
   const int E = B - H;
-  block_compact2(
-      B, [&](int s) { return bit_of(l_hit, s); },
-      [&](int s, int h) { l_newlru[E + h] = static_cast<int16_t>(s); },
-      [&](int j) { return !bit_of(l_hit, l_lru[j]); },
-      [&](int j, int e) {
-        const int16_t sl = l_lru[j];
-        if (e < M) l_ev[e] = sl;
-        l_newlru[e >= M ? e - M : E - M + e] = sl;
-      },
-      s_cnt);
+  int ha = static_cast<int>(base >> 16), eb = static_cast<int>(base & 0xFFFFu);
+  for (int j = j0; j < j1; ++j) {
+    const int i = j - j0;
+    if ((ma >> i) & 1u) l_newlru[E + ha++] = static_cast<int16_t>(j);
+    if ((mb >> i) & 1u) {
+      const int16_t sl = l_lru[j];
+      if (eb < M) l_ev[eb] = sl;
+      l_newlru[eb >= M ? eb - M : E - M + eb] = sl;
+      ++eb;
+    }
+  }
+  if (tid == 0) l_misc[kLHits] = static_cast<uint32_t>(H);
+  __syncthreads();
+}
+
+// Leader: hand every slice the verdict and its victims, written straight
+// into the workers' shared memory, so that after the next cluster barrier a
+// worker reads them locally.
+__device__ void pt_leader_push(int cs, int nw, unsigned char *smem, const PtLayout &L) {
+  const int tid = threadIdx.x;
+  const uint32_t *l_misc = reinterpret_cast<const uint32_t *>(smem + L.l_misc);
+  const int32_t *l_ev = reinterpret_cast<const int32_t *>(smem + L.l_ev);
+  const uint32_t *w_misc0 = reinterpret_cast<const uint32_t *>(smem + L.w_misc);
+  const int32_t *w_vict0 = reinterpret_cast<const int32_t *>(smem + L.w_vict);
+  auto wrank = [&](int w) { return static_cast<uint32_t>(cs == 1 ? 0 : w + 1); };
+  const uint32_t err = l_misc[kLErr];
+  for (int w = tid; w < nw; w += kThreads)
+    st_dsmem_u32(dsmem_addr(&w_misc0[kWLeadErr], wrank(w)), err);
+  if (err) return;
+  const int M = static_cast<int>(l_misc[kLM]);
+  for (int g = tid; g < M; g += kThreads) {
+    int w = 0;
+    while (w + 1 < nw && static_cast<int>(l_misc[kLPrefix + w + 1]) <= g) ++w;
+    const int j = g - static_cast<int>(l_misc[kLPrefix + w]);
+    st_dsmem_u32(dsmem_addr(&w_vict0[j], wrank(w)), static_cast<uint32_t>(l_ev[g]));
+  }
 }
 
 // Leader: publish page table, slot map, LRU order, counts, plan.
@@ -1036,18 +1090,14 @@ __device__ void pt_leader_publish(const PtArgs &a, int r, int32_t prev, int32_t 
   }
 }
 
-// Worker, after the leader's decision: fetch victims' indices, write the
-// slice's slot vector, store the staged records (and read + store the rest).
-// With a cluster this also arrives at barrier #2 once the leader's memory is
-// no longer needed.
-__device__ void pt_worker_finish(const PtArgs &a, int r, int w, int i0, int n, int32_t skip_pos,
+// Worker, after the leader's decision (its verdict and this slice's victims
+// are already in this CTA's shared memory): store the staged records (and read
+// + store the rest), write the slice's slot vector.
+__device__ void pt_worker_finish(const PtArgs &a, int r, int i0, int n, int32_t skip_pos,
                                  bool staged, const uint4 *v, const char *src, char *dst,
                                  unsigned char *smem, const PtLayout &L) {
   const int tid = threadIdx.x;
-  const bool cluster = v != nullptr;
-  const uint32_t *l_misc = reinterpret_cast<const uint32_t *>(smem + L.l_misc);
-  const int32_t *l_ev = reinterpret_cast<const int32_t *>(smem + L.l_ev);
-  int32_t *w_vict = reinterpret_cast<int32_t *>(smem + L.w_vict);
+  const int32_t *w_vict = reinterpret_cast<const int32_t *>(smem + L.w_vict);
   const int32_t *w_out = reinterpret_cast<const int32_t *>(smem + L.w_out);
   const int32_t *w_mi = reinterpret_cast<const int32_t *>(smem + L.w_mi);
   const int32_t *w_mp = reinterpret_cast<const int32_t *>(smem + L.w_mp);
@@ -1055,15 +1105,7 @@ __device__ void pt_worker_finish(const PtArgs &a, int r, int w, int i0, int n, i
   const uint32_t *w_misc = reinterpret_cast<const uint32_t *>(smem + L.w_misc);
   const int mw = static_cast<int>(w_misc[kWCount]);
   const int64_t totc = static_cast<int64_t>(mw) * a.rec16;
-  const uint32_t err = ld_dsmem_u32(dsmem_addr(&l_misc[kLErr], 0));
-  if (!err) {
-    const int pre = static_cast<int>(ld_dsmem_u32(dsmem_addr(&l_misc[kLPrefix + w], 0)));
-    const uint32_t ev0 = dsmem_addr(l_ev, 0);
-    for (int j = tid; j < mw; j += kThreads)
-      w_vict[j] = static_cast<int32_t>(ld_dsmem_u32(ev0 + 4u * static_cast<uint32_t>(pre + j)));
-  }
-  __syncthreads();
-  if (cluster) cluster_arrive_relaxed();  // #2: done with the leader's memory
+  const uint32_t err = w_misc[kWLeadErr];
   if (!err && a.io) {
     int64_t start = 0;
     if (staged) {
@@ -1214,9 +1256,10 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_pt_kernel(const PtArgs a)
     pt_worker_classify(a, r, i0, n, newest, first, smem, L);
     pt_leader_decide(a, cs, nw, newest, smem, L);
     __syncthreads();
+    pt_leader_push(cs, nw, smem, L);
     pt_leader_publish<kRecordPlan>(a, r, prev, skip_pos, smem, L);
     __syncthreads();
-    pt_worker_finish(a, r, w, i0, n, skip_pos, false, nullptr, src, dst, smem, L);
+    pt_worker_finish(a, r, i0, n, skip_pos, false, nullptr, src, dst, smem, L);
     return;
   }
   if (leader) {
@@ -1229,16 +1272,22 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_pt_kernel(const PtArgs a)
     __syncthreads();
     cluster_wait_acquire();    //    the slices are ready
     pt_leader_decide(a, cs, nw, newest, smem, L);
-    cluster_arrive_release();  // #1: the decision, for the workers
+    __syncthreads();
+    pt_leader_push(cs, nw, smem, L);
+    __syncthreads();
+    cluster_arrive_release();  // #1: the verdict and victims, in the workers' memory
     pt_leader_publish<kRecordPlan>(a, r, prev, skip_pos, smem, L);
-    cluster_wait_acquire();
-    cluster_arrive_relaxed();  // #2
-    cluster_wait_acquire();    //    the workers are done with this CTA's memory
+    cluster_wait_acquire();    //    (no CTA touches another's memory after #1)
     return;
   }
   // worker
   pt_worker_classify(a, r, i0, n, newest, first, smem, L);
-  cluster_arrive_release();  // #0: the slice, for the leader
+  // #0: the slice, for the leader.  The block barrier that ends the
+  // classification orders every thread's shared-memory writes before the last
+  // warp's cluster-scope fence, which releases them all; the other warps
+  // arrive without a fence, so their host loads below do not wait on one.
+  if (tid >= kThreads - 32) fence_acq_rel_cluster();
+  cluster_arrive_relaxed();
   // Read this slice's missed records into registers now, before any victim is
   // known: the reads fly while the leader decides.
   const int32_t *w_mp = reinterpret_cast<const int32_t *>(smem + L.w_mp);
@@ -1261,8 +1310,7 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_pt_kernel(const PtArgs a)
   cluster_wait_acquire();
   cluster_arrive_relaxed();  // #1: nothing new to publish; the staged loads stay in flight
   cluster_wait_acquire();    //    the leader's decision is visible
-  pt_worker_finish(a, r, w, i0, n, skip_pos, stage, v, src, dst, smem, L);
-  cluster_wait_acquire();    // #2 completes: the leader may leave
+  pt_worker_finish(a, r, i0, n, skip_pos, stage, v, src, dst, smem, L);
 }
 
 // ---------------------------------------------------------------------------

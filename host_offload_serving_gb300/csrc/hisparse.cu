@@ -1210,6 +1210,11 @@ __device__ void pt_leader_write_through(const PtArgs &a, int r, int32_t prev, un
 template <bool kRecordPlan>
 __global__ void __launch_bounds__(kThreads, 1) resolve_pt_kernel(const PtArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
+  // Programmatic dependent launch: this grid may be set up while the previous
+  // kernel of the stream finishes, but reads nothing before that kernel has
+  // completed; the next kernel may be set up as soon as this one runs.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int cs = static_cast<int>(cluster_nctarank());
   const int rank = static_cast<int>(cluster_ctarank());
   const int r = static_cast<int>(blockIdx.x) / cs;
@@ -1593,7 +1598,7 @@ const char *hisparse_strerror(int code) {
 }
 
 int hisparse_host_alloc(size_t bytes, void **out) {
-  return hisparse_host_alloc_kind(bytes, HISPARSE_HOST_HUGE, out);
+  return hisparse_host_alloc_kind(bytes, HISPARSE_HOST_PINNED, out);
 }
 
 int hisparse_host_alloc_kind(size_t bytes, int32_t kind, void **out) {
@@ -1883,11 +1888,13 @@ int hisparse_resolve_step(hisparse_handle *h, int32_t layer, const int32_t *d_se
   lc.blockDim = dim3(kThreads);
   lc.dynamicSmemBytes = h->smem;
   lc.stream = static_cast<cudaStream_t>(stream);
-  cudaLaunchAttribute at[1];
+  cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeClusterDimension;
   at[0].val.clusterDim.x = h->cs;
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = at;
   lc.numAttrs = 1;
   cudaError_t e;
@@ -1934,6 +1941,7 @@ int hisparse_resolve_step(hisparse_handle *h, int32_t layer, const int32_t *d_se
     a.src = (flags & HISPARSE_FROM_MIRROR) ? Ld.mirror : Ld.host;
     a.src_req_stride = Ld.host_req_stride; a.src_row_stride = Ld.host_row_stride;
     a.hot = Ld.hot; a.hot_req_stride = Ld.hot_req_stride; a.hot_row_stride = Ld.hot_row_stride;
+    lc.numAttrs = 2;  // cluster shape + programmatic dependent launch
     e = plan ? cudaLaunchKernelEx(&lc, resolve_pt_kernel<true>, a)
              : cudaLaunchKernelEx(&lc, resolve_pt_kernel<false>, a);
   }

@@ -29,7 +29,7 @@ from . import hisparse as H
 class HostPool:
     """Pinned + mapped host memory of exactly ``nbytes`` (freed by ``close``)."""
 
-    def __init__(self, nbytes, kind=H.HOST_HUGE):
+    def __init__(self, nbytes, kind=H.HOST_PINNED):
         rc, ptr = H.hisparse_host_alloc_kind(int(nbytes), kind)
         H.check(rc, f"hisparse_host_alloc_kind({nbytes}, {kind})")
         self.ptr = ptr
@@ -160,7 +160,7 @@ class WorkloadMemory:
     Hot buffer of layer l: ``hot[l]`` (uint8 [R][B+1][rec], device).
     """
 
-    def __init__(self, R, L, B, P, rec, device="cuda", mirror=False, pool_kind=H.HOST_HUGE):
+    def __init__(self, R, L, B, P, rec, device="cuda", mirror=False, pool_kind=H.HOST_PINNED):
         self.R, self.L, self.B, self.P, self.rec = R, L, B, P, rec
         self.req_stride = P * rec
         self.layer_stride = R * P * rec

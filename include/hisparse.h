@@ -250,30 +250,29 @@ int hisparse_reset(hisparse_handle *h, int32_t layer, void *stream);
 /* Fill `out` with facts about the instance. */
 int hisparse_get_info(const hisparse_handle *h, hisparse_info *out);
 
-/* Pinned, device-mapped, portable host memory for host pools.  A request of
- * at least one transparent huge page is served by huge-page-advised memory
- * registered with cudaHostRegister (zero-filled, size rounded up to whole huge
- * pages internally): the GPU then translates the pool with large pages, and
- * random record fetches stall far less on address translation than they do
- * on cudaHostAlloc memory.  Such a pool is excluded from fork() children
- * (MADV_DONTFORK): a fork would otherwise split its pinned huge pages in the
- * parent.  Smaller requests, or a refused registration, fall back to
- * cudaHostAlloc (contents unspecified).  Free with hisparse_host_free.
+/* Pinned, device-mapped, portable host memory for host pools: the PINNED kind
+ * below (cudaHostAlloc; contents unspecified).  Free with hisparse_host_free.
  * Errors: EINVAL, ENOMEM. */
 int hisparse_host_alloc(size_t bytes, void **out);
 int hisparse_host_free(void *p);
 
 /* Host-pool kinds for hisparse_host_alloc_kind. */
-#define HISPARSE_HOST_HUGE 0   /* huge-page-backed, registered (hisparse_host_alloc) */
-#define HISPARSE_HOST_PINNED 1 /* cudaHostAlloc: driver-pinned base pages */
+#define HISPARSE_HOST_HUGE 0   /* transparent-huge-page backed, cudaHostRegister'ed */
+#define HISPARSE_HOST_PINNED 1 /* cudaHostAlloc: driver-pinned base pages (the default) */
 
-/* hisparse_host_alloc with an explicit kind.  HUGE maps the pool with few,
- * large translations, which is fastest for random record fetches; on a host
- * whose GPU driver migrates GPU-hot host pages (ATS access-counter migration)
- * such a pool can have huge pages split under it while it is in use, and the
- * GPU then stalls in fault service.  PINNED memory is never migrated or split
- * but costs a translation miss per first-touched 64 KB page.  The operator-side
- * remedy for HUGE is to disable the driver's access-counter migration.
+/* hisparse_host_alloc with an explicit kind.
+ * PINNED: driver-allocated pinned memory.  It is never split or migrated; the
+ *   GPU pays one translation miss per first-touched 64 KB page, after which
+ *   random record fetches run at the host-link rate.
+ * HUGE: huge-page-advised memory (zero-filled, size rounded up to whole huge
+ *   pages) registered with cudaHostRegister, excluded from fork() children
+ *   (MADV_DONTFORK).  The GPU translates it with few, large pages.  On a host
+ *   whose GPU driver migrates GPU-hot host pages (ATS access-counter
+ *   migration), huge pages can be split under the pool while it is in use and
+ *   GPU fetches then stall in fault service for up to milliseconds; the
+ *   operator-side remedy is to disable that migration in the driver.  A
+ *   request smaller than one huge page, or a refused registration, falls back
+ *   to PINNED.
  * Errors: EINVAL, ENOMEM. */
 int hisparse_host_alloc_kind(size_t bytes, int32_t kind, void **out);
 

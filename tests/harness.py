@@ -16,7 +16,7 @@ from workload.traces import all_traces
 
 class Run:
     def __init__(self, w, flags=0, mirror=False, ctas_per_request=0, replay_ctas=0,
-                 num_reqs=None, oracle_bytes=True, traces=None, lookup=0, pool_kind=0,
+                 num_reqs=None, oracle_bytes=True, traces=None, lookup=0, pool_kind=H.HOST_PINNED,
                  fused=True):
         self.w = w
         self.flags = flags

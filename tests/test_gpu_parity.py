@@ -194,9 +194,9 @@ def test_from_mirror_bytes_identical():
              mirror=True)
 
 
-def test_cudahostalloc_pool():
-    """The same results from a driver-pinned (cudaHostAlloc) host pool."""
-    _run_all(get("dsa").scaled(R=3, groups=2, L_ctx=65536, steps=6), pool_kind=H.HOST_PINNED)
+def test_huge_page_pool():
+    """The same results from a huge-page-backed, registered host pool."""
+    _run_all(get("dsa").scaled(R=3, groups=2, L_ctx=65536, steps=6), pool_kind=H.HOST_HUGE)
 
 
 def test_num_reqs_padding_leaves_tail_untouched():

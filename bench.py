@@ -49,6 +49,11 @@ def parse():
                     help="skip the untimed passes over the trace before warm-up")
     ap.add_argument("--burn-in", type=int, default=3,
                     help="untimed passes over the trace before warm-up (default 3)")
+    ap.add_argument("--mirror", action="store_true",
+                    help="fetch missed records from an HBM mirror of the host pool "
+                         "(FROM_MIRROR): the same kernels with HBM as the source; the "
+                         "roofline is then against HBM (rows written back later are not "
+                         "mirrored)")
     ap.add_argument("--unfused", action="store_true",
                     help="write-through as its own launch instead of inside RESOLVE")
     ap.add_argument("--L-ctx", type=int, default=0,
@@ -208,6 +213,59 @@ def cpu_oracle_rate(w, traces, host_views=None, budget_s=10.0):
             "steps": steps_done}
 
 
+def cpu_oracle_rate_threads(w, traces, host_views, threads):
+    """The same C oracle over all decode steps, with the workload's independent
+    units -- one request of one anchor layer, with its shared-index layers --
+    spread over `threads` Python threads (each oracle call releases the GIL)."""
+    import numpy as np
+    from concurrent.futures import ThreadPoolExecutor
+    from oracle.coracle import OracleLayer
+    from workload import records as REC
+
+    anchors = w.anchors()
+    anchor_of = w.anchor_of()
+    new_rows = REC.new_token_records(w)
+    units = []
+    for a in anchors:
+        fls = [l for l in range(w.L) if anchor_of[l] == a]
+        for r in range(w.R):
+            mk = lambda l, meta: OracleLayer(1, w.k, w.B, w.P, w.rec,
+                                             host=host_views[l][r:r + 1], host_split=w.L_ctx,
+                                             metadata=meta)
+            units.append((a, r, mk(a, True), [(f, mk(f, False)) for f in fls]))
+    for _, _, o, _ in units:
+        o.reset()
+
+    def run(chunk):
+        sel = misses = 0
+        for a, r, o, fls in chunk:
+            for t in range(w.steps):
+                if w.write_through:
+                    for l, lay in [(a, o)] + fls:
+                        if t > 0:
+                            lay.writeback(traces[anchors[0]][1][t - 1][r:r + 1])
+                        lay.set_newest_rows(new_rows[t, l, r:r + 1])
+                nw = traces[a][1][t][r:r + 1] if w.write_through else None
+                o.resolve(traces[a][0][t][r:r + 1], nw)
+                misses += int(o.miss_count.sum())
+                for _, lay in fls:
+                    o.replay_into(lay)
+                sel += w.k
+        return sel, misses
+
+    chunks = [units[i::threads] for i in range(threads)]
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        res = list(ex.map(run, chunks))
+    dt = time.perf_counter() - t0
+    sel = sum(x for x, _ in res)
+    return {"value": sel / dt, "unit": "selections/s", "cores": threads, "kind": "oracle",
+            "sample": f"all {w.steps} decode steps of the {w.name} workload, its "
+                      f"{len(units)} independent (request, anchor layer) units spread over "
+                      f"{threads} threads, plain C oracle, record copies included",
+            "miss_bytes_per_s": sum(m for _, m in res) * w.rec / dt, "seconds": dt}
+
+
 # --------------------------------------------------------------------------- #
 def run_reference(args):
     rank, world, local = dist_env()
@@ -265,9 +323,11 @@ def run_ours(args):
     dev = torch.device("cuda", local)
 
     t_setup = time.perf_counter()
-    mem = WorkloadMemory(w.R, w.L, w.B, w.P, w.rec,
+    mem = WorkloadMemory(w.R, w.L, w.B, w.P, w.rec, mirror=args.mirror,
                          pool_kind=H.HOST_HUGE if args.pool == "huge" else H.HOST_PINNED)
     REC.fill_host_pool(w, mem.pool.ptr, mem.layer_stride, mem.req_stride)
+    if args.mirror:
+        mem.fill_mirror()
     hs = HiSparse(w.R, w.L, w.k, w.B, w.P, w.rec, mem.layer_buffers(), anchor_of=w.anchor_of(),
                   ctas_per_request=args.ctas, replay_ctas=args.replay_ctas, lookup=args.lookup)
     info = hs.info()
@@ -302,7 +362,8 @@ def run_ours(args):
         wb = torch.from_numpy(wbn).to(dev)
         new_rows = torch.from_numpy(REC.new_token_records(w)).to(dev)
     out = torch.full((G, w.R, w.k), -1, dtype=torch.int32, device=dev)
-    runner = DecodeStep(hs, mem, groups, fused=not args.unfused)
+    runner = DecodeStep(hs, mem, groups, flags=H.FROM_MIRROR if args.mirror else 0,
+                        fused=not args.unfused)
     miss_hist = torch.zeros((T, G, w.R), dtype=torch.int32, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)     # > 129 MB L2
     setup_s = time.perf_counter() - t_setup
@@ -449,14 +510,14 @@ def run_ours(args):
     hs.reset()
     mem.hot.zero_()
     torch.cuda.synchronize()
-    res_ms = wb_ms = rp_ms = None
+    res_ms = wb_ms = rp_ms = cold_ms = None
     if instr is not None:
         for t in range(T):
-            if t >= args.warmup:
-                flush.fill_(t & 0xFF)
+            flush.fill_(t & 0xFF)
             instr[t][0].replay()
             torch.cuda.synchronize()
         res_ms = [[a.elapsed_time(b) for a, b in instr[args.warmup + i][1]] for i in range(args.steps)]
+        cold_ms = [a.elapsed_time(b) for a, b in instr[0][1]]
         wb_ms = [a.elapsed_time(b) for i in range(args.steps) for a, b in instr[args.warmup + i][2]]
         rp_ms = [a.elapsed_time(b) for i in range(args.steps) for a, b in instr[args.warmup + i][3]]
     else:   # no in-graph timing events in this torch: count misses eagerly
@@ -620,20 +681,35 @@ def run_ours(args):
     kernel_src = os.path.join(ROOT, "host_offload_serving_gb300", "csrc", "hisparse.cu")
     kname = "resolve_pt_kernel" if args.lookup == 0 else "resolve_kernel"
     prof = profile_traffic(kernel_src, kname)
-    roof = {"bound": "host_link", "achieved": round(fetch_gbs, 2), "peak": round(h2d_gbs, 2),
-            "unit": "GB/s", "frac": round(fetch_gbs / h2d_gbs, 4),
+    if args.mirror:   # records move HBM -> HBM: read and write once each
+        bound, ach, peak = "hbm", 2 * fetch_gbs, peaks["hbm_gbs"]
+    else:
+        bound, ach, peak = "host_link", fetch_gbs, h2d_gbs
+    roof = {"bound": bound, "achieved": round(ach, 2), "peak": round(peak, 2),
+            "unit": "GB/s", "frac": round(ach / peak, 4),
             "traffic": prof["dram_bytes_per_launch"] if prof else None,
             "traffic_sysmem": prof["sysmem_bytes_per_launch"] if prof else None,
             "traffic_source": prof["source"] if prof else None,
             "traffic_launch_algorithmic_bytes": prof["algorithmic_bytes"] if prof else None,
             "kernel": kname,
-            "peak_source": "pinned cudaMemcpyAsync H2D, 1 GiB x 20, best of 3 rounds, same run",
+            "peak_source": (f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if args.mirror else
+                            "pinned cudaMemcpyAsync H2D, 1 GiB x 20, best of 3 rounds, same run"),
             "algorithmic_bytes_per_launch": miss_bytes / (args.steps * G),
             "avg_launch_us": round(launch_ms * 1e3, 2),
             "avg_launch_us_event_window": round(resolve_avg_ms * 1e3, 2), "timing": timing_note,
             "launch_us_p50_p90_p99_max": [round(pct(0.5), 2), round(pct(0.9), 2),
                                           round(pct(0.99), 2), round(srt[-1] * 1e3, 2)],
             "writeback_us_avg": round(1e3 * sum(wb_ms) / len(wb_ms), 2) if wb_ms else None}
+    # step 0 from the admission state: every selection but the newest misses,
+    # so each launch moves R x k records -- the fetch path at full size
+    cold = None
+    if cold_ms:
+        cb = int(miss_hist[0].sum().item()) * w.rec
+        c_s = sum(cold_ms) / 1e3
+        cold = {"us_per_launch": round(1e3 * sum(cold_ms) / len(cold_ms), 2),
+                "bytes_per_launch": cb // G, "fetch_gbs": round(cb / c_s / 1e9, 2),
+                "frac_of_link": round(cb / c_s / 1e9 / h2d_gbs, 4),
+                "timing": "step 0 of pass 2 (admission state), events around each RESOLVE"}
     replay = None
     if rp_ms:
         nf = sum(len(f) for _, f in groups)
@@ -648,12 +724,14 @@ def run_ours(args):
         allhit["hbm_frac"] = round(allhit["hbm_gbs"] / peaks.get("hbm_gbs"), 5)
         allhit["hbm_peak_source"] = f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
 
-    cpu = None
+    cpu = cpu_mt = None
     if rank == 0 and not args.no_cpu:
         views = {l: mem.host_view(l) for l in range(w.L)}
         cpu = cpu_oracle_rate(w, traces, host_views=views, budget_s=20.0)
         cpu.pop("seconds", None)
         cpu.pop("steps", None)
+        cpu_mt = cpu_oracle_rate_threads(w, traces, views, os.cpu_count() or 1)
+        cpu_mt.pop("seconds", None)
 
     hp_frac_end = mem.pool.hugepage_fraction()
     s1 = thp_splits()
@@ -674,6 +752,7 @@ def run_ours(args):
                        "lookup": ["page_table", "hash"][info["lookup"]],
                        "write_through_launch": "separate" if args.unfused else "fused into RESOLVE",
                        "host_pool": args.pool,
+                       "fetch_source": "HBM mirror of the host pool" if args.mirror else "host pool",
                        "host_pool_hugepage_fraction": round(hp_frac, 3),
                        "host_pool_hugepage_fraction_end": round(hp_frac_end, 3),
                        "host_thp_splits_during_burn_in": splits_burn,
@@ -685,9 +764,11 @@ def run_ours(args):
             "miss_rate": round(miss_rate, 4),
             "us_per_layer_step": round(launch_ms * 1e3, 2),
             "all_hit_no_io": allhit,
+            "cold_step0": cold,
             "replay": replay,
             "e2e": e2e,
             "cpu_baseline": cpu,
+            "cpu_baseline_threads": cpu_mt,
             "gpu_launches": launches,
             "clocks": clocks.summary(),
             "status_flags": flags,

@@ -744,9 +744,9 @@ __device__ __forceinline__ bool bit_of(const uint32_t *bits, int s) {
 }
 
 // Worker: classify selections [i0, i0 + n) of request r.
-__device__ void pt_worker_classify(const PtArgs &a, int r, int i0, int n, int32_t newest,
-                                   const int32_t (&first)[kGroup], unsigned char *smem,
-                                   const PtLayout &L) {
+__device__ int pt_worker_classify(const PtArgs &a, int r, int i0, int n, int32_t newest,
+                                  const int32_t (&first)[kGroup], unsigned char *smem,
+                                  const PtLayout &L) {
   const int tid = threadIdx.x;
   const int B = a.B;
   const int64_t P = a.P;
@@ -813,32 +813,43 @@ __device__ void pt_worker_classify(const PtArgs &a, int r, int i0, int n, int32_
       },
       s_cnt);
   if (tid == 0) w_misc[kWCount] = static_cast<uint32_t>(mw);
-  // Fetch order: the slice's misses by ascending host row.  Which slot each
-  // lands in does not depend on it; reading in address order lets nearby
-  // records share the GPU's page-table walks, which matters whenever the pool
-  // is not mapped with large pages.
+  __syncthreads();
+  return mw;
+}
+
+// Worker: order the slice's misses j0 .. mw-1 by ascending host row into
+// w_ord[0 .. mw-j0).  Which slot each lands in does not depend on it; reading
+// in address order lets nearby records share the GPU's address-translation
+// walks, which matters whenever the GPU cannot keep the pool's translations
+// cached.  Ties (equal rows) only occur in a failing unit; they are broken by
+// list index, so w_ord always holds each index once.
+__device__ void pt_worker_order(const PtArgs &a, int j0, int mw, unsigned char *smem,
+                                const PtLayout &L) {
+  const int tid = threadIdx.x;
+  const int32_t *w_mp = reinterpret_cast<const int32_t *>(smem + L.w_mp);
   int32_t *w_ord = reinterpret_cast<int32_t *>(smem + L.w_ord);
-  // Ties (equal rows) only occur in a failing unit; they are broken by list
-  // index so that w_ord is always a permutation of [0, mw).
-  if (mw <= 32) {
+  int32_t *s_cnt = reinterpret_cast<int32_t *>(smem + L.cnt);
+  const int n = mw - j0;
+  if (n <= 0) return;
+  if (n <= 32) {
     if (tid < 32) {  // one warp: each lane ranks its miss against the others
-      const int32_t key = tid < mw ? w_mp[tid] : 0;
+      const int32_t key = tid < n ? w_mp[j0 + tid] : 0;
       int rnk = 0;
-      for (int i = 0; i < mw; ++i) {
+      for (int i = 0; i < n; ++i) {
         const int32_t ki = __shfl_sync(kFull, key, i);
         rnk += ki < key || (ki == key && i < tid);
       }
-      if (tid < mw) w_ord[rnk] = tid;
+      if (tid < n) w_ord[rnk] = j0 + tid;
     }
-  } else if (mw <= kRankSortMax) {
-    for (int j = tid; j < mw; j += kThreads) {  // rank against every miss (broadcast reads)
-      const int32_t key = w_mp[j];
+  } else if (n <= kRankSortMax) {
+    for (int i = tid; i < n; i += kThreads) {  // rank against every miss (broadcast reads)
+      const int32_t key = w_mp[j0 + i];
       int rnk = 0;
-      for (int i = 0; i < mw; ++i) {
-        const int32_t ki = w_mp[i];
-        rnk += ki < key || (ki == key && i < j);
+      for (int x = 0; x < n; ++x) {
+        const int32_t kx = w_mp[j0 + x];
+        rnk += kx < key || (kx == key && x < i);
       }
-      w_ord[rnk] = j;
+      w_ord[rnk] = j0 + i;
     }
   } else {  // counting sort into row buckets, then a rank inside each bucket
     int32_t *w_bkt = reinterpret_cast<int32_t *>(smem + L.w_bkt);
@@ -846,13 +857,13 @@ __device__ void pt_worker_classify(const PtArgs &a, int r, int i0, int n, int32_
     const int sh = a.bucket_shift, nb = a.nbuckets;
     for (int b = tid; b < nb; b += kThreads) w_bkt[b] = 0;
     __syncthreads();
-    for (int j = tid; j < mw; j += kThreads) atomicAdd(&w_bkt[w_mp[j] >> sh], 1);
+    for (int j = j0 + tid; j < mw; j += kThreads) atomicAdd(&w_bkt[w_mp[j] >> sh], 1);
     __syncthreads();
     block_exclusive_scan(w_bkt, nb, s_cnt);
-    for (int j = tid; j < mw; j += kThreads) w_bidx[atomicAdd(&w_bkt[w_mp[j] >> sh], 1)] = j;
+    for (int j = j0 + tid; j < mw; j += kThreads) w_bidx[atomicAdd(&w_bkt[w_mp[j] >> sh], 1)] = j;
     __syncthreads();
     // now w_bkt[b] ends bucket b; rank each entry inside its bucket
-    for (int q = tid; q < mw; q += kThreads) {
+    for (int q = tid; q < n; q += kThreads) {
       const int j = w_bidx[q];
       const int32_t p = w_mp[j];
       const int b = p >> sh;
@@ -1091,10 +1102,11 @@ __device__ void pt_leader_publish(const PtArgs &a, int r, int32_t prev, int32_t 
 }
 
 // Worker, after the leader's decision (its verdict and this slice's victims
-// are already in this CTA's shared memory): store the staged records (and read
-// + store the rest), write the slice's slot vector.
+// are already in this CTA's shared memory): store the `staged` records held in
+// registers (the slice's first misses, in list order), read and store the rest
+// in host-row order (w_ord), and write the slice's slot vector.
 __device__ void pt_worker_finish(const PtArgs &a, int r, int i0, int n, int32_t skip_pos,
-                                 bool staged, const uint4 *v, const char *src, char *dst,
+                                 int staged, const uint4 *v, const char *src, char *dst,
                                  unsigned char *smem, const PtLayout &L) {
   const int tid = threadIdx.x;
   const int32_t *w_vict = reinterpret_cast<const int32_t *>(smem + L.w_vict);
@@ -1104,33 +1116,30 @@ __device__ void pt_worker_finish(const PtArgs &a, int r, int i0, int n, int32_t 
   const int32_t *w_ord = reinterpret_cast<const int32_t *>(smem + L.w_ord);
   const uint32_t *w_misc = reinterpret_cast<const uint32_t *>(smem + L.w_misc);
   const int mw = static_cast<int>(w_misc[kWCount]);
-  const int64_t totc = static_cast<int64_t>(mw) * a.rec16;
   const uint32_t err = w_misc[kWLeadErr];
   if (!err && a.io) {
-    int64_t start = 0;
-    if (staged) {
+    const int64_t totc = static_cast<int64_t>(staged) * a.rec16;
 #pragma unroll
-      for (int u = 0; u < kStage; ++u) {
-        const int64_t q = tid + static_cast<int64_t>(u) * kThreads;
-        if (q < totc) {
-          const uint32_t q32 = static_cast<uint32_t>(q);
-          const int f = static_cast<int>(q32 / static_cast<uint32_t>(a.rec16));
-          const int o = static_cast<int>(q32 - static_cast<uint32_t>(f) * a.rec16);
-          if (w_mp[w_ord[f]] != skip_pos)
-            st_v4(dst + static_cast<int64_t>(w_vict[w_ord[f]]) * a.hot_row_stride + 16 * o, v[u]);
-        }
+    for (int u = 0; u < kStage; ++u) {
+      const int64_t q = tid + static_cast<int64_t>(u) * kThreads;
+      if (v && q < totc) {
+        const uint32_t q32 = static_cast<uint32_t>(q);
+        const int f = static_cast<int>(q32 / static_cast<uint32_t>(a.rec16));
+        const int o = static_cast<int>(q32 - static_cast<uint32_t>(f) * a.rec16);
+        if (w_mp[f] != skip_pos)
+          st_v4(dst + static_cast<int64_t>(w_vict[f]) * a.hot_row_stride + 16 * o, v[u]);
       }
-      start = static_cast<int64_t>(kStage) * kThreads;
     }
-    // whatever was not staged, in host-row order
-    for (int64_t b0 = start + tid; b0 < totc; b0 += static_cast<int64_t>(kThreads) * kUnroll) {
+    // the rest of the slice's misses, in host-row order
+    const int64_t totr = static_cast<int64_t>(mw - staged) * a.rec16;
+    for (int64_t b0 = tid; b0 < totr; b0 += static_cast<int64_t>(kThreads) * kUnroll) {
       uint4 x[kUnroll];
       char *d[kUnroll];
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
         const int64_t q = b0 + static_cast<int64_t>(u) * kThreads;
         d[u] = nullptr;
-        if (q < totc) {
+        if (q < totr) {
           const uint32_t q32 = static_cast<uint32_t>(q);
           const int f = static_cast<int>(q32 / static_cast<uint32_t>(a.rec16));
           const int o = static_cast<int>(q32 - static_cast<uint32_t>(f) * a.rec16);
@@ -1146,8 +1155,7 @@ __device__ void pt_worker_finish(const PtArgs &a, int r, int i0, int n, int32_t 
         if (d[u]) st_v4(d[u], x[u]);
     }
   }
-  // the slice's slot vector ([DD] §3.5 stage 5: aligned with the list); it
-  // needs no record bytes, so it goes out before the staged loads land
+  // the slice's slot vector ([DD] §3.5 stage 5: aligned with the list)
   int32_t *g_out = a.out + static_cast<int64_t>(r) * a.k + i0;
   for (int t = tid; t < n; t += kThreads) {
     const int32_t val = w_out[t];
@@ -1258,13 +1266,14 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_pt_kernel(const PtArgs a)
     // one CTA plays every role in order; nothing to overlap, nothing staged
     pt_leader_load_state(a, r, false, make_int4(0, 0, 0, 0), smem, L);
     pt_leader_write_through(a, r, prev, smem, L);
-    pt_worker_classify(a, r, i0, n, newest, first, smem, L);
+    const int mw = pt_worker_classify(a, r, i0, n, newest, first, smem, L);
+    pt_worker_order(a, 0, mw, smem, L);
     pt_leader_decide(a, cs, nw, newest, smem, L);
     __syncthreads();
     pt_leader_push(cs, nw, smem, L);
     pt_leader_publish<kRecordPlan>(a, r, prev, skip_pos, smem, L);
     __syncthreads();
-    pt_worker_finish(a, r, i0, n, skip_pos, false, nullptr, src, dst, smem, L);
+    pt_worker_finish(a, r, i0, n, skip_pos, 0, nullptr, src, dst, smem, L);
     return;
   }
   if (leader) {
@@ -1286,36 +1295,35 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_pt_kernel(const PtArgs a)
     return;
   }
   // worker
-  pt_worker_classify(a, r, i0, n, newest, first, smem, L);
+  const int mw = pt_worker_classify(a, r, i0, n, newest, first, smem, L);
   // #0: the slice, for the leader.  The block barrier that ends the
   // classification orders every thread's shared-memory writes before the last
   // warp's cluster-scope fence, which releases them all; the other warps
   // arrive without a fence, so their host loads below do not wait on one.
   if (tid >= kThreads - 32) fence_acq_rel_cluster();
   cluster_arrive_relaxed();
-  // Read this slice's missed records into registers now, before any victim is
-  // known: the reads fly while the leader decides.
+  // Read the slice's first missed records into registers now, in list order,
+  // before any victim is known: the reads fly while the leader decides.
   const int32_t *w_mp = reinterpret_cast<const int32_t *>(smem + L.w_mp);
-  const int32_t *w_ord = reinterpret_cast<const int32_t *>(smem + L.w_ord);
-  const uint32_t *w_misc = reinterpret_cast<const uint32_t *>(smem + L.w_misc);
-  const int64_t totc = static_cast<int64_t>(w_misc[kWCount]) * a.rec16;
-  const bool stage = a.io;
+  const int staged = a.io ? min(mw, kStage * kThreads / a.rec16) : 0;
+  const int64_t totc = static_cast<int64_t>(staged) * a.rec16;
   uint4 v[kStage];
 #pragma unroll
   for (int u = 0; u < kStage; ++u) {
     const int64_t q = tid + static_cast<int64_t>(u) * kThreads;
-    if (stage && q < totc) {
+    if (q < totc) {
       const uint32_t q32 = static_cast<uint32_t>(q);
       const int f = static_cast<int>(q32 / static_cast<uint32_t>(a.rec16));
       const int o = static_cast<int>(q32 - static_cast<uint32_t>(f) * a.rec16);
-      const int32_t pm = w_mp[w_ord[f]];
+      const int32_t pm = w_mp[f];
       if (pm != skip_pos) v[u] = ld_nc_v4(src + static_cast<int64_t>(pm) * a.src_row_stride + 16 * o);
     }
   }
+  pt_worker_order(a, staged, mw, smem, L);  // the rest go out in host-row order later
   cluster_wait_acquire();
   cluster_arrive_relaxed();  // #1: nothing new to publish; the staged loads stay in flight
   cluster_wait_acquire();    //    the leader's decision is visible
-  pt_worker_finish(a, r, i0, n, skip_pos, stage, v, src, dst, smem, L);
+  pt_worker_finish(a, r, i0, n, skip_pos, staged, v, src, dst, smem, L);
 }
 
 // ---------------------------------------------------------------------------

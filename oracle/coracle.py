@@ -56,6 +56,9 @@ def _load():
         lib.hso_resolve_unit.restype = ctypes.c_int32
         lib.hso_resolve_layer.argtypes = [P, vp, vp, ctypes.c_int32, ctypes.c_int32, vp]
         lib.hso_resolve_layer.restype = ctypes.c_int32
+        lib.hso_resolve_layer_res.argtypes = [P, vp, vp, vp, ctypes.c_int32, ctypes.c_int32,
+                                              ctypes.c_int32, ctypes.c_int32, vp]
+        lib.hso_resolve_layer_res.restype = ctypes.c_int32
         lib.hso_set_newest_rows.argtypes = [P, vp, ctypes.c_int32]
         lib.hso_writeback.argtypes = [P, vp, ctypes.c_int32]
         lib.hso_writeback.restype = ctypes.c_int32
@@ -115,14 +118,22 @@ class OracleLayer:
         for rr in (range(self.R) if r is None else [r]):
             self._lib.hso_reset_unit(ctypes.byref(self._s), rr)
 
-    def resolve(self, sel, newest=None, num_reqs=None, io=True):
-        """sel int32 [R][k]; newest int32 [R] or None.  Returns (out [R][k], err)."""
+    def resolve(self, sel, newest=None, num_reqs=None, io=True, res_blocks=None, res_tok=1):
+        """sel int32 [R][k]; newest int32 [R] or None; res_blocks int32
+        [R][nblk] (resident block table, -1 = not resident) or None.
+        Returns (out [R][k], err)."""
         sel = np.ascontiguousarray(sel, dtype=np.int32)
         nr = self.R if num_reqs is None else num_reqs
         out = np.full((self.R, self.k), -1, np.int32)
         nw = None if newest is None else np.ascontiguousarray(newest, dtype=np.int32)
-        e = self._lib.hso_resolve_layer(ctypes.byref(self._s), _p(sel), _p(nw), nr, int(bool(io)),
-                                        _p(out))
+        if res_blocks is None:
+            e = self._lib.hso_resolve_layer(ctypes.byref(self._s), _p(sel), _p(nw), nr,
+                                            int(bool(io)), _p(out))
+        else:
+            rb = np.ascontiguousarray(res_blocks, dtype=np.int32)
+            e = self._lib.hso_resolve_layer_res(ctypes.byref(self._s), _p(sel), _p(nw), _p(rb),
+                                                rb.shape[1], int(res_tok), nr, int(bool(io)),
+                                                _p(out))
         return out, e
 
     def set_newest_rows(self, rows, num_reqs=None):

@@ -22,10 +22,18 @@
  *
  * The page table is a direct-address table over [0, P) (-1 = host-only), which
  * is the plainest dictionary for integer keys in a known range.
+ *
+ * Three-tier resolve (docs.vllm.ai "HiSparse local KV offload architecture",
+ * "Hot lookup and LRU"; gentlecold.top §6.5): with a resident block table, a
+ * position whose block has a device-resident copy resolves to that copy first
+ * (output B + 1 + row, row = entry * block_tokens + offset in the block) and
+ * is neither a hit nor a miss.  A block entry below -1, or a row whose output
+ * does not fit int32, fails the unit like an out-of-range position.
  */
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#include <limits.h>
 
 #define HSO_ERR_RANGE 1
 #define HSO_ERR_DUP 2
@@ -78,12 +86,31 @@ void hso_reset_unit(hso_layer *L, int32_t r) {
   L->plan_count[r] = 0;
 }
 
+/* Resident row of position p for one request's block table `blk` ([nblk],
+   entries -1 = not resident), -1 if not resident, -2 if the entry or the row
+   is invalid. */
+static int64_t resident_row(const hso_layer *L, const int32_t *blk, int32_t nblk, int32_t tok,
+                            int32_t p) {
+  int64_t b, e, row;
+  if (!blk) return -1;
+  b = p / tok;
+  if (b >= nblk) return -1;
+  e = blk[b];
+  if (e == -1) return -1;
+  if (e < -1) return -2;
+  row = e * tok + p % tok;
+  if ((int64_t)L->B + 1 + row > INT32_MAX) return -2;
+  return row;
+}
+
 /* RESOLVE for unit (r) of this layer.  sel: [k]; out: [k].
    io: 1 = copy missed records from the host pool into the hot rows,
        0 = metadata only (the pages' no-IO mode: bytes left stale).
+   blk / nblk / tok: this request's resident block table (NULL: none).
    Returns 0 or a bit-OR of HSO_ERR_*. */
-int32_t hso_resolve_unit(hso_layer *L, int32_t r, const int32_t *sel, int32_t newest,
-                         int32_t io, int32_t *out) {
+int32_t hso_resolve_unit_res(hso_layer *L, int32_t r, const int32_t *sel, int32_t newest,
+                             int32_t io, const int32_t *blk, int32_t nblk, int32_t tok,
+                             int32_t *out) {
   const int32_t B = L->B, k = L->k;
   const int64_t P = L->P;
   int32_t *slot_pos = L->slot_pos + (int64_t)r * B;
@@ -101,6 +128,7 @@ int32_t hso_resolve_unit(hso_layer *L, int32_t r, const int32_t *sel, int32_t ne
     if (p < -1 || (int64_t)p >= P) { err |= HSO_ERR_RANGE; continue; }
     if (L->mark[p] == L->mark_gen) err |= HSO_ERR_DUP;
     L->mark[p] = L->mark_gen;
+    if (resident_row(L, blk, nblk, tok, p) == -2) err |= HSO_ERR_RANGE;
   }
   if (newest < -1 || (int64_t)newest >= P) err |= HSO_ERR_RANGE;
   L->unit_err[r] = err;
@@ -117,6 +145,8 @@ int32_t hso_resolve_unit(hso_layer *L, int32_t r, const int32_t *sel, int32_t ne
     int32_t p = sel[i];
     if (p == -1) {
       out[i] = -1;
+    } else if (resident_row(L, blk, nblk, tok, p) >= 0) {
+      out[i] = (int32_t)(L->B + 1 + resident_row(L, blk, nblk, tok, p));
     } else if (newest >= 0 && p == newest) {
       out[i] = B;
     } else if (pt[p] >= 0) {
@@ -159,15 +189,28 @@ int32_t hso_resolve_unit(hso_layer *L, int32_t r, const int32_t *sel, int32_t ne
   return 0;
 }
 
+int32_t hso_resolve_unit(hso_layer *L, int32_t r, const int32_t *sel, int32_t newest,
+                         int32_t io, int32_t *out) {
+  return hso_resolve_unit_res(L, r, sel, newest, io, NULL, 0, 1, out);
+}
+
 /* One layer-step over requests [0, num_reqs): sel [R][k], newest [R] or NULL,
-   out [R][k].  Returns the bit-OR of the units' errors. */
-int32_t hso_resolve_layer(hso_layer *L, const int32_t *sel, const int32_t *newest,
-                          int32_t num_reqs, int32_t io, int32_t *out) {
+   res_blocks [R][nblk] or NULL, out [R][k].  Returns the bit-OR of the units'
+   errors. */
+int32_t hso_resolve_layer_res(hso_layer *L, const int32_t *sel, const int32_t *newest,
+                              const int32_t *res_blocks, int32_t nblk, int32_t tok,
+                              int32_t num_reqs, int32_t io, int32_t *out) {
   int32_t r, e = 0;
   for (r = 0; r < num_reqs; r++)
-    e |= hso_resolve_unit(L, r, sel + (int64_t)r * L->k, newest ? newest[r] : -1, io,
-                          out + (int64_t)r * L->k);
+    e |= hso_resolve_unit_res(L, r, sel + (int64_t)r * L->k, newest ? newest[r] : -1, io,
+                              res_blocks ? res_blocks + (int64_t)r * nblk : NULL, nblk, tok,
+                              out + (int64_t)r * L->k);
   return e;
+}
+
+int32_t hso_resolve_layer(hso_layer *L, const int32_t *sel, const int32_t *newest,
+                          int32_t num_reqs, int32_t io, int32_t *out) {
+  return hso_resolve_layer_res(L, sel, newest, NULL, 0, 1, num_reqs, io, out);
 }
 
 /* The caller writes the new token's KV into row B of each request. */

@@ -30,6 +30,16 @@ readings of points the pages leave open:
       the whole unit fail with its state untouched and an output row of -1;
   R8  the miss count excludes padding and the newest binding.
 
+With a resident tier (the three-tier resolver of docs.vllm.ai "HiSparse local
+KV offload architecture", "Hot lookup and LRU"; gentlecold.top §6.5), a
+position whose block has a device-resident copy resolves to that copy before
+the hot buffer is consulted, and touches neither the LRU nor the page table:
+  R14 the resident check comes first, before the newest binding and the hot
+      lookup; a resident selection outputs ``B + 1 + row`` (row = its block's
+      entry * block size + the position's offset in the block) and is neither
+      a hit nor a miss; a block entry below -1, or a row too large for that
+      encoding in int32, fails the unit like an out-of-range position.
+
 See ``tests/test_oracle_pins.py`` for what pins each of these.
 
 [P1] = gentlecold.top, "HiSparse 深度解析：论文、SGLang 实现与 vLLM Hybrid
@@ -38,6 +48,7 @@ HiSparse" (sections as numbered on that page).
 
 ERR_RANGE = 1  # a position outside [-1, P), or newest outside [-1, P)
 ERR_DUP = 2    # the same position appears twice in one selection
+INT32_MAX = 2**31 - 1
 
 
 class Unit:
@@ -56,19 +67,33 @@ class Unit:
         self.miss_count = 0
 
     # ------------------------------------------------------------------ #
-    def resolve(self, sel, newest=-1, skip_io=False):
+    def resolve(self, sel, newest=-1, skip_io=False, res_blocks=None, res_tok=1):
         """One RESOLVE of this unit for the selection list ``sel``.
 
         Returns ``(out, plan, err)``: ``out[i]`` is the physical slot for
-        ``sel[i]`` (``B`` for the newest token, -1 for padding); ``plan`` is
-        the list of ``(pos, slot)`` fetches in miss order ([P1] §5.5, the miss
-        plan written where the eviction is decided); ``err`` is 0 or a bit-OR
-        of ``ERR_RANGE`` / ``ERR_DUP``.
+        ``sel[i]`` (``B`` for the newest token, -1 for padding, ``B + 1 + row``
+        for a resident copy); ``plan`` is the list of ``(pos, slot)`` fetches in
+        miss order ([P1] §5.5, the miss plan written where the eviction is
+        decided); ``err`` is 0 or a bit-OR of ``ERR_RANGE`` / ``ERR_DUP``.
+        ``res_blocks`` (optional) is this request's resident block table: the
+        entry of block ``p // res_tok`` is -1 (not resident) or the block's
+        index in the resident store (reading R14).
         """
         B, P = self.B, self.P
         k = len(sel)
 
-        # Validation (reading R6).
+        def resident_row(p):
+            if res_blocks is None or p // res_tok >= len(res_blocks):
+                return -1
+            e = res_blocks[p // res_tok]
+            if e < -1:
+                return None                # invalid entry
+            if e == -1:
+                return -1
+            row = e * res_tok + p % res_tok
+            return row if B + 1 + row <= INT32_MAX else None
+
+        # Validation (readings R6 and R14).
         err = 0
         seen = set()
         for p in sel:
@@ -80,19 +105,24 @@ class Unit:
             if p in seen:
                 err |= ERR_DUP
             seen.add(p)
+            if resident_row(p) is None:
+                err |= ERR_RANGE
         if newest < -1 or newest >= P:
             err |= ERR_RANGE
         if err:
             self.miss_count = 0            # nothing was fetched this step
             return [-1] * k, [], err
 
-        # Stages 1-2: classify every selection as padding, newest, hit or miss.
+        # Stages 1-2: classify every selection as padding, resident, newest,
+        # hit or miss.
         out = [None] * k
         hit_slots = set()
         misses = []                        # selection indices, in list order
         for i, p in enumerate(sel):
             if p == -1:
                 out[i] = -1
+            elif resident_row(p) >= 0:
+                out[i] = B + 1 + resident_row(p)   # reading R14
             elif newest >= 0 and p == newest:
                 out[i] = B                 # reading R4
             elif p in self.page_table:

@@ -72,10 +72,11 @@ class CUnit:
     def preset(self, slot_pos, lru):
         self._pending = (list(slot_pos), list(lru))
 
-    def resolve(self, sel, newest=-1, skip_io=False):
+    def resolve(self, sel, newest=-1, skip_io=False, res_blocks=None, res_tok=1):
         L = self._layer(len(sel))
+        rb = None if res_blocks is None else np.array([res_blocks], np.int32)
         out, e = L.resolve(np.array([sel], np.int32), np.array([newest], np.int32),
-                           io=not skip_io)
+                           io=not skip_io, res_blocks=rb, res_tok=res_tok)
         plan = [(int(L.plan_pos[0, j]), int(L.plan_slot[0, j])) for j in range(L.plan_count[0])]
         return [int(x) for x in out[0]], plan, int(e)
 
@@ -336,6 +337,100 @@ def pin_belady_bound(cls, seeds=range(40)):
         assert total >= optimal_misses(trace, B), (seed, total)
 
 
+# ---------------------------------------------------------------------- #
+# The resident tier (docs.vllm.ai "HiSparse local KV offload architecture", #
+# "Hot lookup and LRU": resident page -> resident physical row, before the  #
+# hot lookup; resident hits bypass the hot LRU and host copies)             #
+# ---------------------------------------------------------------------- #
+def _snap(u):
+    return list(u.slot_pos), list(u.lru), dict(u.page_table), u.miss_count
+
+
+def pin_resident_none_is_plain(cls, seeds=range(8)):
+    """An all -1 block table changes nothing: same outputs, plan and state."""
+    for seed in seeds:
+        rnd = random.Random(7000 + seed)
+        k, B, P, tok = 5, 8, 40, 4
+        a, b = make(cls, B, P, k=k), make(cls, B, P, k=k)
+        blocks = [-1] * (P // tok)
+        for _ in range(10):
+            sel = rnd.sample(range(P), k)
+            newest = rnd.choice([-1, sel[0]])
+            ra = a.resolve(sel, newest=newest, res_blocks=blocks, res_tok=tok)
+            rb = b.resolve(sel, newest=newest)
+            assert ra == rb and _snap(a) == _snap(b)
+
+
+def pin_resident_masks(cls, seeds=range(20)):
+    """A resident selection acts on the cache exactly as padding would, and
+    outputs B + 1 + (entry * block size + offset): the state, plan and miss
+    count equal those of the same list with its resident entries set to -1.
+    Block tables change from step to step, so positions resident now are
+    often hot from earlier steps, and the newest position is sometimes
+    resident (the resident check comes first)."""
+    for seed in seeds:
+        rnd = random.Random(8000 + seed)
+        k = rnd.randint(2, 6)
+        B = k + rnd.randint(0, 3)
+        tok = rnd.choice([1, 2, 4])
+        P = tok * rnd.randint(8, 12)
+        host = lambda p: bytes([(p * 11 + i) & 0xFF for i in range(8)])  # noqa: E731
+        a, b = make(cls, B, P, k=k, host=host), make(cls, B, P, k=k, host=host)
+        for t in range(12):
+            nb = P // tok
+            blocks = [rnd.randrange(50) if rnd.random() < 0.35 else -1 for _ in range(nb - 1)]
+            sel = rnd.sample(range(P), rnd.randint(1, k))
+            sel += [-1] * (k - len(sel))
+            rnd.shuffle(sel)
+            newest = rnd.choice([-1] + [p for p in sel if p >= 0])
+            row = {}
+            for p in sel:
+                if p >= 0 and p // tok < len(blocks) and blocks[p // tok] >= 0:
+                    row[p] = blocks[p // tok] * tok + p % tok
+            masked = [-1 if p in row else p for p in sel]
+            oa, pa, ea = a.resolve(sel, newest=newest, res_blocks=blocks, res_tok=tok)
+            ob, pb, eb = b.resolve(masked, newest=newest)
+            assert ea == 0 and eb == 0
+            assert [tuple(x) for x in pa] == [tuple(x) for x in pb]
+            assert _snap(a) == _snap(b), (seed, t)
+            for i, p in enumerate(sel):
+                assert oa[i] == (B + 1 + row[p] if p in row else ob[i]), (seed, t, i)
+            assert a.hot[:B] == b.hot[:B]
+
+
+def pin_resident_all(cls):
+    """A request whose every selection is resident leaves its cache untouched."""
+    k, B, P, tok = 4, 6, 32, 8
+    u = make(cls, B, P, k=k)
+    u.resolve([1, 9, 17, 25])
+    snap = _snap(u)[:3]
+    blocks = [3, 0, 5, 2]
+    out, plan, err = u.resolve([9, 2, 30, -1], newest=30, res_blocks=blocks, res_tok=tok)
+    assert err == 0 and plan == [] and u.miss_count == 0
+    assert out == [B + 1 + 0 * 8 + 1, B + 1 + 3 * 8 + 2, B + 1 + 2 * 8 + 6, -1]
+    assert _snap(u)[:3] == snap
+
+
+def pin_resident_errors(cls):
+    """An invalid block entry (below -1) or a row past int32 fails the unit,
+    state untouched, but only when a selected position falls in that block."""
+    k, B, P, tok = 3, 4, 16, 4
+    u = make(cls, B, P, k=k)
+    u.resolve([1, 2, 3])
+    snap = _snap(u)[:3]
+    out, plan, err = u.resolve([4, 9, 0], res_blocks=[-1, -5, 2, -1], res_tok=tok)
+    assert err == 1 and out == [-1] * 3 and _snap(u)[:3] == snap
+    out, plan, err = u.resolve([4, 9, 0], res_blocks=[-1, 2**29, 2, -1], res_tok=tok)
+    assert err == 1 and out == [-1] * 3 and _snap(u)[:3] == snap
+    out, plan, err = u.resolve([0, 9, 13], res_blocks=[-1, -1, 2, -5], res_tok=tok)
+    assert err == 1
+    out, plan, err = u.resolve([0, 9, 1], res_blocks=[-1, -1, 2, -5], res_tok=tok)
+    assert err == 0 and out[1] == B + 1 + 2 * 4 + 1
+
+
+RESIDENT_PINS = [pin_resident_none_is_plain, pin_resident_masks, pin_resident_all,
+                 pin_resident_errors]
+
 ALL_PINS = [pin_example_b, pin_example_a, pin_textbook_lru, pin_hit_order, pin_miss_order,
             pin_newest_and_padding, pin_errors, pin_invariants, pin_disjoint_at_b_equals_k,
-            pin_belady_bound]
+            pin_belady_bound] + RESIDENT_PINS

@@ -74,8 +74,9 @@ def test_optimal_closed_forms():
 # ---------------------------------------------------------------------- #
 # Python model == C model, full state, on random traces                   #
 # ---------------------------------------------------------------------- #
+@pytest.mark.parametrize("resident", [False, True])
 @pytest.mark.parametrize("seed", range(12))
-def test_python_equals_c(seed):
+def test_python_equals_c(seed, resident):
     from oracle.coracle import OracleLayer
     rnd = random.Random(seed)
     R = rnd.randint(1, 3)
@@ -101,10 +102,18 @@ def test_python_equals_c(seed):
             rnd.shuffle(sel[r])
             if S and rnd.random() < 0.3:
                 newest[r] = rnd.choice(S)
-        out_c, e_c = c.resolve(sel, newest)
+        tok, blocks = rnd.choice([1, 2, 4]), None
+        if resident:
+            nb = rnd.randint(1, P // tok + 1)
+            blocks = np.array([[rnd.randrange(200) if rnd.random() < 0.3 else
+                                (-1 if rnd.random() < 0.97 else -4) for _ in range(nb)]
+                               for _ in range(R)], np.int32)
+        out_c, e_c = c.resolve(sel, newest, res_blocks=blocks, res_tok=tok)
         e_py = 0
         for r in range(R):
-            out, plan, err = py[r].resolve([int(x) for x in sel[r]], int(newest[r]))
+            out, plan, err = py[r].resolve([int(x) for x in sel[r]], int(newest[r]),
+                                           res_blocks=None if blocks is None else
+                                           [int(x) for x in blocks[r]], res_tok=tok)
             e_py |= err
             assert out == list(out_c[r]), (t, r)
             assert err == c.unit_err[r]
@@ -178,9 +187,21 @@ def test_replay_follows_anchor_slots():
 class _Mutant(Unit):
     mutation = None
 
-    def resolve(self, sel, newest=-1, skip_io=False):
+    def resolve(self, sel, newest=-1, skip_io=False, res_blocks=None, res_tok=1):
         m = self.mutation
         B, P, k = self.B, self.P, len(sel)
+
+        def rrow(p):
+            if res_blocks is None or p // res_tok >= len(res_blocks):
+                return -1
+            e = res_blocks[p // res_tok]
+            if e < -1 and m != "resident_no_entry_check":
+                return None
+            if e < 0:
+                return -1
+            row = e * res_tok + (0 if m == "resident_no_offset" else p % res_tok)
+            return row if B + 1 + row < 2**31 else None
+
         err, seen = 0, set()
         for p in sel:
             if p == -1:
@@ -191,17 +212,31 @@ class _Mutant(Unit):
             if p in seen and m != "no_dup_check":
                 err |= ERR_DUP
             seen.add(p)
+            if rrow(p) is None:
+                err |= ERR_RANGE
         if newest < -1 or newest >= P:
             err |= ERR_RANGE
         if err:
             return [-1] * k, [], err
         out, hits, misses = [None] * k, [], []
         for i, p in enumerate(sel):
+            hot = p in self.page_table
             if p == -1:
                 out[i] = -1
+            elif m == "resident_after_hot" and hot:
+                out[i] = self.page_table[p]
+                hits.append(out[i])
+            elif m == "resident_after_newest" and newest >= 0 and p == newest:
+                out[i] = B
+            elif rrow(p) >= 0:
+                out[i] = B + 1 + rrow(p)
+                if m == "resident_is_hit" and hot:
+                    hits.append(self.page_table[p])
+                if m == "resident_counts_miss":
+                    misses.append(i)
             elif newest >= 0 and p == newest and m != "newest_is_miss":
                 out[i] = B
-            elif p in self.page_table:
+            elif hot:
                 out[i] = self.page_table[p]
                 hits.append(out[i])
             else:
@@ -243,7 +278,10 @@ class _Mutant(Unit):
 
 MUTATIONS = ["no_dup_check", "newest_is_miss", "victims_from_newest_end", "keep_stale_mapping",
              "no_fetch", "fetch_off_by_one", "hits_in_selection_order", "hits_before_misses",
-             "misses_oldest", "misses_reversed", "count_newest"]
+             "misses_oldest", "misses_reversed", "count_newest",
+             # resident tier
+             "resident_after_hot", "resident_after_newest", "resident_is_hit",
+             "resident_counts_miss", "resident_no_offset", "resident_no_entry_check"]
 
 
 @pytest.mark.parametrize("mutation", MUTATIONS)

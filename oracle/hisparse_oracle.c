@@ -28,7 +28,9 @@
  * position whose block has a device-resident copy resolves to that copy first
  * (output B + 1 + row, row = entry * block_tokens + offset in the block) and
  * is neither a hit nor a miss.  A block entry below -1, or a row whose output
- * does not fit int32, fails the unit like an out-of-range position.
+ * does not fit int32, fails the unit like an out-of-range position.  The
+ * duplicate check covers positions that reach the hot tier only (a resident
+ * position never touches the cache; the pages exit before the hash table).
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -119,6 +121,7 @@ int32_t hso_resolve_unit_res(hso_layer *L, int32_t r, const int32_t *sel, int32_
   int32_t *plan_pos = L->plan_pos + (int64_t)r * k;
   int32_t *plan_slot = L->plan_slot + (int64_t)r * k;
   int32_t err = 0, i, j, s, M = 0, E = 0, n = 0;
+  int64_t rr;
 
   /* validation */
   L->mark_gen++;
@@ -126,9 +129,11 @@ int32_t hso_resolve_unit_res(hso_layer *L, int32_t r, const int32_t *sel, int32_
     int32_t p = sel[i];
     if (p == -1) continue;
     if (p < -1 || (int64_t)p >= P) { err |= HSO_ERR_RANGE; continue; }
+    rr = resident_row(L, blk, nblk, tok, p);
+    if (rr == -2) { err |= HSO_ERR_RANGE; continue; }
+    if (rr >= 0) continue; /* resident: never reaches the hot tier */
     if (L->mark[p] == L->mark_gen) err |= HSO_ERR_DUP;
     L->mark[p] = L->mark_gen;
-    if (resident_row(L, blk, nblk, tok, p) == -2) err |= HSO_ERR_RANGE;
   }
   if (newest < -1 || (int64_t)newest >= P) err |= HSO_ERR_RANGE;
   L->unit_err[r] = err;

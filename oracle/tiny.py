@@ -38,7 +38,11 @@ the hot buffer is consulted, and touches neither the LRU nor the page table:
       lookup; a resident selection outputs ``B + 1 + row`` (row = its block's
       entry * block size + the position's offset in the block) and is neither
       a hit nor a miss; a block entry below -1, or a row too large for that
-      encoding in int32, fails the unit like an out-of-range position.
+      encoding in int32, fails the unit like an out-of-range position.  The
+      duplicate check covers the positions that reach the hot tier: a
+      resident position never touches the cache, and the pages place the
+      resident exit before the hash table is built, so a repeated resident
+      position is not an error and outputs its row at each index.
 
 See ``tests/test_oracle_pins.py`` for what pins each of these.
 
@@ -102,11 +106,15 @@ class Unit:
             if p < -1 or p >= P:
                 err |= ERR_RANGE
                 continue
+            rr = resident_row(p)
+            if rr is None:
+                err |= ERR_RANGE
+                continue
+            if rr >= 0:
+                continue                   # never reaches the hot tier (R14)
             if p in seen:
                 err |= ERR_DUP
             seen.add(p)
-            if resident_row(p) is None:
-                err |= ERR_RANGE
         if newest < -1 or newest >= P:
             err |= ERR_RANGE
         if err:

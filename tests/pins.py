@@ -428,8 +428,20 @@ def pin_resident_errors(cls):
     assert err == 0 and out[1] == B + 1 + 2 * 4 + 1
 
 
+def pin_resident_repeat(cls):
+    """A repeated resident position is not a duplicate (it never reaches the
+    hot tier) and outputs its row at each index; a repeat that reaches the hot
+    tier still fails the unit."""
+    k, B, P, tok = 4, 6, 32, 4
+    u = make(cls, B, P, k=k)
+    out, plan, err = u.resolve([5, 9, 5, 20], res_blocks=[-1, 7, -1, -1], res_tok=tok)
+    assert err == 0 and out[0] == out[2] == B + 1 + 7 * 4 + 1 and u.miss_count == 2
+    out, plan, err = u.resolve([5, 9, 9, 20], res_blocks=[-1, 7, -1, -1], res_tok=tok)
+    assert err == 2 and out == [-1] * 4
+
+
 RESIDENT_PINS = [pin_resident_none_is_plain, pin_resident_masks, pin_resident_all,
-                 pin_resident_errors]
+                 pin_resident_errors, pin_resident_repeat]
 
 ALL_PINS = [pin_example_b, pin_example_a, pin_textbook_lru, pin_hit_order, pin_miss_order,
             pin_newest_and_padding, pin_errors, pin_invariants, pin_disjoint_at_b_equals_k,

@@ -209,11 +209,14 @@ class _Mutant(Unit):
             if p < -1 or p >= P:
                 err |= ERR_RANGE
                 continue
+            if rrow(p) is None:
+                err |= ERR_RANGE
+                continue
+            if rrow(p) >= 0 and m != "resident_dup_checked":
+                continue
             if p in seen and m != "no_dup_check":
                 err |= ERR_DUP
             seen.add(p)
-            if rrow(p) is None:
-                err |= ERR_RANGE
         if newest < -1 or newest >= P:
             err |= ERR_RANGE
         if err:
@@ -281,7 +284,8 @@ MUTATIONS = ["no_dup_check", "newest_is_miss", "victims_from_newest_end", "keep_
              "misses_oldest", "misses_reversed", "count_newest",
              # resident tier
              "resident_after_hot", "resident_after_newest", "resident_is_hit",
-             "resident_counts_miss", "resident_no_offset", "resident_no_entry_check"]
+             "resident_counts_miss", "resident_no_offset", "resident_no_entry_check",
+             "resident_dup_checked"]
 
 
 @pytest.mark.parametrize("mutation", MUTATIONS)

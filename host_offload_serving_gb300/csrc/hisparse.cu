@@ -643,6 +643,11 @@ struct PtArgs {
   char *host_w;
   int64_t host_req_stride, host_row_stride;
   int32_t prev_from_row;
+  // Resident tier (three-tier resolve): per request a block table
+  // [R][res_nblk] of resident block indices (-1 = not resident), res_tok
+  // positions per block; NULL = no resident tier.
+  const int32_t *res_blocks;
+  int32_t res_nblk, res_tok;
   int64_t P;
   const int32_t *sel, *num_reqs, *newest;
   int32_t *out;
@@ -744,6 +749,7 @@ __device__ __forceinline__ bool bit_of(const uint32_t *bits, int s) {
 }
 
 // Worker: classify selections [i0, i0 + n) of request r.
+template <bool kResident>
 __device__ int pt_worker_classify(const PtArgs &a, int r, int i0, int n, int32_t newest,
                                   const int32_t (&first)[kGroup], unsigned char *smem,
                                   const PtLayout &L) {
@@ -763,6 +769,7 @@ __device__ int pt_worker_classify(const PtArgs &a, int r, int i0, int n, int32_t
   __syncthreads();
   const int32_t *g_sel = a.sel + static_cast<int64_t>(r) * a.k + i0;
   const int32_t *g_pt = a.page_table + static_cast<int64_t>(r) * P;
+  const int32_t *g_res = kResident ? a.res_blocks + static_cast<int64_t>(r) * a.res_nblk : nullptr;
   for (int base = 0; base < n; base += kGroup * kThreads) {
     int32_t p[kGroup], s[kGroup];
 #pragma unroll
@@ -770,10 +777,15 @@ __device__ int pt_worker_classify(const PtArgs &a, int r, int i0, int n, int32_t
       const int t = base + u * kThreads + tid;
       p[u] = base == 0 ? first[u] : (t < n ? g_sel[t] : -1);
     }
+    int32_t e[kGroup];  // resident block entry of each selection (-1: none)
 #pragma unroll
     for (int u = 0; u < kGroup; ++u) {
       s[u] = -1;
-      if (p[u] >= 0 && p[u] < P && p[u] != newest) s[u] = g_pt[p[u]];
+      e[u] = -1;
+      if (p[u] >= 0 && p[u] < P) {
+        if (kResident && p[u] / a.res_tok < a.res_nblk) e[u] = g_res[p[u] / a.res_tok];
+        if (p[u] != newest) s[u] = g_pt[p[u]];
+      }
     }
 #pragma unroll
     for (int u = 0; u < kGroup; ++u) {
@@ -785,6 +797,16 @@ __device__ int pt_worker_classify(const PtArgs &a, int r, int i0, int n, int32_t
       } else if (p[u] < -1 || p[u] >= P) {
         atomicOr(&w_misc[kWErr], HISPARSE_ERR_RANGE);
         v = -1;
+      } else if (kResident && e[u] != -1) {
+        // resident copy: B + 1 + row, no hit, no miss, no duplicate check
+        // (vLLM docs "Hot lookup and LRU"; gentlecold.top §6.5)
+        const int64_t row = static_cast<int64_t>(e[u]) * a.res_tok + p[u] % a.res_tok;
+        if (e[u] < -1 || static_cast<int64_t>(B) + 1 + row > INT32_MAX) {
+          atomicOr(&w_misc[kWErr], HISPARSE_ERR_RANGE);
+          v = -1;
+        } else {
+          v = static_cast<int32_t>(B + 1 + row);
+        }
       } else if (p[u] == newest) {
         atomicAdd(&w_misc[kWNewest], 1u);
         v = B;
@@ -1215,7 +1237,7 @@ __device__ void pt_leader_write_through(const PtArgs &a, int r, int32_t prev, un
   }
 }
 
-template <bool kRecordPlan>
+template <bool kRecordPlan, bool kResident>
 __global__ void __launch_bounds__(kThreads, 1) resolve_pt_kernel(const PtArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   // Programmatic dependent launch: this grid may be set up while the previous
@@ -1266,7 +1288,7 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_pt_kernel(const PtArgs a)
     // one CTA plays every role in order; nothing to overlap, nothing staged
     pt_leader_load_state(a, r, false, make_int4(0, 0, 0, 0), smem, L);
     pt_leader_write_through(a, r, prev, smem, L);
-    const int mw = pt_worker_classify(a, r, i0, n, newest, first, smem, L);
+    const int mw = pt_worker_classify<kResident>(a, r, i0, n, newest, first, smem, L);
     pt_worker_order(a, 0, mw, smem, L);
     pt_leader_decide(a, cs, nw, newest, smem, L);
     __syncthreads();
@@ -1295,7 +1317,7 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_pt_kernel(const PtArgs a)
     return;
   }
   // worker
-  const int mw = pt_worker_classify(a, r, i0, n, newest, first, smem, L);
+  const int mw = pt_worker_classify<kResident>(a, r, i0, n, newest, first, smem, L);
   // #0: the slice, for the leader.  The block barrier that ends the
   // classification orders every thread's shared-memory writes before the last
   // warp's cluster-scope fence, which releases them all; the other warps
@@ -1505,20 +1527,24 @@ uint32_t resolve_smem(const hisparse_handle *h, int cs) {
 // for the whole batch (one wave), at most 16.
 int configure_resolve(hisparse_handle *h, int want_cs) {
   const bool hash = h->lookup == HISPARSE_LOOKUP_HASH;
-  const void *fns[2];
+  const void *fns[4];
+  int nf = 2;
   if (hash) {
     fns[0] = reinterpret_cast<const void *>(&resolve_kernel<false>);
     fns[1] = reinterpret_cast<const void *>(&resolve_kernel<true>);
   } else {
-    fns[0] = reinterpret_cast<const void *>(&resolve_pt_kernel<false>);
-    fns[1] = reinterpret_cast<const void *>(&resolve_pt_kernel<true>);
+    fns[0] = reinterpret_cast<const void *>(&resolve_pt_kernel<false, false>);
+    fns[1] = reinterpret_cast<const void *>(&resolve_pt_kernel<true, false>);
+    fns[2] = reinterpret_cast<const void *>(&resolve_pt_kernel<false, true>);
+    fns[3] = reinterpret_cast<const void *>(&resolve_pt_kernel<true, true>);
+    nf = 4;
   }
   uint32_t smax = 0;
   for (int cs = 1; cs <= 16; ++cs) smax = std::max(smax, resolve_smem(h, cs));
   if (smax > 227u * 1024u) return HISPARSE_EBOUND;
-  for (const void *f : fns) {
-    HS_CUDA(cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smax));
-    HS_CUDA(cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
+  for (int i = 0; i < nf; ++i) {
+    HS_CUDA(cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smax));
+    HS_CUDA(cudaFuncSetAttribute(fns[i], cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
   }
   auto active_clusters = [&](int cs) -> int {
     cudaLaunchConfig_t lc = {};
@@ -1881,7 +1907,20 @@ int hisparse_resolve_step(hisparse_handle *h, int32_t layer, const int32_t *d_se
                           const int32_t *d_num_reqs, const int32_t *d_newest,
                           const int32_t *d_prev_pos, const void *d_new_rows, int32_t *d_out,
                           uint32_t flags, void *stream) {
+  return hisparse_resolve_resident(h, layer, d_sel, d_num_reqs, d_newest, d_prev_pos, d_new_rows,
+                                   nullptr, 0, 0, d_out, flags, stream);
+}
+
+int hisparse_resolve_resident(hisparse_handle *h, int32_t layer, const int32_t *d_sel,
+                              const int32_t *d_num_reqs, const int32_t *d_newest,
+                              const int32_t *d_prev_pos, const void *d_new_rows,
+                              const int32_t *d_res_blocks, int32_t res_max_blocks,
+                              int32_t res_block_tokens, int32_t *d_out, uint32_t flags,
+                              void *stream) {
   if (layer_ok(h, layer)) return HISPARSE_EINVAL;
+  if (d_res_blocks && (res_max_blocks < 1 || res_block_tokens < 1 ||
+                       h->lookup == HISPARSE_LOOKUP_HASH))
+    return HISPARSE_EINVAL;
   if (d_new_rows && !aligned16(d_new_rows)) return HISPARSE_EINVAL;
   if (!d_sel || !d_out) return HISPARSE_EINVAL;
   if (flags & ~(HISPARSE_RECORD_PLAN | HISPARSE_SKIP_IO | HISPARSE_FROM_MIRROR)) return HISPARSE_EINVAL;
@@ -1941,6 +1980,9 @@ int hisparse_resolve_step(hisparse_handle *h, int32_t layer, const int32_t *d_se
     a.host_req_stride = Ld.host_req_stride;
     a.host_row_stride = Ld.host_row_stride;
     a.prev_from_row = (d_prev_pos && !(flags & HISPARSE_FROM_MIRROR)) ? 1 : 0;
+    a.res_blocks = d_res_blocks;
+    a.res_nblk = d_res_blocks ? res_max_blocks : 0;
+    a.res_tok = d_res_blocks ? res_block_tokens : 1;
     a.P = h->P;
     a.sel = d_sel; a.num_reqs = d_num_reqs; a.newest = d_newest; a.out = d_out;
     a.slot_pos = m.slot_pos; a.lru = m.lru; a.page_table = m.page_table;
@@ -1950,8 +1992,12 @@ int hisparse_resolve_step(hisparse_handle *h, int32_t layer, const int32_t *d_se
     a.src_req_stride = Ld.host_req_stride; a.src_row_stride = Ld.host_row_stride;
     a.hot = Ld.hot; a.hot_req_stride = Ld.hot_req_stride; a.hot_row_stride = Ld.hot_row_stride;
     lc.numAttrs = 2;  // cluster shape + programmatic dependent launch
-    e = plan ? cudaLaunchKernelEx(&lc, resolve_pt_kernel<true>, a)
-             : cudaLaunchKernelEx(&lc, resolve_pt_kernel<false>, a);
+    if (d_res_blocks)
+      e = plan ? cudaLaunchKernelEx(&lc, resolve_pt_kernel<true, true>, a)
+               : cudaLaunchKernelEx(&lc, resolve_pt_kernel<false, true>, a);
+    else
+      e = plan ? cudaLaunchKernelEx(&lc, resolve_pt_kernel<true, false>, a)
+               : cudaLaunchKernelEx(&lc, resolve_pt_kernel<false, false>, a);
   }
   if (e != cudaSuccess) return cuda_fail(e);
   return HISPARSE_OK;

@@ -45,6 +45,8 @@ SIGNATURES = [
     ("hisparse_destroy", _i32, [_vp]),
     ("hisparse_resolve", _i32, [_vp, _i32, _vp, _vp, _vp, _vp, _u32, _vp]),
     ("hisparse_resolve_step", _i32, [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _u32, _vp]),
+    ("hisparse_resolve_resident", _i32, [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _vp,
+                                         _u32, _vp]),
     ("hisparse_writeback", _i32, [_vp, _i32, _vp, _vp, _vp, _vp]),
     ("hisparse_prefetch_plan", _i32, [_vp, _i32, _i32, _vp, _vp]),
     ("hisparse_copy_miss_counts", _i32, [_vp, _i32, _vp, _vp]),
@@ -119,6 +121,14 @@ def hisparse_resolve_step(h, layer, d_sel, d_num_reqs, d_newest, d_prev_pos, d_n
                           flags, stream):
     return load().hisparse_resolve_step(h, layer, d_sel, d_num_reqs, d_newest, d_prev_pos,
                                         d_new_rows, d_out, flags, stream)
+
+
+def hisparse_resolve_resident(h, layer, d_sel, d_num_reqs, d_newest, d_prev_pos, d_new_rows,
+                              d_res_blocks, res_max_blocks, res_block_tokens, d_out, flags,
+                              stream):
+    return load().hisparse_resolve_resident(h, layer, d_sel, d_num_reqs, d_newest, d_prev_pos,
+                                            d_new_rows, d_res_blocks, res_max_blocks,
+                                            res_block_tokens, d_out, flags, stream)
 
 
 def hisparse_writeback(h, layer, d_pos, d_new_rows, d_num_reqs, stream):

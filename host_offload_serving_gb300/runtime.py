@@ -96,6 +96,17 @@ class HiSparse:
                                         _ptr(prev_pos), _ptr(new_rows), _ptr(out), flags,
                                         _stream(stream)), "hisparse_resolve_step")
 
+    def resolve_resident(self, layer, sel, out, res_blocks, res_block_tokens, num_reqs=None,
+                         newest=None, prev_pos=None, new_rows=None, flags=0, stream=None):
+        """Three-tier RESOLVE: ``res_blocks`` is a device int32 [R][max_blocks]
+        resident block table (-1 = not resident), ``res_block_tokens``
+        positions per block."""
+        H.check(H.hisparse_resolve_resident(self.h, layer, _ptr(sel), _ptr(num_reqs),
+                                            _ptr(newest), _ptr(prev_pos), _ptr(new_rows),
+                                            _ptr(res_blocks), int(res_blocks.shape[1]),
+                                            int(res_block_tokens), _ptr(out), flags,
+                                            _stream(stream)), "hisparse_resolve_resident")
+
     def writeback(self, layer, pos, num_reqs=None, stream=None, new_rows=None):
         H.check(H.hisparse_writeback(self.h, layer, _ptr(pos), _ptr(new_rows), _ptr(num_reqs),
                                      _stream(stream)), "hisparse_writeback")
@@ -204,6 +215,10 @@ class DecodeStep:
     token's KV, placed in row B), and ``out`` int32 [Lr][R][k] receives the slot
     vectors.
 
+    ``resident`` (optional) = (device int32 [R][max_blocks] resident block
+    table, tokens per block) resolves every anchor with the resident tier
+    first (``hisparse_resolve_resident``).
+
     ``fused=True`` (default) writes each anchor's previous token through, and
     installs its new token, inside that anchor's RESOLVE launch
     (``hisparse_resolve_step``); shared-index layers get a write-back launch on
@@ -212,11 +227,12 @@ class DecodeStep:
     pages describe (gentlecold.top "HiSparse 深度解析" §5.4).
     """
 
-    def __init__(self, hs, mem, groups, flags=0, num_reqs=None, fused=True):
+    def __init__(self, hs, mem, groups, flags=0, num_reqs=None, fused=True, resident=None):
         self.hs, self.mem, self.groups = hs, mem, groups
         self.flags = flags
         self.num_reqs = num_reqs
         self.fused = fused
+        self.resident = resident    # (device int32 [R][max_blocks], tokens per block) or None
         self.compute = torch.cuda.Stream()
         self.backup = torch.cuda.Stream()
         self.side = torch.cuda.Stream()
@@ -247,7 +263,13 @@ class DecodeStep:
             self.compute.wait_event(self.ev_wb)
         for gi, (anchor, followers) in enumerate(self.groups):
             f = self.flags | (H.RECORD_PLAN if followers else 0)
-            if through and self.fused:
+            if self.resident is not None:
+                fused = through and self.fused
+                hs.resolve_resident(anchor, sel[gi], out[gi], self.resident[0], self.resident[1],
+                                    self.num_reqs, newest, pos[anchor] if fused else None,
+                                    new_rows[anchor] if (fused and new_rows is not None) else None,
+                                    f, stream=self.compute)
+            elif through and self.fused:
                 hs.resolve_step(anchor, sel[gi], out[gi], self.num_reqs, newest, pos[anchor],
                                 new_rows[anchor] if new_rows is not None else None, f,
                                 stream=self.compute)

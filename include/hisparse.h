@@ -188,6 +188,30 @@ int hisparse_resolve_step(hisparse_handle *h, int32_t layer, const int32_t *d_se
                           const int32_t *d_prev_pos, const void *d_new_rows, int32_t *d_out,
                           uint32_t flags, void *stream);
 
+/* Three-tier RESOLVE ([VD] "Hot lookup and LRU": resident page -> resident
+ * physical row, else hot row, else a copy from pinned host memory; [DD] §6.5):
+ * hisparse_resolve_step with a resident tier checked first.  d_res_blocks is a
+ * device int32 [R][res_max_blocks] block table shared by the layers: entry b of
+ * request r is -1 when positions [b*res_block_tokens, (b+1)*res_block_tokens)
+ * have no device-resident copy, else the index of their block in the caller's
+ * resident store; positions past the table are not resident.  A selected
+ * position p in a resident block outputs B + 1 + row, row = entry *
+ * res_block_tokens + p % res_block_tokens: it touches neither the LRU, the page
+ * table, the miss count nor the plan, and is not part of the duplicate check
+ * (a repeated resident position outputs its row at each index).  A selected
+ * position whose entry is below -1, or whose B + 1 + row exceeds INT32_MAX,
+ * fails the request with HISPARSE_ERR_RANGE.  A request whose selections are
+ * all resident leaves its cache state unchanged.  d_res_blocks == NULL is
+ * hisparse_resolve_step.  Page-table lookup only (EINVAL with
+ * HISPARSE_LOOKUP_HASH, or with res_max_blocks or res_block_tokens < 1).
+ * Errors: as hisparse_resolve_step. */
+int hisparse_resolve_resident(hisparse_handle *h, int32_t layer, const int32_t *d_sel,
+                              const int32_t *d_num_reqs, const int32_t *d_newest,
+                              const int32_t *d_prev_pos, const void *d_new_rows,
+                              const int32_t *d_res_blocks, int32_t res_max_blocks,
+                              int32_t res_block_tokens, int32_t *d_out, uint32_t flags,
+                              void *stream);
+
 /* Write-through of the newest row ([DD] §3.4 step 4, §5.4 eager backup):
  * for r < *d_num_reqs with d_pos[r] >= 0, copy hot row B of (layer, r) to
  * host row d_pos[r] of (layer, r); then, if d_new_rows is not NULL, place the

@@ -17,7 +17,10 @@ from workload.traces import all_traces
 class Run:
     def __init__(self, w, flags=0, mirror=False, ctas_per_request=0, replay_ctas=0,
                  num_reqs=None, oracle_bytes=True, traces=None, lookup=0, pool_kind=H.HOST_PINNED,
-                 fused=True):
+                 fused=True, resident=None):
+        """``resident`` = (int32 [steps][R][nblk] block tables, tokens per
+        block) runs every anchor through the three-tier resolve, with the
+        table of step t in place before step t."""
         self.w = w
         self.flags = flags
         dev = torch.device("cuda", 0)
@@ -46,8 +49,15 @@ class Run:
         self.out = torch.full((len(self.groups), w.R, w.k), -7, dtype=torch.int32, device=dev)
         self.nreq_val = w.R if num_reqs is None else num_reqs
         self.num_reqs = torch.tensor([self.nreq_val], dtype=torch.int32, device=dev)
+        self.res_np = self.res_dev = None
+        self.res_tok = 1
+        if resident is not None:
+            self.res_np, self.res_tok = resident
+            self.res_dev = torch.from_numpy(np.ascontiguousarray(self.res_np[0])).to(dev)
         self.step_runner = DecodeStep(self.hs, self.mem, self.groups, flags=flags,
-                                      num_reqs=self.num_reqs, fused=fused)
+                                      num_reqs=self.num_reqs, fused=fused,
+                                      resident=None if resident is None else
+                                      (self.res_dev, self.res_tok))
         # oracle
         self.oracle = {}
         for l in range(w.L):
@@ -62,6 +72,8 @@ class Run:
 
     # ------------------------------------------------------------------ #
     def gpu_step(self, t):
+        if self.res_dev is not None:
+            self.res_dev.copy_(torch.from_numpy(np.ascontiguousarray(self.res_np[t])))
         self.step_runner.issue(self.sel[t], self.out,
                                newest=self.newest[t] if self.newest is not None else None,
                                wb_pos=self.wb[t] if (self.w.write_through and t > 0) else None,
@@ -80,7 +92,9 @@ class Run:
                 self.oracle[l].set_newest_rows(self.new_rows_np[t, l], num_reqs=nr)
         for gi, (a, fl) in enumerate(self.groups):
             nw = self.newest_np[t] if self.newest_np is not None else None
-            out, _ = self.oracle[a].resolve(self.sel_np[t, gi], nw, num_reqs=nr, io=io)
+            out, _ = self.oracle[a].resolve(self.sel_np[t, gi], nw, num_reqs=nr, io=io,
+                                            res_blocks=None if self.res_np is None else
+                                            self.res_np[t], res_tok=self.res_tok)
             self.oracle_out[gi, :nr] = out[:nr]
             for f in fl:
                 self.oracle[a].replay_into(self.oracle[f], num_reqs=nr)

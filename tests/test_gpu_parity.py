@@ -272,6 +272,67 @@ def test_duplicate_among_one_slices_misses(cs, m):
     hs.close(); mem.close()
 
 
+# ---------------------------------------------------------------------- #
+# Three-tier resolve: resident block table first                          #
+# ---------------------------------------------------------------------- #
+from workload.resident import resident_tables  # noqa: E402
+
+
+@pytest.mark.parametrize("cs", [0, 1, 3])
+def test_resident_tier_small(cs):
+    """One request wholly resident, the others with a resident recent window,
+    write-through fused; state, slot vectors and bytes equal the oracle's."""
+    w = get("dsa").scaled(R=4, groups=2, L_ctx=16384, steps=8)
+    _run_all(w, ctas_per_request=cs, resident=(resident_tables(w, 64, full=1, window=1024), 64))
+
+
+def test_resident_tier_dsa_full_size():
+    """The DSA-style workload at full size with half the requests resident."""
+    w = get("dsa")
+    _run_all(w, every=4, resident=(resident_tables(w, 64, full=4, window=4096), 64))
+
+
+def test_resident_tier_shared_layers():
+    """Anchors resolved with the resident tier; shared layers replay their plans."""
+    w = get("shared").scaled(R=3, groups=2, L_ctx=8192, steps=6)
+    _run_all(w, resident=(resident_tables(w, 16, full=1, window=512), 16))
+
+
+def test_resident_all_and_errors():
+    """A wholly resident request keeps its state; a bad block entry fails only
+    the request that selects a position in it; repeats of a resident position
+    are not duplicates."""
+    R, k, B, P, tok = 3, 8, 16, 256, 16
+    mem, hs = _instance(R, k, B, P)
+    out = torch.empty((R, k), dtype=torch.int32, device="cuda")
+    warm = np.array([[1, 2, 3, 4, 5, 6, 7, 8]] * R, np.int32)
+    hs.resolve(0, _dev(warm), out)
+    before = hs.export_state(0)
+    blocks = np.full((R, P // tok), -1, np.int32)
+    blocks[0, :] = np.arange(P // tok) + 100          # request 0: everything resident
+    blocks[1, 2] = -5                                  # request 1: a bad entry in block 2
+    blocks[2, 0] = 7                                   # request 2: block 0 resident
+    sel = np.array([[1, 40, 41, 200, 7, -1, 90, 3],
+                    [1, 33, 2, -1, -1, -1, -1, -1],    # 33 is in block 2
+                    [1, 1 + 0, 40, 50, -1, -1, -1, -1]], np.int32)
+    sel[2, 1] = 1                                      # a repeat of a resident position
+    hs.resolve_resident(0, _dev(sel), out, _dev(blocks), tok)
+    o = out.cpu().numpy()
+    assert o[0].tolist() == [B + 1 + 100 * tok + 1, B + 1 + 102 * tok + 8, B + 1 + 102 * tok + 9,
+                             B + 1 + 112 * tok + 8, B + 1 + 100 * tok + 7, -1,
+                             B + 1 + 105 * tok + 10, B + 1 + 100 * tok + 3]
+    assert (o[1] == -1).all()
+    assert o[2, 0] == o[2, 1] == B + 1 + 7 * tok + 1
+    flags, ue = hs.status()
+    assert flags == H.ERR_RANGE and ue[0].tolist() == [0, H.ERR_RANGE, 0]
+    after = hs.export_state(0)
+    for r in (0, 1):
+        for x, y in zip(before[:3], after[:3]):
+            np.testing.assert_array_equal(x[r], y[r])
+    assert after[3][2] == 2                            # request 2 fetched 40 and 50
+    hs.close(); mem.close()
+
+
 def test_import_rejects_inconsistent_state():
     mem, hs = _instance(1, 2, 4, 16)
     sp = np.array([[3, -1, 5, -1]], np.int32)

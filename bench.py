@@ -49,6 +49,10 @@ def parse():
                     help="skip the untimed passes over the trace before warm-up")
     ap.add_argument("--burn-in", type=int, default=3,
                     help="untimed passes over the trace before warm-up (default 3)")
+    ap.add_argument("--resident", default="",
+                    help="FULL,WINDOW,TOKENS: three-tier resolve with the first FULL requests "
+                         "resident over their whole context and the others over their last "
+                         "WINDOW positions, TOKENS positions per resident block")
     ap.add_argument("--mirror", action="store_true",
                     help="fetch missed records from an HBM mirror of the host pool "
                          "(FROM_MIRROR): the same kernels with HBM as the source; the "
@@ -368,7 +372,16 @@ def run_ours(args):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)     # > 129 MB L2
     setup_s = time.perf_counter() - t_setup
 
+    res_all = None
+    if args.resident:
+        from workload.resident import resident_tables
+        full, window, tok = (int(x) for x in args.resident.split(","))
+        res_all = torch.from_numpy(resident_tables(w, tok, full=full, window=window)).to(dev)
+        res_tok = tok
+
     def issue(t):
+        if res_all is not None:          # step t's resident block table, by pointer
+            runner.resident = (res_all[t], res_tok)
         runner.issue(sel[t], out, newest=newest[t] if newest is not None else None,
                      wb_pos=wb[t] if (wb is not None and t > 0) else None,
                      new_rows=new_rows[t] if new_rows is not None else None)
@@ -392,6 +405,7 @@ def run_ours(args):
         RESOLVE and write-back launch and a copy of the miss counts."""
         evs, wev, rpev = [], [], []
         orig_resolve, orig_step = hs.resolve, hs.resolve_step
+        orig_res = hs.resolve_resident
         orig_wb, orig_rp = hs.writeback, hs.prefetch_plan
 
         def timed_resolve(layer, *a, **kw):
@@ -407,6 +421,14 @@ def run_ours(args):
             e0, e1 = timing_event()[0], timing_event()[0]
             e0.record(st)
             orig_step(layer, *a, **kw)
+            e1.record(st)
+            evs.append((e0, e1))
+
+        def timed_res(layer, *a, **kw):
+            st = kw.get("stream")
+            e0, e1 = timing_event()[0], timing_event()[0]
+            e0.record(st)
+            orig_res(layer, *a, **kw)
             e1.record(st)
             evs.append((e0, e1))
 
@@ -428,6 +450,7 @@ def run_ours(args):
 
         if instrument:
             hs.resolve, hs.resolve_step = timed_resolve, timed_step
+            hs.resolve_resident = timed_res
             hs.writeback, hs.prefetch_plan = timed_wb, timed_rp
         g = torch.cuda.CUDAGraph()
         try:
@@ -440,6 +463,7 @@ def run_ours(args):
                                                 stream=torch.cuda.current_stream())
         finally:
             hs.resolve, hs.resolve_step = orig_resolve, orig_step
+            hs.resolve_resident = orig_res
             hs.writeback, hs.prefetch_plan = orig_wb, orig_rp
         return g, evs, wev, rpev
 
@@ -501,7 +525,7 @@ def run_ours(args):
     flags, _ = hs.status()
 
     verify = None
-    if args.verify:
+    if args.verify and not args.resident:
         verify = verify_against_oracle(w, hs, mem, groups, traces, args.warmup + args.steps)
 
     # ---- pass 2 (per-kernel durations for the roofline): the same steps from
@@ -644,6 +668,8 @@ def run_ours(args):
                         d_newest.copy_(h_newest[t], non_blocking=True)
                         d_wb.copy_(h_wb[t], non_blocking=True)
                         d_new.copy_(h_new[t], non_blocking=True)
+                    if res_all is not None:
+                        runner.resident = (res_all[t], res_tok)
                     runner.issue(d_sel, out, newest=d_newest if w.write_through else None,
                                  wb_pos=d_wb if (w.write_through and t > 0) else None,
                                  new_rows=d_new if w.write_through else None)
@@ -725,7 +751,7 @@ def run_ours(args):
         allhit["hbm_peak_source"] = f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
 
     cpu = cpu_mt = None
-    if rank == 0 and not args.no_cpu:
+    if rank == 0 and not args.no_cpu and not args.resident:
         views = {l: mem.host_view(l) for l in range(w.L)}
         cpu = cpu_oracle_rate(w, traces, host_views=views, budget_s=20.0)
         cpu.pop("seconds", None)
@@ -753,6 +779,9 @@ def run_ours(args):
                        "write_through_launch": "separate" if args.unfused else "fused into RESOLVE",
                        "host_pool": args.pool,
                        "fetch_source": "HBM mirror of the host pool" if args.mirror else "host pool",
+                       "resident_tier": (dict(zip(("full_requests", "window", "tokens_per_block"),
+                                                  (int(x) for x in args.resident.split(","))))
+                                         if args.resident else None),
                        "host_pool_hugepage_fraction": round(hp_frac, 3),
                        "host_pool_hugepage_fraction_end": round(hp_frac_end, 3),
                        "host_thp_splits_during_burn_in": splits_burn,

@@ -629,7 +629,7 @@ __host__ __device__ inline PtLayout pt_layout(int k, int B, int ks, int hcap, in
 
 // worker misc words / leader misc words
 enum { kWErr = 0, kWNewest = 1, kWCount = 2, kWLeadErr = 3 };
-enum { kLErr = 0, kLM = 1, kLHits = 2, kLPrefix = 8 };
+enum { kLErr = 0, kLM = 1, kLHits = 2, kLAnyHit = 3, kLSame = 4, kLPrefix = 8 };
 
 struct PtArgs {
   int32_t R, k, B, rec16, io, ks, hcap_log2;
@@ -950,6 +950,8 @@ __device__ void pt_leader_decide(const PtArgs &a, int cs, int nw, int32_t newest
       l_misc[kLErr] = err;
       l_misc[kLM] = static_cast<uint32_t>(inc);
       l_misc[kLHits] = 0;
+      l_misc[kLAnyHit] = 0;
+      l_misc[kLSame] = 0;
     }
   }
   for (int x = tid; x < nwords; x += kThreads) l_hit[x] = 0;
@@ -958,12 +960,14 @@ __device__ void pt_leader_decide(const PtArgs &a, int cs, int nw, int32_t newest
   //     and the miss positions in list order, with duplicates among misses
   //     caught by an open-addressing set ([DD] §3.5 stage 1's hash).
   {
-    uint32_t dup = 0;
+    uint32_t dup = 0, any = 0;
     for (int idx = tid; idx < nw * nwords; idx += kThreads) {
       const int w = idx / nwords, x = idx - w * nwords;
       const uint32_t b = ld_dsmem_u32(dsmem_addr(&w_hit0[x], wrank(w)));
       if (b) dup |= atomicOr(&l_hit[x], b) & b;
+      any |= b;
     }
+    if (any) l_misc[kLAnyHit] = 1;
     const int M = static_cast<int>(l_misc[kLM]);
     for (int g = tid; g < M; g += kThreads) {
       int w = 0;
@@ -986,6 +990,13 @@ __device__ void pt_leader_decide(const PtArgs &a, int cs, int nw, int32_t newest
   }
   __syncthreads();
   if (l_misc[kLErr]) return;  // uniform
+  // No miss and no hot hit (every selection resident, newest or padding): the
+  // LRU order stays as it is ([DD] §6.5: resident hits exit before the LRU).
+  if (l_misc[kLM] == 0 && l_misc[kLAnyHit] == 0) {
+    __syncthreads();
+    if (tid == 0) l_misc[kLSame] = 1;
+    return;
+  }
   // (3) one block-wide pass compacts the hits (slot order) and the evictables
   //     (LRU order) together.  Thread t owns slots and LRU positions
   //     [t*per, t*per + per); one exclusive scan of the packed per-thread
@@ -1115,7 +1126,8 @@ __device__ void pt_leader_publish(const PtArgs &a, int r, int32_t prev, int32_t 
     }
   }
   int16_t *g_lru = a.lru + static_cast<int64_t>(r) * B;
-  for (int s = tid; s < B; s += kThreads) g_lru[s] = l_newlru[s];
+  if (!l_misc[kLSame])
+    for (int s = tid; s < B; s += kThreads) g_lru[s] = l_newlru[s];
   if (tid == 0) {
     a.miss_count[r] = M;
     a.unit_err[r] = 0;

@@ -648,6 +648,9 @@ struct PtArgs {
   // positions per block; NULL = no resident tier.
   const int32_t *res_blocks;
   int32_t res_nblk, res_tok;
+  // Block-id selections: sel holds k / sel_bt block ids per request, each
+  // standing for sel_bt consecutive positions (1 = sel holds positions).
+  int32_t sel_bt;
   int64_t P;
   const int32_t *sel, *num_reqs, *newest;
   int32_t *out;
@@ -749,7 +752,22 @@ __device__ __forceinline__ bool bit_of(const uint32_t *bits, int s) {
 }
 
 // Worker: classify selections [i0, i0 + n) of request r.
-template <bool kResident>
+// Position of selection index t (0 <= t < k) of request r: the list entry
+// itself, or, for block-id selections, entry t / sel_bt expanded in registers
+// (gentlecold.top §5.5: block ids are expanded into token positions without a
+// token list in memory).  -1 blocks give padding; other negative ids give
+// negative positions, which classification rejects as out of range.
+template <bool kExt>
+__device__ __forceinline__ int32_t sel_position(const PtArgs &a, int r, int t) {
+  if (!kExt || a.sel_bt == 1) return a.sel[static_cast<int64_t>(r) * a.k + t];
+  const int kb = a.k / a.sel_bt;
+  const int32_t b = a.sel[static_cast<int64_t>(r) * kb + t / a.sel_bt];
+  if (b == -1) return -1;
+  const int64_t q = static_cast<int64_t>(b) * a.sel_bt + t % a.sel_bt;
+  return q > INT32_MAX ? INT32_MAX : (q < INT32_MIN ? INT32_MIN : static_cast<int32_t>(q));
+}
+
+template <bool kExt>
 __device__ int pt_worker_classify(const PtArgs &a, int r, int i0, int n, int32_t newest,
                                   const int32_t (&first)[kGroup], unsigned char *smem,
                                   const PtLayout &L) {
@@ -767,15 +785,14 @@ __device__ int pt_worker_classify(const PtArgs &a, int r, int i0, int n, int32_t
   for (int x = tid; x < nwords; x += kThreads) w_hit[x] = 0;
   if (tid < 8) w_misc[tid] = 0;
   __syncthreads();
-  const int32_t *g_sel = a.sel + static_cast<int64_t>(r) * a.k + i0;
   const int32_t *g_pt = a.page_table + static_cast<int64_t>(r) * P;
-  const int32_t *g_res = kResident ? a.res_blocks + static_cast<int64_t>(r) * a.res_nblk : nullptr;
+  const int32_t *g_res = (kExt && a.res_blocks) ? a.res_blocks + static_cast<int64_t>(r) * a.res_nblk : nullptr;
   for (int base = 0; base < n; base += kGroup * kThreads) {
     int32_t p[kGroup], s[kGroup];
 #pragma unroll
     for (int u = 0; u < kGroup; ++u) {
       const int t = base + u * kThreads + tid;
-      p[u] = base == 0 ? first[u] : (t < n ? g_sel[t] : -1);
+      p[u] = base == 0 ? first[u] : (t < n ? sel_position<kExt>(a, r, i0 + t) : -1);
     }
     int32_t e[kGroup];  // resident block entry of each selection (-1: none)
 #pragma unroll
@@ -783,7 +800,7 @@ __device__ int pt_worker_classify(const PtArgs &a, int r, int i0, int n, int32_t
       s[u] = -1;
       e[u] = -1;
       if (p[u] >= 0 && p[u] < P) {
-        if (kResident && p[u] / a.res_tok < a.res_nblk) e[u] = g_res[p[u] / a.res_tok];
+        if (kExt && g_res && p[u] / a.res_tok < a.res_nblk) e[u] = g_res[p[u] / a.res_tok];
         if (p[u] != newest) s[u] = g_pt[p[u]];
       }
     }
@@ -797,7 +814,7 @@ __device__ int pt_worker_classify(const PtArgs &a, int r, int i0, int n, int32_t
       } else if (p[u] < -1 || p[u] >= P) {
         atomicOr(&w_misc[kWErr], HISPARSE_ERR_RANGE);
         v = -1;
-      } else if (kResident && e[u] != -1) {
+      } else if (kExt && e[u] != -1) {
         // resident copy: B + 1 + row, no hit, no miss, no duplicate check
         // (vLLM docs "Hot lookup and LRU"; gentlecold.top §6.5)
         const int64_t row = static_cast<int64_t>(e[u]) * a.res_tok + p[u] % a.res_tok;
@@ -1249,7 +1266,7 @@ __device__ void pt_leader_write_through(const PtArgs &a, int r, int32_t prev, un
   }
 }
 
-template <bool kRecordPlan, bool kResident>
+template <bool kRecordPlan, bool kExt>
 __global__ void __launch_bounds__(kThreads, 1) resolve_pt_kernel(const PtArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   // Programmatic dependent launch: this grid may be set up while the previous
@@ -1280,7 +1297,7 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_pt_kernel(const PtArgs a)
 #pragma unroll
     for (int u = 0; u < kGroup; ++u) {
       const int t = u * kThreads + tid;
-      first[u] = t < n ? a.sel[static_cast<int64_t>(r) * a.k + i0 + t] : -1;
+      first[u] = t < n ? sel_position<kExt>(a, r, i0 + t) : -1;
     }
   } else if (sp_ahead) {
     const int4 v = reinterpret_cast<const int4 *>(a.slot_pos + static_cast<int64_t>(r) * a.B)[tid];
@@ -1300,7 +1317,7 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_pt_kernel(const PtArgs a)
     // one CTA plays every role in order; nothing to overlap, nothing staged
     pt_leader_load_state(a, r, false, make_int4(0, 0, 0, 0), smem, L);
     pt_leader_write_through(a, r, prev, smem, L);
-    const int mw = pt_worker_classify<kResident>(a, r, i0, n, newest, first, smem, L);
+    const int mw = pt_worker_classify<kExt>(a, r, i0, n, newest, first, smem, L);
     pt_worker_order(a, 0, mw, smem, L);
     pt_leader_decide(a, cs, nw, newest, smem, L);
     __syncthreads();
@@ -1329,7 +1346,7 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_pt_kernel(const PtArgs a)
     return;
   }
   // worker
-  const int mw = pt_worker_classify<kResident>(a, r, i0, n, newest, first, smem, L);
+  const int mw = pt_worker_classify<kExt>(a, r, i0, n, newest, first, smem, L);
   // #0: the slice, for the leader.  The block barrier that ends the
   // classification orders every thread's shared-memory writes before the last
   // warp's cluster-scope fence, which releases them all; the other warps
@@ -1919,8 +1936,10 @@ int hisparse_resolve_step(hisparse_handle *h, int32_t layer, const int32_t *d_se
                           const int32_t *d_num_reqs, const int32_t *d_newest,
                           const int32_t *d_prev_pos, const void *d_new_rows, int32_t *d_out,
                           uint32_t flags, void *stream) {
-  return hisparse_resolve_resident(h, layer, d_sel, d_num_reqs, d_newest, d_prev_pos, d_new_rows,
-                                   nullptr, 0, 0, d_out, flags, stream);
+  hisparse_resolve_options o = {};
+  o.d_prev_pos = d_prev_pos;
+  o.d_new_rows = d_new_rows;
+  return hisparse_resolve_ex(h, layer, d_sel, d_num_reqs, d_newest, &o, d_out, flags, stream);
 }
 
 int hisparse_resolve_resident(hisparse_handle *h, int32_t layer, const int32_t *d_sel,
@@ -1929,9 +1948,31 @@ int hisparse_resolve_resident(hisparse_handle *h, int32_t layer, const int32_t *
                               const int32_t *d_res_blocks, int32_t res_max_blocks,
                               int32_t res_block_tokens, int32_t *d_out, uint32_t flags,
                               void *stream) {
+  hisparse_resolve_options o = {};
+  o.d_prev_pos = d_prev_pos;
+  o.d_new_rows = d_new_rows;
+  o.d_res_blocks = d_res_blocks;
+  o.res_max_blocks = res_max_blocks;
+  o.res_block_tokens = res_block_tokens;
+  return hisparse_resolve_ex(h, layer, d_sel, d_num_reqs, d_newest, &o, d_out, flags, stream);
+}
+
+int hisparse_resolve_ex(hisparse_handle *h, int32_t layer, const int32_t *d_sel,
+                        const int32_t *d_num_reqs, const int32_t *d_newest,
+                        const hisparse_resolve_options *opt, int32_t *d_out, uint32_t flags,
+                        void *stream) {
+  static const hisparse_resolve_options kNone = {};
+  if (!opt) opt = &kNone;
+  const int32_t *d_prev_pos = opt->d_prev_pos;
+  const void *d_new_rows = opt->d_new_rows;
+  const int32_t *d_res_blocks = opt->d_res_blocks;
+  const int32_t res_max_blocks = opt->res_max_blocks, res_block_tokens = opt->res_block_tokens;
+  const int32_t sel_bt = opt->sel_block_tokens < 1 ? 1 : opt->sel_block_tokens;
   if (layer_ok(h, layer)) return HISPARSE_EINVAL;
   if (d_res_blocks && (res_max_blocks < 1 || res_block_tokens < 1 ||
                        h->lookup == HISPARSE_LOOKUP_HASH))
+    return HISPARSE_EINVAL;
+  if (sel_bt > 1 && (h->k % sel_bt != 0 || h->lookup == HISPARSE_LOOKUP_HASH))
     return HISPARSE_EINVAL;
   if (d_new_rows && !aligned16(d_new_rows)) return HISPARSE_EINVAL;
   if (!d_sel || !d_out) return HISPARSE_EINVAL;
@@ -1995,6 +2036,7 @@ int hisparse_resolve_resident(hisparse_handle *h, int32_t layer, const int32_t *
     a.res_blocks = d_res_blocks;
     a.res_nblk = d_res_blocks ? res_max_blocks : 0;
     a.res_tok = d_res_blocks ? res_block_tokens : 1;
+    a.sel_bt = sel_bt;
     a.P = h->P;
     a.sel = d_sel; a.num_reqs = d_num_reqs; a.newest = d_newest; a.out = d_out;
     a.slot_pos = m.slot_pos; a.lru = m.lru; a.page_table = m.page_table;
@@ -2004,7 +2046,7 @@ int hisparse_resolve_resident(hisparse_handle *h, int32_t layer, const int32_t *
     a.src_req_stride = Ld.host_req_stride; a.src_row_stride = Ld.host_row_stride;
     a.hot = Ld.hot; a.hot_req_stride = Ld.hot_req_stride; a.hot_row_stride = Ld.hot_row_stride;
     lc.numAttrs = 2;  // cluster shape + programmatic dependent launch
-    if (d_res_blocks)
+    if (d_res_blocks || sel_bt > 1)  // the extended instantiation
       e = plan ? cudaLaunchKernelEx(&lc, resolve_pt_kernel<true, true>, a)
                : cudaLaunchKernelEx(&lc, resolve_pt_kernel<false, true>, a);
     else

@@ -47,6 +47,7 @@ SIGNATURES = [
     ("hisparse_resolve_step", _i32, [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _u32, _vp]),
     ("hisparse_resolve_resident", _i32, [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _vp,
                                          _u32, _vp]),
+    ("hisparse_resolve_ex", _i32, [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _u32, _vp]),
     ("hisparse_writeback", _i32, [_vp, _i32, _vp, _vp, _vp, _vp]),
     ("hisparse_prefetch_plan", _i32, [_vp, _i32, _i32, _vp, _vp]),
     ("hisparse_copy_miss_counts", _i32, [_vp, _i32, _vp, _vp]),
@@ -121,6 +122,19 @@ def hisparse_resolve_step(h, layer, d_sel, d_num_reqs, d_newest, d_prev_pos, d_n
                           flags, stream):
     return load().hisparse_resolve_step(h, layer, d_sel, d_num_reqs, d_newest, d_prev_pos,
                                         d_new_rows, d_out, flags, stream)
+
+
+class ResolveOptions(ctypes.Structure):
+    """hisparse_resolve_options."""
+    _fields_ = [("d_prev_pos", ctypes.c_void_p), ("d_new_rows", ctypes.c_void_p),
+                ("d_res_blocks", ctypes.c_void_p), ("res_max_blocks", ctypes.c_int32),
+                ("res_block_tokens", ctypes.c_int32), ("sel_block_tokens", ctypes.c_int32)]
+
+
+def hisparse_resolve_ex(h, layer, d_sel, d_num_reqs, d_newest, opt, d_out, flags, stream):
+    return load().hisparse_resolve_ex(h, layer, d_sel, d_num_reqs, d_newest,
+                                      ctypes.addressof(opt) if opt is not None else None, d_out,
+                                      flags, stream)
 
 
 def hisparse_resolve_resident(h, layer, d_sel, d_num_reqs, d_newest, d_prev_pos, d_new_rows,

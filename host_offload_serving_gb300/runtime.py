@@ -107,6 +107,17 @@ class HiSparse:
                                             int(res_block_tokens), _ptr(out), flags,
                                             _stream(stream)), "hisparse_resolve_resident")
 
+    def resolve_ex(self, layer, sel, out, num_reqs=None, newest=None, prev_pos=None,
+                   new_rows=None, res_blocks=None, res_block_tokens=0, sel_block_tokens=1,
+                   flags=0, stream=None):
+        """The general RESOLVE (``hisparse_resolve_ex``): fused write-through,
+        resident tier and block-id selections, each optional."""
+        o = H.ResolveOptions(_ptr(prev_pos), _ptr(new_rows), _ptr(res_blocks),
+                             int(res_blocks.shape[1]) if res_blocks is not None else 0,
+                             int(res_block_tokens), int(sel_block_tokens))
+        H.check(H.hisparse_resolve_ex(self.h, layer, _ptr(sel), _ptr(num_reqs), _ptr(newest), o,
+                                      _ptr(out), flags, _stream(stream)), "hisparse_resolve_ex")
+
     def writeback(self, layer, pos, num_reqs=None, stream=None, new_rows=None):
         H.check(H.hisparse_writeback(self.h, layer, _ptr(pos), _ptr(new_rows), _ptr(num_reqs),
                                      _stream(stream)), "hisparse_writeback")
@@ -217,7 +228,8 @@ class DecodeStep:
 
     ``resident`` (optional) = (device int32 [R][max_blocks] resident block
     table, tokens per block) resolves every anchor with the resident tier
-    first (``hisparse_resolve_resident``).
+    first; ``sel_block_tokens`` > 1 means ``sel`` holds block ids of that many
+    positions each (both through ``hisparse_resolve_ex``).
 
     ``fused=True`` (default) writes each anchor's previous token through, and
     installs its new token, inside that anchor's RESOLVE launch
@@ -227,12 +239,14 @@ class DecodeStep:
     pages describe (gentlecold.top "HiSparse 深度解析" §5.4).
     """
 
-    def __init__(self, hs, mem, groups, flags=0, num_reqs=None, fused=True, resident=None):
+    def __init__(self, hs, mem, groups, flags=0, num_reqs=None, fused=True, resident=None,
+                 sel_block_tokens=1):
         self.hs, self.mem, self.groups = hs, mem, groups
         self.flags = flags
         self.num_reqs = num_reqs
         self.fused = fused
         self.resident = resident    # (device int32 [R][max_blocks], tokens per block) or None
+        self.sel_block_tokens = sel_block_tokens
         self.compute = torch.cuda.Stream()
         self.backup = torch.cuda.Stream()
         self.side = torch.cuda.Stream()
@@ -263,12 +277,15 @@ class DecodeStep:
             self.compute.wait_event(self.ev_wb)
         for gi, (anchor, followers) in enumerate(self.groups):
             f = self.flags | (H.RECORD_PLAN if followers else 0)
-            if self.resident is not None:
+            if self.resident is not None or self.sel_block_tokens > 1:
                 fused = through and self.fused
-                hs.resolve_resident(anchor, sel[gi], out[gi], self.resident[0], self.resident[1],
-                                    self.num_reqs, newest, pos[anchor] if fused else None,
-                                    new_rows[anchor] if (fused and new_rows is not None) else None,
-                                    f, stream=self.compute)
+                res = self.resident
+                hs.resolve_ex(anchor, sel[gi], out[gi], self.num_reqs, newest,
+                              pos[anchor] if fused else None,
+                              new_rows[anchor] if (fused and new_rows is not None) else None,
+                              res[0] if res is not None else None,
+                              res[1] if res is not None else 0, self.sel_block_tokens, f,
+                              stream=self.compute)
             elif through and self.fused:
                 hs.resolve_step(anchor, sel[gi], out[gi], self.num_reqs, newest, pos[anchor],
                                 new_rows[anchor] if new_rows is not None else None, f,

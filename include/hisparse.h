@@ -188,6 +188,37 @@ int hisparse_resolve_step(hisparse_handle *h, int32_t layer, const int32_t *d_se
                           const int32_t *d_prev_pos, const void *d_new_rows, int32_t *d_out,
                           uint32_t flags, void *stream);
 
+/* Options of hisparse_resolve_ex; zero-initialise and set what is used. */
+typedef struct {
+  /* fused write-through, as hisparse_resolve_step (both NULL: none) */
+  const int32_t *d_prev_pos;  /* device [R] */
+  const void *d_new_rows;     /* device [R][record_bytes], 16-byte aligned */
+  /* resident tier, as hisparse_resolve_resident (NULL: none) */
+  const int32_t *d_res_blocks; /* device [R][res_max_blocks] */
+  int32_t res_max_blocks;
+  int32_t res_block_tokens;
+  /* Block-id selections ([DD] §5.5, TopKIsBlocks): when > 1, d_sel holds
+   * top_k / sel_block_tokens block ids per request ([R][top_k /
+   * sel_block_tokens]); block b stands for positions b*sel_block_tokens ..
+   * b*sel_block_tokens + sel_block_tokens - 1 in that order, -1 for as many
+   * paddings, and d_out stays [R][top_k], one entry per position.  The kernel
+   * expands the ids in registers; no position list is written.  Other negative
+   * ids, and ids whose positions reach P, fail the request with
+   * HISPARSE_ERR_RANGE.  top_k must be a multiple; page-table lookup only.
+   * 0 or 1: d_sel holds positions. */
+  int32_t sel_block_tokens;
+} hisparse_resolve_options;
+
+/* The general RESOLVE: hisparse_resolve with the options above (opt may be
+ * NULL = hisparse_resolve).  hisparse_resolve_step and
+ * hisparse_resolve_resident are this call with the corresponding options.
+ * Errors: as hisparse_resolve_step; EINVAL for options the lookup does not
+ * support or a top_k that is not a multiple of sel_block_tokens. */
+int hisparse_resolve_ex(hisparse_handle *h, int32_t layer, const int32_t *d_sel,
+                        const int32_t *d_num_reqs, const int32_t *d_newest,
+                        const hisparse_resolve_options *opt, int32_t *d_out, uint32_t flags,
+                        void *stream);
+
 /* Three-tier RESOLVE ([VD] "Hot lookup and LRU": resident page -> resident
  * physical row, else hot row, else a copy from pinned host memory; [DD] §6.5):
  * hisparse_resolve_step with a resident tier checked first.  d_res_blocks is a

@@ -180,6 +180,22 @@ class Unit:
         return {p for p in self.slot_pos if p >= 0}
 
 
+def expand_blocks(sel_blocks, block_tokens):
+    """Token positions of a block-id selection list (gentlecold.top §5.5: a
+    selector that picks blocks; the kernel expands each block id into its
+    positions).  Block b stands for positions b*block_tokens .. b*block_tokens
+    + block_tokens - 1, in that order; -1 stands for block_tokens paddings.
+    Any other negative id gives negative positions, which the resolve rejects
+    as out of range."""
+    out = []
+    for b in sel_blocks:
+        if b == -1:
+            out.extend([-1] * block_tokens)
+        else:
+            out.extend(b * block_tokens + j for j in range(block_tokens))
+    return out
+
+
 def replay(plan, follower_hot, follower_host):
     """Copy-only replay of an anchor's miss plan into a shared layer.
 

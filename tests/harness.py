@@ -35,8 +35,17 @@ class Run:
         self.groups = [(a, [l for l in range(w.L) if anchor_of[l] == a]) for a in w.anchors()]
         tr = traces if traces is not None else all_traces(w)
         self.sel_np = np.stack([tr[a][0] for a, _ in self.groups], axis=1)  # [T][G][R][k]
+        self.sel_gpu_np = self.sel_np
+        bt = w.sel_block_tokens
+        if bt > 1:   # the GPU reads block ids; the oracle gets the positions
+            from oracle.tiny import expand_blocks
+            blk = self.sel_np
+            pos = (blk[..., None].astype(np.int64) * bt + np.arange(bt)).reshape(*blk.shape[:-1], -1)
+            pos = np.where(np.repeat(blk == -1, bt, axis=-1), -1, pos).astype(np.int32)
+            assert pos[0, 0, 0].tolist() == expand_blocks(blk[0, 0, 0].tolist(), bt)
+            self.sel_np = pos
         self.newest_np = tr[self.groups[0][0]][1] if w.write_through else None  # [T][R]
-        self.sel = torch.from_numpy(self.sel_np).to(dev)
+        self.sel = torch.from_numpy(self.sel_gpu_np).to(dev)
         self.newest = torch.from_numpy(self.newest_np).to(dev) if w.write_through else None
         self.new_rows_np = REC.new_token_records(w)                       # [T][L][R][rec]
         self.new_rows = torch.from_numpy(self.new_rows_np).to(dev) if w.write_through else None
@@ -57,7 +66,7 @@ class Run:
         self.step_runner = DecodeStep(self.hs, self.mem, self.groups, flags=flags,
                                       num_reqs=self.num_reqs, fused=fused,
                                       resident=None if resident is None else
-                                      (self.res_dev, self.res_tok))
+                                      (self.res_dev, self.res_tok), sel_block_tokens=bt)
         # oracle
         self.oracle = {}
         for l in range(w.L):

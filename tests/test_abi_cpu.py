@@ -96,3 +96,40 @@ def test_hugepage_query_on_ordinary_memory():
     a = np.zeros(1 << 20, np.uint8)
     rc, huge = H.hisparse_host_hugepage_bytes(a.ctypes.data, a.nbytes)
     assert rc == H.OK and 0 <= huge <= a.nbytes
+
+
+def test_struct_layouts_match_the_header(tmp_path):
+    """The ctypes mirrors of the header's structs have the C sizes and offsets
+    (compiled with the host C compiler against include/hisparse.h)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    prog = tmp_path / "layout.c"
+    prog.write_text(
+        '#include <stdio.h>\n#include <stddef.h>\n#include "hisparse.h"\n'
+        "int main(void) {\n"
+        '  printf("%zu %zu %zu %zu\\n", sizeof(hisparse_resolve_options),'
+        " offsetof(hisparse_resolve_options, d_res_blocks),"
+        " offsetof(hisparse_resolve_options, res_max_blocks),"
+        " offsetof(hisparse_resolve_options, sel_block_tokens));\n"
+        '  printf("%zu %zu %zu\\n", sizeof(hisparse_config), sizeof(hisparse_layer_buffers),'
+        " sizeof(hisparse_info));\n"
+        "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.check_call([cc, "-I", os.path.join(ROOT, "include"), str(prog), "-o", str(exe)])
+    got = subprocess.check_output([str(exe)], text=True).split("\n")
+    o = H.ResolveOptions
+    assert [int(x) for x in got[0].split()] == [ctypes.sizeof(o), o.d_res_blocks.offset,
+                                                o.res_max_blocks.offset,
+                                                o.sel_block_tokens.offset]
+    assert [int(x) for x in got[1].split()] == [ctypes.sizeof(H.Config),
+                                                ctypes.sizeof(H.LayerBuffers),
+                                                ctypes.sizeof(H.Info)]
+
+
+def test_resolve_ex_without_a_handle_is_rejected():
+    o = H.ResolveOptions(None, None, 0x1000, 4, 64, 1)
+    assert H.hisparse_resolve_ex(None, 0, 0x10, None, None, o, 0x20, 0, None) == H.EINVAL
+    assert H.hisparse_resolve_ex(None, 0, 0x10, None, None, None, 0x20, 0, None) == H.EINVAL

@@ -333,6 +333,44 @@ def test_resident_all_and_errors():
     hs.close(); mem.close()
 
 
+# ---------------------------------------------------------------------- #
+# Block-id selections expanded in the kernel                               #
+# ---------------------------------------------------------------------- #
+@pytest.mark.parametrize("cs", [0, 1, 5])
+def test_block_selections_small(cs):
+    """Top-k blocks of 4 positions, read as block ids by the kernel; the
+    oracle resolves the expanded positions."""
+    _run_all(get("blocks").scaled(R=3, groups=2, L_ctx=16384, steps=8), ctas_per_request=cs)
+
+
+def test_block_selections_full_size():
+    """8 requests x 4 layers, 128K context, top-512 blocks of 4 positions."""
+    _run_all(get("blocks"), every=4)
+
+
+def test_block_selections_with_resident_tier():
+    w = get("blocks").scaled(R=3, groups=2, L_ctx=8192, steps=6)
+    _run_all(w, resident=(resident_tables(w, 16, full=1, window=256), 16))
+
+
+def test_block_selection_errors():
+    """A negative block id other than -1 and a block past P fail the request;
+    -1 blocks are padding."""
+    R, k, B, P, bt = 3, 8, 16, 64, 4
+    mem, hs = _instance(R, k, B, P)
+    out = torch.empty((R, k), dtype=torch.int32, device="cuda")
+    blocks = np.array([[2, -1], [3, -2], [15, 16]], np.int32)   # 16 * 4 = 64 = P
+    hs.resolve_ex(0, _dev(blocks), out, sel_block_tokens=bt)
+    o = out.cpu().numpy()
+    sp = hs.export_state(0)[0]
+    assert o[0, :4].tolist() == sorted(o[0, :4].tolist()) and (o[0, 4:] == -1).all()
+    assert [int(sp[0, s]) for s in o[0, :4]] == [8, 9, 10, 11]
+    assert (o[1] == -1).all() and (o[2] == -1).all()
+    flags, ue = hs.status()
+    assert flags == H.ERR_RANGE and ue[0].tolist() == [0, H.ERR_RANGE, H.ERR_RANGE]
+    hs.close(); mem.close()
+
+
 def test_import_rejects_inconsistent_state():
     mem, hs = _instance(1, 2, 4, 16)
     sp = np.array([[3, -1, 5, -1]], np.int32)

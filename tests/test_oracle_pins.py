@@ -304,3 +304,26 @@ def test_unmutated_copy_passes_every_pin():
     cls = type("M_none", (_Mutant,), {"mutation": None})
     for pin in ALL_PINS:
         pin(cls)
+
+
+# ---------------------------------------------------------------------- #
+# Block-id selections                                                      #
+# ---------------------------------------------------------------------- #
+def test_expand_blocks_written_out():
+    from oracle.tiny import expand_blocks
+    assert expand_blocks([3, -1, 0], 4) == [12, 13, 14, 15, -1, -1, -1, -1, 0, 1, 2, 3]
+    assert expand_blocks([5, 2], 1) == [5, 2]
+    assert expand_blocks([], 4) == []
+    bad = expand_blocks([-2], 2)
+    assert all(p < -1 for p in bad)
+
+
+def test_block_selection_resolves_like_its_positions():
+    """A block-id list resolves exactly as its expanded position list does,
+    including the error for a negative block id other than -1."""
+    from oracle.tiny import expand_blocks
+    u = Unit(16, 64, k=8)
+    out, plan, err = u.resolve(expand_blocks([2, 7], 4))
+    assert err == 0 and u.miss_count == 8 and sorted(p for p, _ in plan) == list(range(8, 12)) + list(range(28, 32))
+    out, plan, err = u.resolve(expand_blocks([7, -3], 4))
+    assert err == ERR_RANGE and out == [-1] * 8

@@ -31,6 +31,7 @@ class Workload:
     step0: str = "zipf"  # "zipf" (sink + local + Zipf) or "uniform"
     all_hit: bool = False  # every step repeats step 0's selection list
     seed: int = 0
+    sel_block_tokens: int = 1  # > 1: the selector picks blocks of this many positions
 
     @property
     def L(self):
@@ -77,6 +78,11 @@ WORKLOADS = {
     "quest": Workload("quest", R=16, groups=8, followers=0, L_ctx=12800, k=128, B=256,
                       rec=32768, steps=32, write_through=False, f=0.80, W_hist=1, n_sink=0,
                       W_loc=0, zipf_s=1.0, seed=303),
+    # Block selections: 8 requests x 4 layers, 128K context, top-512 blocks of 4
+    # positions (2048 positions), B=4096 (an NSA-style selector).
+    "blocks": Workload("blocks", R=8, groups=4, followers=0, L_ctx=131072, k=2048, B=4096,
+                       rec=1152, steps=32, write_through=False, f=0.87, W_hist=4, n_sink=4,
+                       W_loc=128, zipf_s=1.1, seed=606, sel_block_tokens=4),
     # Shared-index groups: 32 requests x 4 groups of (1 anchor + 3 shared layers).
     "shared": Workload("shared", R=32, groups=4, followers=3, L_ctx=131072, k=2048, B=4096,
                        rec=1152, steps=32, write_through=False, f=0.87, W_hist=4, n_sink=4,

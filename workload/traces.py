@@ -136,5 +136,19 @@ def layer_traces(w, layer):
 
 
 def all_traces(w):
-    """{anchor layer: (sel [steps][R][k], newest [steps][R])}."""
+    """{anchor layer: (sel [steps][R][k], newest [steps][R])}.
+
+    For a block-selecting workload (``sel_block_tokens`` = t > 1) the lists
+    hold block ids ([steps][R][k / t]): the same recipe run over the context
+    in blocks of t positions, with k, the sink and the local window counted
+    in blocks."""
+    t = w.sel_block_tokens
+    if t > 1 and w.write_through:
+        raise ValueError("block-selecting workloads here have no write-through (the newest "
+                         "token is one position, not a block)")
+    if t > 1:
+        wb = w.scaled(L_ctx=w.L_ctx // t, k=w.k // t, B=max(w.B // t, w.k // t),
+                      n_sink=max(1, w.n_sink // t), W_loc=max(1, w.W_loc // t),
+                      sel_block_tokens=1)
+        return {l: layer_traces(wb, l) for l in w.anchors()}
     return {l: layer_traces(w, l) for l in w.anchors()}

@@ -162,6 +162,20 @@ def profile_traffic(kernel_file, kernel):
 
 
 # --------------------------------------------------------------------------- #
+def token_traces(w, traces):
+    """The traces as positions: block ids expanded for a block-selecting
+    workload (block b -> positions b*t .. b*t + t - 1, -1 -> t paddings)."""
+    import numpy as np
+    t = w.sel_block_tokens
+    if t <= 1:
+        return traces
+    out = {}
+    for a, (blk, nw) in traces.items():
+        pos = (blk[..., None].astype(np.int64) * t + np.arange(t)).reshape(*blk.shape[:-1], -1)
+        out[a] = (np.where(np.repeat(blk == -1, t, axis=-1), -1, pos).astype(np.int32), nw)
+    return out
+
+
 def cpu_oracle_rate(w, traces, host_views=None, budget_s=10.0):
     """The C oracle (single thread) on the same workload's steps: selections/s.
 
@@ -280,7 +294,7 @@ def run_reference(args):
     w = get(args.workload)
     w = w.scaled(steps=max(w.steps, args.warmup + args.steps)) if w.write_through else w
     traces = all_traces(w)
-    res = cpu_oracle_rate(w, traces, budget_s=60.0)
+    res = cpu_oracle_rate(w, token_traces(w, traces), budget_s=60.0)
     steps = res["steps"]
     line = {"impl": "reference", "metric": METRIC, "value": res["value"], "unit": "selections/s",
             "n_gpus": args.gpus, "steps": steps, "warmup": 0,
@@ -367,7 +381,7 @@ def run_ours(args):
         new_rows = torch.from_numpy(REC.new_token_records(w)).to(dev)
     out = torch.full((G, w.R, w.k), -1, dtype=torch.int32, device=dev)
     runner = DecodeStep(hs, mem, groups, flags=H.FROM_MIRROR if args.mirror else 0,
-                        fused=not args.unfused)
+                        fused=not args.unfused, sel_block_tokens=w.sel_block_tokens)
     miss_hist = torch.zeros((T, G, w.R), dtype=torch.int32, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)     # > 129 MB L2
     setup_s = time.perf_counter() - t_setup
@@ -405,7 +419,7 @@ def run_ours(args):
         RESOLVE and write-back launch and a copy of the miss counts."""
         evs, wev, rpev = [], [], []
         orig_resolve, orig_step = hs.resolve, hs.resolve_step
-        orig_res = hs.resolve_resident
+        orig_res, orig_ex = hs.resolve_resident, hs.resolve_ex
         orig_wb, orig_rp = hs.writeback, hs.prefetch_plan
 
         def timed_resolve(layer, *a, **kw):
@@ -432,6 +446,14 @@ def run_ours(args):
             e1.record(st)
             evs.append((e0, e1))
 
+        def timed_ex(layer, *a, **kw):
+            st = kw.get("stream")
+            e0, e1 = timing_event()[0], timing_event()[0]
+            e0.record(st)
+            orig_ex(layer, *a, **kw)
+            e1.record(st)
+            evs.append((e0, e1))
+
         def timed_wb(layer, *a, **kw):
             st = kw.get("stream")
             e0, e1 = timing_event()[0], timing_event()[0]
@@ -450,7 +472,7 @@ def run_ours(args):
 
         if instrument:
             hs.resolve, hs.resolve_step = timed_resolve, timed_step
-            hs.resolve_resident = timed_res
+            hs.resolve_resident, hs.resolve_ex = timed_res, timed_ex
             hs.writeback, hs.prefetch_plan = timed_wb, timed_rp
         g = torch.cuda.CUDAGraph()
         try:
@@ -463,7 +485,7 @@ def run_ours(args):
                                                 stream=torch.cuda.current_stream())
         finally:
             hs.resolve, hs.resolve_step = orig_resolve, orig_step
-            hs.resolve_resident = orig_res
+            hs.resolve_resident, hs.resolve_ex = orig_res, orig_ex
             hs.writeback, hs.prefetch_plan = orig_wb, orig_rp
         return g, evs, wev, rpev
 
@@ -525,7 +547,7 @@ def run_ours(args):
     flags, _ = hs.status()
 
     verify = None
-    if args.verify and not args.resident:
+    if args.verify and not args.resident and w.sel_block_tokens == 1:
         verify = verify_against_oracle(w, hs, mem, groups, traces, args.warmup + args.steps)
 
     # ---- pass 2 (per-kernel durations for the roofline): the same steps from
@@ -616,9 +638,10 @@ def run_ours(args):
         with torch.cuda.stream(cap):
             with torch.cuda.graph(gh, stream=cap):
                 for gi, (a, _) in enumerate(groups):
-                    hs.resolve(a, sel[t_last, gi], out[gi], None,
-                               newest[t_last] if newest is not None else None, H.SKIP_IO,
-                               stream=torch.cuda.current_stream())
+                    hs.resolve_ex(a, sel[t_last, gi], out[gi], None,
+                                  newest[t_last] if newest is not None else None,
+                                  sel_block_tokens=w.sel_block_tokens, flags=H.SKIP_IO,
+                                  stream=torch.cuda.current_stream())
         torch.cuda.synchronize()
         hit_ms = []
         for i in range(10):
@@ -646,7 +669,7 @@ def run_ours(args):
     if not args.no_e2e:
         h_sel = torch.from_numpy(sel_np).pin_memory()
         h_out = torch.empty((T, G, w.R, w.k), dtype=torch.int32).pin_memory()
-        d_sel = torch.empty((G, w.R, w.k), dtype=torch.int32, device=dev)
+        d_sel = torch.empty(sel_np.shape[1:], dtype=torch.int32, device=dev)
         if w.write_through:
             h_new = torch.from_numpy(REC.new_token_records(w)).pin_memory()
             h_newest = torch.from_numpy(newest_np).pin_memory()
@@ -753,10 +776,11 @@ def run_ours(args):
     cpu = cpu_mt = None
     if rank == 0 and not args.no_cpu and not args.resident:
         views = {l: mem.host_view(l) for l in range(w.L)}
-        cpu = cpu_oracle_rate(w, traces, host_views=views, budget_s=20.0)
+        ttr = token_traces(w, traces)
+        cpu = cpu_oracle_rate(w, ttr, host_views=views, budget_s=20.0)
         cpu.pop("seconds", None)
         cpu.pop("steps", None)
-        cpu_mt = cpu_oracle_rate_threads(w, traces, views, os.cpu_count() or 1)
+        cpu_mt = cpu_oracle_rate_threads(w, ttr, views, os.cpu_count() or 1)
         cpu_mt.pop("seconds", None)
 
     hp_frac_end = mem.pool.hugepage_fraction()

@@ -42,6 +42,7 @@ class _Layer(ctypes.Structure):
         ("plan_count", ctypes.c_void_p), ("mark", ctypes.c_void_p),
         ("mark_gen", ctypes.c_int32), ("hit", ctypes.c_void_p),
         ("misses", ctypes.c_void_p), ("ev", ctypes.c_void_p),
+        ("first", ctypes.c_void_p),
     ]
 
 
@@ -57,7 +58,7 @@ def _load():
         lib.hso_resolve_layer.argtypes = [P, vp, vp, ctypes.c_int32, ctypes.c_int32, vp]
         lib.hso_resolve_layer.restype = ctypes.c_int32
         lib.hso_resolve_layer_res.argtypes = [P, vp, vp, vp, ctypes.c_int32, ctypes.c_int32,
-                                              ctypes.c_int32, ctypes.c_int32, vp]
+                                              ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, vp]
         lib.hso_resolve_layer_res.restype = ctypes.c_int32
         lib.hso_set_newest_rows.argtypes = [P, vp, ctypes.c_int32]
         lib.hso_writeback.argtypes = [P, vp, ctypes.c_int32]
@@ -106,34 +107,37 @@ class OracleLayer:
         self._hit = np.zeros(B, np.uint8)
         self._misses = np.zeros(k, np.int32)
         self._ev = np.zeros(B, np.int16)
+        self._first = np.zeros(P, np.int32) if m else None
         self._s = _Layer(R, k, B, P, rec, _p(self.slot_pos), _p(self.lru), _p(self.page_table),
                          _p(self.miss_count), _p(self.unit_err), _p(self.hot),
                          ctypes.c_void_p(host_ptr) if host_ptr else None, host_req_stride,
                          self.host_split, _p(self.host_tail), _p(self.plan_pos),
                          _p(self.plan_slot), _p(self.plan_count), _p(self._mark), 0,
-                         _p(self._hit), _p(self._misses), _p(self._ev))
+                         _p(self._hit), _p(self._misses), _p(self._ev), _p(self._first))
         self._lib = _load()
 
     def reset(self, r=None):
         for rr in (range(self.R) if r is None else [r]):
             self._lib.hso_reset_unit(ctypes.byref(self._s), rr)
 
-    def resolve(self, sel, newest=None, num_reqs=None, io=True, res_blocks=None, res_tok=1):
+    def resolve(self, sel, newest=None, num_reqs=None, io=True, res_blocks=None, res_tok=1,
+                union=False):
         """sel int32 [R][k]; newest int32 [R] or None; res_blocks int32
-        [R][nblk] (resident block table, -1 = not resident) or None.
+        [R][nblk] (resident block table, -1 = not resident) or None; union:
+        repeated positions share their first reference's row.
         Returns (out [R][k], err)."""
         sel = np.ascontiguousarray(sel, dtype=np.int32)
         nr = self.R if num_reqs is None else num_reqs
         out = np.full((self.R, self.k), -1, np.int32)
         nw = None if newest is None else np.ascontiguousarray(newest, dtype=np.int32)
-        if res_blocks is None:
+        if res_blocks is None and not union:
             e = self._lib.hso_resolve_layer(ctypes.byref(self._s), _p(sel), _p(nw), nr,
                                             int(bool(io)), _p(out))
         else:
-            rb = np.ascontiguousarray(res_blocks, dtype=np.int32)
+            rb = None if res_blocks is None else np.ascontiguousarray(res_blocks, dtype=np.int32)
             e = self._lib.hso_resolve_layer_res(ctypes.byref(self._s), _p(sel), _p(nw), _p(rb),
-                                                rb.shape[1], int(res_tok), nr, int(bool(io)),
-                                                _p(out))
+                                                0 if rb is None else rb.shape[1], int(res_tok),
+                                                int(bool(union)), nr, int(bool(io)), _p(out))
         return out, e
 
     def set_newest_rows(self, rows, num_reqs=None):

@@ -31,6 +31,11 @@
  * does not fit int32, fails the unit like an out-of-range position.  The
  * duplicate check covers positions that reach the hot tier only (a resident
  * position never touches the cache; the pages exit before the hash table).
+ *
+ * Union mode (speculative verification, gentlecold.top §6.5: one block
+ * resolves the union of all verify rows' top-k, misses in (row, top-k)
+ * first-reference order): the rows come as one list; a repeated position is
+ * resolved at its first reference and later references output the same row.
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -66,6 +71,7 @@ typedef struct {
   uint8_t *hit;              /* [B] scratch */
   int32_t *misses;           /* [k] scratch */
   int16_t *ev;               /* [B] scratch */
+  int32_t *first;            /* [P] scratch: first list index of each position */
 } hso_layer;
 
 static const uint8_t *host_row(const hso_layer *L, int32_t r, int64_t p) {
@@ -112,7 +118,7 @@ static int64_t resident_row(const hso_layer *L, const int32_t *blk, int32_t nblk
    Returns 0 or a bit-OR of HSO_ERR_*. */
 int32_t hso_resolve_unit_res(hso_layer *L, int32_t r, const int32_t *sel, int32_t newest,
                              int32_t io, const int32_t *blk, int32_t nblk, int32_t tok,
-                             int32_t *out) {
+                             int32_t union_mode, int32_t *out) {
   const int32_t B = L->B, k = L->k;
   const int64_t P = L->P;
   int32_t *slot_pos = L->slot_pos + (int64_t)r * B;
@@ -132,8 +138,12 @@ int32_t hso_resolve_unit_res(hso_layer *L, int32_t r, const int32_t *sel, int32_
     rr = resident_row(L, blk, nblk, tok, p);
     if (rr == -2) { err |= HSO_ERR_RANGE; continue; }
     if (rr >= 0) continue; /* resident: never reaches the hot tier */
-    if (L->mark[p] == L->mark_gen) err |= HSO_ERR_DUP;
-    L->mark[p] = L->mark_gen;
+    if (L->mark[p] == L->mark_gen) {
+      if (!union_mode) err |= HSO_ERR_DUP;
+    } else {
+      L->mark[p] = L->mark_gen;
+      L->first[p] = i;
+    }
   }
   if (newest < -1 || (int64_t)newest >= P) err |= HSO_ERR_RANGE;
   L->unit_err[r] = err;
@@ -152,6 +162,8 @@ int32_t hso_resolve_unit_res(hso_layer *L, int32_t r, const int32_t *sel, int32_
       out[i] = -1;
     } else if (resident_row(L, blk, nblk, tok, p) >= 0) {
       out[i] = (int32_t)(L->B + 1 + resident_row(L, blk, nblk, tok, p));
+    } else if (union_mode && L->first[p] != i) {
+      out[i] = INT32_MIN; /* a later reference: its first's row, below */
     } else if (newest >= 0 && p == newest) {
       out[i] = B;
     } else if (pt[p] >= 0) {
@@ -183,6 +195,10 @@ int32_t hso_resolve_unit_res(hso_layer *L, int32_t r, const int32_t *sel, int32_
     plan_slot[j] = s;
   }
 
+  if (union_mode)
+    for (i = 0; i < k; i++)
+      if (out[i] == INT32_MIN) out[i] = out[L->first[sel[i]]];
+
   /* new LRU: remaining evictables, then this step's fetches, then hits */
   for (j = M; j < E; j++) lru[n++] = L->ev[j];
   for (j = 0; j < M; j++) lru[n++] = L->ev[j];
@@ -196,7 +212,7 @@ int32_t hso_resolve_unit_res(hso_layer *L, int32_t r, const int32_t *sel, int32_
 
 int32_t hso_resolve_unit(hso_layer *L, int32_t r, const int32_t *sel, int32_t newest,
                          int32_t io, int32_t *out) {
-  return hso_resolve_unit_res(L, r, sel, newest, io, NULL, 0, 1, out);
+  return hso_resolve_unit_res(L, r, sel, newest, io, NULL, 0, 1, 0, out);
 }
 
 /* One layer-step over requests [0, num_reqs): sel [R][k], newest [R] or NULL,
@@ -204,18 +220,18 @@ int32_t hso_resolve_unit(hso_layer *L, int32_t r, const int32_t *sel, int32_t ne
    errors. */
 int32_t hso_resolve_layer_res(hso_layer *L, const int32_t *sel, const int32_t *newest,
                               const int32_t *res_blocks, int32_t nblk, int32_t tok,
-                              int32_t num_reqs, int32_t io, int32_t *out) {
+                              int32_t union_mode, int32_t num_reqs, int32_t io, int32_t *out) {
   int32_t r, e = 0;
   for (r = 0; r < num_reqs; r++)
     e |= hso_resolve_unit_res(L, r, sel + (int64_t)r * L->k, newest ? newest[r] : -1, io,
                               res_blocks ? res_blocks + (int64_t)r * nblk : NULL, nblk, tok,
-                              out + (int64_t)r * L->k);
+                              union_mode, out + (int64_t)r * L->k);
   return e;
 }
 
 int32_t hso_resolve_layer(hso_layer *L, const int32_t *sel, const int32_t *newest,
                           int32_t num_reqs, int32_t io, int32_t *out) {
-  return hso_resolve_layer_res(L, sel, newest, NULL, 0, 1, num_reqs, io, out);
+  return hso_resolve_layer_res(L, sel, newest, NULL, 0, 1, 0, num_reqs, io, out);
 }
 
 /* The caller writes the new token's KV into row B of each request. */

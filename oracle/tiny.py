@@ -44,6 +44,16 @@ the hot buffer is consulted, and touches neither the LRU nor the page table:
       resident exit before the hash table is built, so a repeated resident
       position is not an error and outputs its row at each index.
 
+For speculative verification (gentlecold.top §6.5, "one block resolves the
+union of all verify rows' top-k ... misses are allocated in (row, top-k)
+first-reference order"; docs.vllm.ai "Hot lookup and LRU", speculative
+decoding) a request's verify rows are passed as one list, row after row, in
+union mode:
+  R15 a position repeated anywhere in the list is resolved once, at its
+      first reference, and every later reference outputs the same row; it is
+      not an error.  Misses are the first references, in list order; the
+      miss count and the plan count each missed position once.
+
 See ``tests/test_oracle_pins.py`` for what pins each of these.
 
 [P1] = gentlecold.top, "HiSparse 深度解析：论文、SGLang 实现与 vLLM Hybrid
@@ -71,7 +81,7 @@ class Unit:
         self.miss_count = 0
 
     # ------------------------------------------------------------------ #
-    def resolve(self, sel, newest=-1, skip_io=False, res_blocks=None, res_tok=1):
+    def resolve(self, sel, newest=-1, skip_io=False, res_blocks=None, res_tok=1, union=False):
         """One RESOLVE of this unit for the selection list ``sel``.
 
         Returns ``(out, plan, err)``: ``out[i]`` is the physical slot for
@@ -81,7 +91,8 @@ class Unit:
         decided); ``err`` is 0 or a bit-OR of ``ERR_RANGE`` / ``ERR_DUP``.
         ``res_blocks`` (optional) is this request's resident block table: the
         entry of block ``p // res_tok`` is -1 (not resident) or the block's
-        index in the resident store (reading R14).
+        index in the resident store (reading R14).  ``union``: repeated
+        positions share their first reference's row (reading R15).
         """
         B, P = self.B, self.P
         k = len(sel)
@@ -112,7 +123,7 @@ class Unit:
                 continue
             if rr >= 0:
                 continue                   # never reaches the hot tier (R14)
-            if p in seen:
+            if p in seen and not union:
                 err |= ERR_DUP
             seen.add(p)
         if newest < -1 or newest >= P:
@@ -126,7 +137,11 @@ class Unit:
         out = [None] * k
         hit_slots = set()
         misses = []                        # selection indices, in list order
+        first = {}                         # union mode: position -> first index
         for i, p in enumerate(sel):
+            if union and p != -1 and p in first:
+                continue                   # a later reference: filled in below
+            first[p] = i
             if p == -1:
                 out[i] = -1
             elif resident_row(p) >= 0:
@@ -159,6 +174,11 @@ class Unit:
                 self.hot[s] = self.host(p)
             out[i] = s
             plan.append((p, s))
+
+        if union:                          # later references share the first's row
+            for i, p in enumerate(sel):
+                if out[i] is None:
+                    out[i] = out[first[p]]
 
         # New recency order: untouched evictables (oldest), then this step's
         # fetches, then this step's hits (newest) -- [P1] §3.3 and the worked

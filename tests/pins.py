@@ -72,11 +72,11 @@ class CUnit:
     def preset(self, slot_pos, lru):
         self._pending = (list(slot_pos), list(lru))
 
-    def resolve(self, sel, newest=-1, skip_io=False, res_blocks=None, res_tok=1):
+    def resolve(self, sel, newest=-1, skip_io=False, res_blocks=None, res_tok=1, union=False):
         L = self._layer(len(sel))
         rb = None if res_blocks is None else np.array([res_blocks], np.int32)
         out, e = L.resolve(np.array([sel], np.int32), np.array([newest], np.int32),
-                           io=not skip_io, res_blocks=rb, res_tok=res_tok)
+                           io=not skip_io, res_blocks=rb, res_tok=res_tok, union=union)
         plan = [(int(L.plan_pos[0, j]), int(L.plan_slot[0, j])) for j in range(L.plan_count[0])]
         return [int(x) for x in out[0]], plan, int(e)
 
@@ -443,6 +443,76 @@ def pin_resident_repeat(cls):
 RESIDENT_PINS = [pin_resident_none_is_plain, pin_resident_masks, pin_resident_all,
                  pin_resident_errors, pin_resident_repeat]
 
+
+# ---------------------------------------------------------------------- #
+# Union mode: speculative verify rows resolved as one list               #
+# (gentlecold.top §6.5: the union of all verify rows' top-k; misses in     #
+# (row, top-k) first-reference order)                                     #
+# ---------------------------------------------------------------------- #
+def pin_union_without_repeats_is_plain(cls, seeds=range(6)):
+    for seed in seeds:
+        rnd = random.Random(9000 + seed)
+        k, B, P = 6, 10, 40
+        a, b = make(cls, B, P, k=k), make(cls, B, P, k=k)
+        for _ in range(8):
+            sel = rnd.sample(range(P), rnd.randint(0, k))
+            sel += [-1] * (k - len(sel))
+            ra = a.resolve(sel, union=True)
+            rb = b.resolve(sel)
+            assert ra == rb and _snap(a) == _snap(b)
+
+
+def pin_union_is_first_reference(cls, seeds=range(20)):
+    """Union resolve == resolving the list with every repeat replaced by
+    padding, then copying each repeat's output from its first reference
+    (state, plan and miss count identical).  Rows overlap like the top-k of
+    consecutive draft tokens."""
+    for seed in seeds:
+        rnd = random.Random(9500 + seed)
+        V, kr = rnd.randint(2, 4), rnd.randint(2, 4)
+        k, P = V * kr, 30
+        B = k + rnd.randint(0, 3)
+        host = lambda p: bytes([(p * 13 + i) & 0xFF for i in range(8)])  # noqa: E731
+        a, b = make(cls, B, P, k=k, host=host), make(cls, B, P, k=k, host=host)
+        base = rnd.sample(range(P), kr)
+        for t in range(8):
+            rows = []
+            for _ in range(V):
+                row = [p if rnd.random() < 0.7 else rnd.randrange(P) for p in base]
+                row = list(dict.fromkeys(row))          # a top-k row has no repeats
+                rows += row + [-1] * (kr - len(row))
+            newest = rnd.choice([-1] + [p for p in rows if p >= 0])
+            first, masked = {}, []
+            for i, p in enumerate(rows):
+                if p >= 0 and p in first:
+                    masked.append(-1)
+                else:
+                    first.setdefault(p, i)
+                    masked.append(p)
+            oa, pa, ea = a.resolve(rows, newest=newest, union=True)
+            ob, pb, eb = b.resolve(masked, newest=newest)
+            assert ea == 0 and eb == 0
+            assert [tuple(x) for x in pa] == [tuple(x) for x in pb]
+            assert _snap(a) == _snap(b), (seed, t)
+            for i, p in enumerate(rows):
+                assert oa[i] == (ob[first[p]] if p >= 0 else -1), (seed, t, i)
+            assert a.hot[:B] == b.hot[:B]
+            base = [p for p in rows if p >= 0][:kr] or base
+
+
+def pin_union_example(cls):
+    """Two verify rows {1,2,3} and {3,4,1} from the admission state: misses
+    1, 2, 3, 4 take slots 0..3 in first-reference order."""
+    u = make(cls, 8, 32, k=6)
+    out, plan, err = u.resolve([1, 2, 3, 3, 4, 1], union=True)
+    assert err == 0 and out == [0, 1, 2, 2, 3, 0]
+    assert [tuple(x) for x in plan] == [(1, 0), (2, 1), (3, 2), (4, 3)]
+    assert u.miss_count == 4 and list(u.lru) == [4, 5, 6, 7, 0, 1, 2, 3]
+
+
+UNION_PINS = [pin_union_without_repeats_is_plain, pin_union_is_first_reference,
+              pin_union_example]
+
 ALL_PINS = [pin_example_b, pin_example_a, pin_textbook_lru, pin_hit_order, pin_miss_order,
             pin_newest_and_padding, pin_errors, pin_invariants, pin_disjoint_at_b_equals_k,
-            pin_belady_bound] + RESIDENT_PINS
+            pin_belady_bound] + RESIDENT_PINS + UNION_PINS

@@ -74,9 +74,10 @@ def test_optimal_closed_forms():
 # ---------------------------------------------------------------------- #
 # Python model == C model, full state, on random traces                   #
 # ---------------------------------------------------------------------- #
+@pytest.mark.parametrize("union", [False, True])
 @pytest.mark.parametrize("resident", [False, True])
 @pytest.mark.parametrize("seed", range(12))
-def test_python_equals_c(seed, resident):
+def test_python_equals_c(seed, resident, union):
     from oracle.coracle import OracleLayer
     rnd = random.Random(seed)
     R = rnd.randint(1, 3)
@@ -94,8 +95,10 @@ def test_python_equals_c(seed, resident):
         for r in range(R):
             n = rnd.randint(0, k)
             S = rnd.sample(range(P), n)
-            if rnd.random() < 0.08 and n >= 2:
-                S[1] = S[0]                      # duplicate
+            if rnd.random() < (0.5 if union else 0.08) and n >= 2:
+                S[1] = S[0]                      # duplicate (a shared position in union mode)
+            if union and n >= 4 and rnd.random() < 0.5:
+                S[3] = S[2]
             if rnd.random() < 0.05 and n >= 1:
                 S[0] = rnd.choice([P, P + 5, -3])  # out of range
             sel[r, :n] = S
@@ -108,12 +111,13 @@ def test_python_equals_c(seed, resident):
             blocks = np.array([[rnd.randrange(200) if rnd.random() < 0.3 else
                                 (-1 if rnd.random() < 0.97 else -4) for _ in range(nb)]
                                for _ in range(R)], np.int32)
-        out_c, e_c = c.resolve(sel, newest, res_blocks=blocks, res_tok=tok)
+        out_c, e_c = c.resolve(sel, newest, res_blocks=blocks, res_tok=tok, union=union)
         e_py = 0
         for r in range(R):
             out, plan, err = py[r].resolve([int(x) for x in sel[r]], int(newest[r]),
                                            res_blocks=None if blocks is None else
-                                           [int(x) for x in blocks[r]], res_tok=tok)
+                                           [int(x) for x in blocks[r]], res_tok=tok,
+                                           union=union)
             e_py |= err
             assert out == list(out_c[r]), (t, r)
             assert err == c.unit_err[r]
@@ -187,9 +191,14 @@ def test_replay_follows_anchor_slots():
 class _Mutant(Unit):
     mutation = None
 
-    def resolve(self, sel, newest=-1, skip_io=False, res_blocks=None, res_tok=1):
+    def resolve(self, sel, newest=-1, skip_io=False, res_blocks=None, res_tok=1, union=False):
         m = self.mutation
         B, P, k = self.B, self.P, len(sel)
+        if union and m == "union_last_reference":
+            sel = list(sel)
+            order = list(range(k))[::-1]      # classify from the end: last reference wins
+        else:
+            order = list(range(k))
 
         def rrow(p):
             if res_blocks is None or p // res_tok >= len(res_blocks):
@@ -214,7 +223,7 @@ class _Mutant(Unit):
                 continue
             if rrow(p) >= 0 and m != "resident_dup_checked":
                 continue
-            if p in seen and m != "no_dup_check":
+            if p in seen and m != "no_dup_check" and (not union or m == "union_repeat_is_error"):
                 err |= ERR_DUP
             seen.add(p)
         if newest < -1 or newest >= P:
@@ -222,7 +231,12 @@ class _Mutant(Unit):
         if err:
             return [-1] * k, [], err
         out, hits, misses = [None] * k, [], []
-        for i, p in enumerate(sel):
+        first = {}
+        for i in order:
+            p = sel[i]
+            if union and p != -1 and p in first and m != "union_counts_repeats":
+                continue
+            first.setdefault(p, i)
             hot = p in self.page_table
             if p == -1:
                 out[i] = -1
@@ -244,6 +258,7 @@ class _Mutant(Unit):
                 hits.append(out[i])
             else:
                 misses.append(i)
+        misses.sort()
         ev = [s for s in self.lru if s not in hits]
         if m == "victims_from_newest_end":
             ev = ev[::-1]
@@ -261,6 +276,9 @@ class _Mutant(Unit):
                 self.hot[s] = self.host(p + 1 if m == "fetch_off_by_one" else p)
             out[i] = s
             plan.append((p, s))
+        for i, p in enumerate(sel):
+            if out[i] is None:
+                out[i] = out[first[p]]
         hs = sorted(hits)
         if m == "hits_in_selection_order":
             hs = hits
@@ -285,7 +303,9 @@ MUTATIONS = ["no_dup_check", "newest_is_miss", "victims_from_newest_end", "keep_
              # resident tier
              "resident_after_hot", "resident_after_newest", "resident_is_hit",
              "resident_counts_miss", "resident_no_offset", "resident_no_entry_check",
-             "resident_dup_checked"]
+             "resident_dup_checked",
+             # union mode
+             "union_last_reference", "union_counts_repeats", "union_repeat_is_error"]
 
 
 @pytest.mark.parametrize("mutation", MUTATIONS)

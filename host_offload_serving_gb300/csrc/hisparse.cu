@@ -49,6 +49,7 @@ constexpr int kThreads = 1024;            // threads per resolve CTA
 constexpr int kWarps = kThreads / 32;     // == 32: one warp total per lane
 constexpr int kUnroll = 4;                // 16-byte loads in flight per thread
 constexpr int32_t kUnresolved = INT32_MIN;
+constexpr uint32_t kAlias = 1u << 30;  // a victim entry of a repeated miss (union mode): not fetched
 constexpr unsigned kFull = 0xffffffffu;
 static_assert(kWarps == 32, "warp-total scan assumes 32 warps");
 
@@ -596,6 +597,7 @@ struct PtLayout {
   uint32_t w_sel, w_out, w_mi, w_mp, w_hit, w_vict, w_misc, w_bkt, w_bidx, w_ord;  // worker
   uint32_t l_lru, l_slotpos, l_hit, l_newlru, l_ev, l_mpos, l_hkey, l_misc;     // leader
   uint32_t l_prevrow;                                                             // leader
+  uint32_t l_hmin, l_alias;  // union mode: first list index per set entry, per miss its unique index
   uint32_t cnt, total;
 };
 
@@ -621,6 +623,8 @@ __host__ __device__ inline PtLayout pt_layout(int k, int B, int ks, int hcap, in
   L.l_mpos = o;    o += align16(4u * k);
   L.l_hkey = o;    o += align16(4u * hcap);
   L.l_misc = o;    o += align16(4u * (8 + kMaxWorkers + 1));
+  L.l_hmin = o;    o += align16(4u * hcap);
+  L.l_alias = o;   o += align16(4u * k);
   L.cnt = o;       o += align16(4u * 64);
   L.l_prevrow = o; o += align16(static_cast<uint32_t>(rec));
   L.total = o;
@@ -651,6 +655,9 @@ struct PtArgs {
   // Block-id selections: sel holds k / sel_bt block ids per request, each
   // standing for sel_bt consecutive positions (1 = sel holds positions).
   int32_t sel_bt;
+  // Union mode (speculative verify rows resolved as one list): a repeated
+  // position is resolved at its first reference and shares its row.
+  int32_t union_mode;
   int64_t P;
   const int32_t *sel, *num_reqs, *newest;
   int32_t *out;
@@ -833,7 +840,8 @@ __device__ int pt_worker_classify(const PtArgs &a, int r, int i0, int n, int32_t
           v = -1;
         } else {
           const uint32_t bit = 1u << (s[u] & 31);
-          if (atomicOr(&w_hit[s[u] >> 5], bit) & bit) atomicOr(&w_misc[kWErr], HISPARSE_ERR_DUP);
+          if ((atomicOr(&w_hit[s[u] >> 5], bit) & bit) && !(kExt && a.union_mode))
+            atomicOr(&w_misc[kWErr], HISPARSE_ERR_DUP);
           v = s[u];
         }
       } else {
@@ -920,8 +928,10 @@ __device__ void pt_worker_order(const PtArgs &a, int j0, int mw, unsigned char *
 
 // Leader: merge the workers' slices, check duplicates, choose victims and the
 // new LRU order.  Returns nothing; results live in the leader's shared memory.
+template <bool kExt>
 __device__ void pt_leader_decide(const PtArgs &a, int cs, int nw, int32_t newest,
                                  unsigned char *smem, const PtLayout &L) {
+  const bool uni = kExt && a.union_mode;
   const int tid = threadIdx.x, lane = tid & 31;
   const int B = a.B;
   const int nwords = (B + 31) / 32;
@@ -932,6 +942,8 @@ __device__ void pt_leader_decide(const PtArgs &a, int cs, int nw, int32_t newest
   int32_t *l_ev = reinterpret_cast<int32_t *>(smem + L.l_ev);
   int32_t *l_mpos = reinterpret_cast<int32_t *>(smem + L.l_mpos);
   int32_t *l_hkey = reinterpret_cast<int32_t *>(smem + L.l_hkey);
+  int32_t *l_hmin = reinterpret_cast<int32_t *>(smem + L.l_hmin);
+  int32_t *l_alias = reinterpret_cast<int32_t *>(smem + L.l_alias);
   uint32_t *l_misc = reinterpret_cast<uint32_t *>(smem + L.l_misc);
   int32_t *s_cnt = reinterpret_cast<int32_t *>(smem + L.cnt);
   const uint32_t *w_misc0 = reinterpret_cast<const uint32_t *>(smem + L.w_misc);
@@ -962,7 +974,7 @@ __device__ void pt_leader_decide(const PtArgs &a, int cs, int nw, int32_t newest
     if (lane < nw) l_misc[kLPrefix + lane] = static_cast<uint32_t>(inc - cnt);
     if (lane == 31) {
       if (newest < -1 || newest >= a.P) err |= HISPARSE_ERR_RANGE;
-      if (seen > 1) err |= HISPARSE_ERR_DUP;
+      if (seen > 1 && !uni) err |= HISPARSE_ERR_DUP;
       l_misc[kLPrefix + nw] = static_cast<uint32_t>(inc);
       l_misc[kLErr] = err;
       l_misc[kLM] = static_cast<uint32_t>(inc);
@@ -984,6 +996,7 @@ __device__ void pt_leader_decide(const PtArgs &a, int cs, int nw, int32_t newest
       if (b) dup |= atomicOr(&l_hit[x], b) & b;
       any |= b;
     }
+    if (uni) dup = 0;  // a slot hit from two slices is one shared position
     if (any) l_misc[kLAnyHit] = 1;
     const int M = static_cast<int>(l_misc[kLM]);
     for (int g = tid; g < M; g += kThreads) {
@@ -995,9 +1008,9 @@ __device__ void pt_leader_decide(const PtArgs &a, int cs, int nw, int32_t newest
       uint32_t h = hash_pos(p, a.hcap_log2);
       for (int probe = 0; probe < hcap; ++probe) {
         const int32_t prev = atomicCAS(&l_hkey[h], -1, p);
-        if (prev == -1) break;
-        if (prev == p) {
-          dup = 1;
+        if (prev == -1 || prev == p) {
+          if (uni) atomicMin(&l_hmin[h], g);  // the entry keeps its first reference
+          else if (prev == p) dup = 1;
           break;
         }
         h = (h + 1) & (hcap - 1);
@@ -1007,6 +1020,55 @@ __device__ void pt_leader_decide(const PtArgs &a, int cs, int nw, int32_t newest
   }
   __syncthreads();
   if (l_misc[kLErr]) return;  // uniform
+  if (uni) {
+    // Union mode ([DD] §6.5: misses in first-reference order): miss g is a
+    // real miss when it is its position's first reference; its unique index
+    // u is the number of first references before it.  Every miss g records in
+    // l_alias the unique index of its position's first reference, negated and
+    // offset (-1 - u) for a later reference.  The unique positions then
+    // replace l_mpos in list order.
+    const int Mall = static_cast<int>(l_misc[kLM]);
+    int32_t *l_upos = l_hkey;  // the set is not needed once l_alias is known
+    for (int g0 = 0; g0 < Mall; g0 += kThreads) {
+      const int g = g0 + tid;
+      int32_t rep = g;
+      if (g < Mall) {
+        const int32_t p = l_mpos[g];
+        uint32_t h = hash_pos(p, a.hcap_log2);
+        for (int probe = 0; probe < hcap && l_hkey[h] != p; ++probe) h = (h + 1) & (hcap - 1);
+        rep = l_hmin[h];
+      }
+      const bool first = g < Mall && rep == g;
+      const uint32_t m = __ballot_sync(kFull, first);
+      if (lane == 31) s_cnt[tid >> 5] = __popc(m);
+      __syncthreads();
+      int before = static_cast<int>(l_misc[kLHits]);  // running count of first references
+      for (int x = 0; x < (tid >> 5); ++x) before += s_cnt[x];
+      const int u = before + __popc(m & lanemask_lt());
+      if (first) l_alias[g] = u;
+      else if (g < Mall) l_alias[g] = -1 - rep;  // resolved below, once every u is known
+      __syncthreads();
+      if (tid == kThreads - 1) l_misc[kLHits] = static_cast<uint32_t>(u + (first ? 1 : 0));
+      __syncthreads();
+    }
+    for (int g = tid; g < Mall; g += kThreads) {
+      const int32_t v = l_alias[g];
+      if (v >= 0) l_upos[v] = l_mpos[g];
+    }
+    __syncthreads();
+    for (int g = tid; g < Mall; g += kThreads) {
+      const int32_t v = l_alias[g];
+      if (v < 0) l_alias[g] = -1 - l_alias[-1 - v];  // later reference: -1 - (its first's u)
+    }
+    const int M = static_cast<int>(l_misc[kLHits]);
+    __syncthreads();
+    for (int u = tid; u < M; u += kThreads) l_mpos[u] = l_upos[u];
+    if (tid == 0) {
+      l_misc[kLM] = static_cast<uint32_t>(M);
+      l_misc[kLHits] = 0;
+    }
+    __syncthreads();
+  }
   // No miss and no hot hit (every selection resident, newest or padding): the
   // LRU order stays as it is ([DD] §6.5: resident hits exit before the LRU).
   if (l_misc[kLM] == 0 && l_misc[kLAnyHit] == 0) {
@@ -1065,10 +1127,13 @@ __device__ void pt_leader_decide(const PtArgs &a, int cs, int nw, int32_t newest
 // Leader: hand every slice the verdict and its victims, written straight
 // into the workers' shared memory, so that after the next cluster barrier a
 // worker reads them locally.
-__device__ void pt_leader_push(int cs, int nw, unsigned char *smem, const PtLayout &L) {
+template <bool kExt>
+__device__ void pt_leader_push(const PtArgs &a, int cs, int nw, unsigned char *smem,
+                               const PtLayout &L) {
   const int tid = threadIdx.x;
   const uint32_t *l_misc = reinterpret_cast<const uint32_t *>(smem + L.l_misc);
   const int32_t *l_ev = reinterpret_cast<const int32_t *>(smem + L.l_ev);
+  const int32_t *l_alias = reinterpret_cast<const int32_t *>(smem + L.l_alias);
   const uint32_t *w_misc0 = reinterpret_cast<const uint32_t *>(smem + L.w_misc);
   const int32_t *w_vict0 = reinterpret_cast<const int32_t *>(smem + L.w_vict);
   auto wrank = [&](int w) { return static_cast<uint32_t>(cs == 1 ? 0 : w + 1); };
@@ -1076,12 +1141,21 @@ __device__ void pt_leader_push(int cs, int nw, unsigned char *smem, const PtLayo
   for (int w = tid; w < nw; w += kThreads)
     st_dsmem_u32(dsmem_addr(&w_misc0[kWLeadErr], wrank(w)), err);
   if (err) return;
-  const int M = static_cast<int>(l_misc[kLM]);
-  for (int g = tid; g < M; g += kThreads) {
+  const bool uni = kExt && a.union_mode;
+  // every miss of every slice, repeats included (union mode)
+  const int Mall = static_cast<int>(uni ? l_misc[kLPrefix + nw] : l_misc[kLM]);
+  for (int g = tid; g < Mall; g += kThreads) {
     int w = 0;
     while (w + 1 < nw && static_cast<int>(l_misc[kLPrefix + w + 1]) <= g) ++w;
     const int j = g - static_cast<int>(l_misc[kLPrefix + w]);
-    st_dsmem_u32(dsmem_addr(&w_vict0[j], wrank(w)), static_cast<uint32_t>(l_ev[g]));
+    uint32_t v;
+    if (uni) {  // a later reference takes its first's slot and is not fetched
+      const int32_t al = l_alias[g];
+      v = al >= 0 ? static_cast<uint32_t>(l_ev[al]) : (static_cast<uint32_t>(l_ev[-1 - al]) | kAlias);
+    } else {
+      v = static_cast<uint32_t>(l_ev[g]);
+    }
+    st_dsmem_u32(dsmem_addr(&w_vict0[j], wrank(w)), v);
   }
 }
 
@@ -1177,7 +1251,7 @@ __device__ void pt_worker_finish(const PtArgs &a, int r, int i0, int n, int32_t 
         const uint32_t q32 = static_cast<uint32_t>(q);
         const int f = static_cast<int>(q32 / static_cast<uint32_t>(a.rec16));
         const int o = static_cast<int>(q32 - static_cast<uint32_t>(f) * a.rec16);
-        if (w_mp[f] != skip_pos)
+        if (w_mp[f] != skip_pos && !(w_vict[f] & kAlias))
           st_v4(dst + static_cast<int64_t>(w_vict[f]) * a.hot_row_stride + 16 * o, v[u]);
       }
     }
@@ -1195,7 +1269,7 @@ __device__ void pt_worker_finish(const PtArgs &a, int r, int i0, int n, int32_t 
           const int f = static_cast<int>(q32 / static_cast<uint32_t>(a.rec16));
           const int o = static_cast<int>(q32 - static_cast<uint32_t>(f) * a.rec16);
           const int j = w_ord[f];
-          if (w_mp[j] != skip_pos) {
+          if (w_mp[j] != skip_pos && !(w_vict[j] & kAlias)) {
             x[u] = ld_nc_v4(src + static_cast<int64_t>(w_mp[j]) * a.src_row_stride + 16 * o);
             d[u] = dst + static_cast<int64_t>(w_vict[j]) * a.hot_row_stride + 16 * o;
           }
@@ -1214,7 +1288,7 @@ __device__ void pt_worker_finish(const PtArgs &a, int r, int i0, int n, int32_t 
     else if (val != kUnresolved) g_out[t] = val;
   }
   if (!err)
-    for (int j = tid; j < mw; j += kThreads) g_out[w_mi[j]] = w_vict[j];
+    for (int j = tid; j < mw; j += kThreads) g_out[w_mi[j]] = w_vict[j] & ~static_cast<int32_t>(kAlias);
 }
 
 // Leader: the unit's LRU order and slot map into shared memory, and an empty
@@ -1243,6 +1317,10 @@ __device__ void pt_leader_load_state(const PtArgs &a, int r, bool have_sp0, int4
     }
   }
   for (int i = tid; i < (1 << a.hcap_log2); i += kThreads) l_hkey[i] = -1;
+  if (a.union_mode) {
+    int32_t *l_hmin = reinterpret_cast<int32_t *>(smem + L.l_hmin);
+    for (int i = tid; i < (1 << a.hcap_log2); i += kThreads) l_hmin[i] = INT32_MAX;
+  }
 }
 
 // Leader, fused write-through ([DD] §3.4 step 4), first half: keep the
@@ -1319,9 +1397,9 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_pt_kernel(const PtArgs a)
     pt_leader_write_through(a, r, prev, smem, L);
     const int mw = pt_worker_classify<kExt>(a, r, i0, n, newest, first, smem, L);
     pt_worker_order(a, 0, mw, smem, L);
-    pt_leader_decide(a, cs, nw, newest, smem, L);
+    pt_leader_decide<kExt>(a, cs, nw, newest, smem, L);
     __syncthreads();
-    pt_leader_push(cs, nw, smem, L);
+    pt_leader_push<kExt>(a, cs, nw, smem, L);
     pt_leader_publish<kRecordPlan>(a, r, prev, skip_pos, smem, L);
     __syncthreads();
     pt_worker_finish(a, r, i0, n, skip_pos, 0, nullptr, src, dst, smem, L);
@@ -1336,9 +1414,9 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_pt_kernel(const PtArgs a)
     pt_leader_write_through(a, r, prev, smem, L);
     __syncthreads();
     cluster_wait_acquire();    //    the slices are ready
-    pt_leader_decide(a, cs, nw, newest, smem, L);
+    pt_leader_decide<kExt>(a, cs, nw, newest, smem, L);
     __syncthreads();
-    pt_leader_push(cs, nw, smem, L);
+    pt_leader_push<kExt>(a, cs, nw, smem, L);
     __syncthreads();
     cluster_arrive_release();  // #1: the verdict and victims, in the workers' memory
     pt_leader_publish<kRecordPlan>(a, r, prev, skip_pos, smem, L);
@@ -1976,7 +2054,9 @@ int hisparse_resolve_ex(hisparse_handle *h, int32_t layer, const int32_t *d_sel,
     return HISPARSE_EINVAL;
   if (d_new_rows && !aligned16(d_new_rows)) return HISPARSE_EINVAL;
   if (!d_sel || !d_out) return HISPARSE_EINVAL;
-  if (flags & ~(HISPARSE_RECORD_PLAN | HISPARSE_SKIP_IO | HISPARSE_FROM_MIRROR)) return HISPARSE_EINVAL;
+  if (flags & ~(HISPARSE_RECORD_PLAN | HISPARSE_SKIP_IO | HISPARSE_FROM_MIRROR | HISPARSE_UNION))
+    return HISPARSE_EINVAL;
+  if ((flags & HISPARSE_UNION) && h->lookup == HISPARSE_LOOKUP_HASH) return HISPARSE_EINVAL;
   if (h->anchor_of[layer] != -1) return HISPARSE_EROLE;
   const LayerDev &Ld = h->layers[layer];
   const AnchorMeta &m = h->meta[layer];
@@ -2037,6 +2117,7 @@ int hisparse_resolve_ex(hisparse_handle *h, int32_t layer, const int32_t *d_sel,
     a.res_nblk = d_res_blocks ? res_max_blocks : 0;
     a.res_tok = d_res_blocks ? res_block_tokens : 1;
     a.sel_bt = sel_bt;
+    a.union_mode = (flags & HISPARSE_UNION) ? 1 : 0;
     a.P = h->P;
     a.sel = d_sel; a.num_reqs = d_num_reqs; a.newest = d_newest; a.out = d_out;
     a.slot_pos = m.slot_pos; a.lru = m.lru; a.page_table = m.page_table;
@@ -2046,7 +2127,7 @@ int hisparse_resolve_ex(hisparse_handle *h, int32_t layer, const int32_t *d_sel,
     a.src_req_stride = Ld.host_req_stride; a.src_row_stride = Ld.host_row_stride;
     a.hot = Ld.hot; a.hot_req_stride = Ld.hot_req_stride; a.hot_row_stride = Ld.hot_row_stride;
     lc.numAttrs = 2;  // cluster shape + programmatic dependent launch
-    if (d_res_blocks || sel_bt > 1)  // the extended instantiation
+    if (d_res_blocks || sel_bt > 1 || a.union_mode)  // the extended instantiation
       e = plan ? cudaLaunchKernelEx(&lc, resolve_pt_kernel<true, true>, a)
                : cudaLaunchKernelEx(&lc, resolve_pt_kernel<false, true>, a);
     else

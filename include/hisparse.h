@@ -65,6 +65,14 @@ extern "C" {
                                    rows keep stale bytes ([DD] §4.4, §5.6) */
 #define HISPARSE_FROM_MIRROR 4u /* copy missed rows from the layer's HBM mirror
                                    of the host pool instead of the host pool */
+#define HISPARSE_UNION 8u       /* speculative verification ([DD] §6.5): d_sel holds a
+                                   request's verify rows one after another (top_k
+                                   entries in all) and RESOLVE works on their union:
+                                   a position repeated anywhere is resolved at its
+                                   first reference and every reference outputs the
+                                   same row (no HISPARSE_ERR_DUP); misses take victims
+                                   in first-reference order and are fetched, counted
+                                   and planned once.  Page-table lookup only. */
 
 /* ---- lookup strategies (hisparse_config.lookup) ------------------------- */
 #define HISPARSE_LOOKUP_PAGE_TABLE 0

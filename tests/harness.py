@@ -103,7 +103,8 @@ class Run:
             nw = self.newest_np[t] if self.newest_np is not None else None
             out, _ = self.oracle[a].resolve(self.sel_np[t, gi], nw, num_reqs=nr, io=io,
                                             res_blocks=None if self.res_np is None else
-                                            self.res_np[t], res_tok=self.res_tok)
+                                            self.res_np[t], res_tok=self.res_tok,
+                                            union=bool(self.flags & H.UNION))
             self.oracle_out[gi, :nr] = out[:nr]
             for f in fl:
                 self.oracle[a].replay_into(self.oracle[f], num_reqs=nr)

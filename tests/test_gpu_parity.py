@@ -371,6 +371,58 @@ def test_block_selection_errors():
     hs.close(); mem.close()
 
 
+# ---------------------------------------------------------------------- #
+# Union mode: speculative verify rows resolved together                   #
+# ---------------------------------------------------------------------- #
+def _verify_row_traces(w, V):
+    """Verify rows of V draft tokens: the row for draft d at step t is the
+    top-k of step t + d of a trace with k / V selections per row, so rows
+    overlap as consecutive steps do (87 % reuse)."""
+    from workload.traces import all_traces
+    wr = w.scaled(k=w.k // V, steps=w.steps + V - 1, W_loc=min(w.W_loc, w.k // V // 4))
+    tr = all_traces(wr)
+    out = {}
+    for a, (sel, nw) in tr.items():
+        rows = np.concatenate([sel[d:d + w.steps] for d in range(V)], axis=-1)  # [T][R][k]
+        out[a] = (np.ascontiguousarray(rows), None if nw is None else nw[:w.steps])
+    return out
+
+
+@pytest.mark.parametrize("cs", [0, 1, 3])
+def test_union_verify_rows_small(cs):
+    w = get("dsa").scaled(R=3, groups=2, L_ctx=16384, steps=8, k=512, B=1024,
+                          write_through=False)
+    _run_all(w, traces=_verify_row_traces(w, 4), flags=H.UNION, ctas_per_request=cs)
+
+
+def test_union_verify_rows_full_size():
+    """8 requests x 4 layers, 4 verify rows of 512 selections (2048 in all), B=4096."""
+    w = get("dsa").scaled(write_through=False)
+    _run_all(w, every=4, traces=_verify_row_traces(w, 4), flags=H.UNION)
+
+
+def test_union_with_shared_layers_and_resident_tier():
+    w = get("shared").scaled(R=3, groups=2, L_ctx=8192, steps=6, k=512, B=1024)
+    _run_all(w, traces=_verify_row_traces(w, 2), flags=H.UNION,
+             resident=(resident_tables(w, 16, full=0, window=256), 16))
+
+
+def test_union_repeats_are_not_errors():
+    R, k, B, P = 2, 8, 16, 64
+    mem, hs = _instance(R, k, B, P)
+    out = torch.empty((R, k), dtype=torch.int32, device="cuda")
+    sel = np.array([[1, 2, 3, 3, 4, 1, -1, 2],
+                    [5, 5, 5, 5, 70, -1, -1, -1]], np.int32)     # 70 >= P: still an error
+    hs.resolve(0, _dev(sel), out, flags=H.UNION)
+    o = out.cpu().numpy()
+    assert o[0].tolist() == [0, 1, 2, 2, 3, 0, -1, 1]
+    assert (o[1] == -1).all()
+    flags, ue = hs.status()
+    assert flags == H.ERR_RANGE and ue[0].tolist() == [0, H.ERR_RANGE]
+    assert hs.export_state(0)[3].tolist() == [4, 0]
+    hs.close(); mem.close()
+
+
 def test_import_rejects_inconsistent_state():
     mem, hs = _instance(1, 2, 4, 16)
     sp = np.array([[3, -1, 5, -1]], np.int32)

@@ -53,6 +53,9 @@ def parse():
                     help="FULL,WINDOW,TOKENS: three-tier resolve with the first FULL requests "
                          "resident over their whole context and the others over their last "
                          "WINDOW positions, TOKENS positions per resident block")
+    ap.add_argument("--verify-rows", type=int, default=1,
+                    help="V > 1: each request's list is V speculative verify rows of top_k / V "
+                         "selections, resolved as one union (HISPARSE_UNION)")
     ap.add_argument("--mirror", action="store_true",
                     help="fetch missed records from an HBM mirror of the host pool "
                          "(FROM_MIRROR): the same kernels with HBM as the source; the "
@@ -176,7 +179,7 @@ def token_traces(w, traces):
     return out
 
 
-def cpu_oracle_rate(w, traces, host_views=None, budget_s=10.0):
+def cpu_oracle_rate(w, traces, host_views=None, budget_s=10.0, union=False):
     """The C oracle (single thread) on the same workload's steps: selections/s.
 
     ``host_views[l]`` is a uint8 [R][>=L_ctx][rec] view of layer l's host rows
@@ -213,7 +216,7 @@ def cpu_oracle_rate(w, traces, host_views=None, budget_s=10.0):
                 layers[l].set_newest_rows(new_rows[t, l])
         for a in anchors:
             nw = traces[a][1][t] if w.write_through else None
-            layers[a].resolve(traces[a][0][t], nw)
+            layers[a].resolve(traces[a][0][t], nw, union=union)
             miss_bytes += int(layers[a].miss_count.sum()) * w.rec
             for f in (l for l in range(w.L) if anchor_of[l] == a):
                 layers[a].replay_into(layers[f])
@@ -231,7 +234,7 @@ def cpu_oracle_rate(w, traces, host_views=None, budget_s=10.0):
             "steps": steps_done}
 
 
-def cpu_oracle_rate_threads(w, traces, host_views, threads):
+def cpu_oracle_rate_threads(w, traces, host_views, threads, union=False):
     """The same C oracle over all decode steps, with the workload's independent
     units -- one request of one anchor layer, with its shared-index layers --
     spread over `threads` Python threads (each oracle call releases the GIL)."""
@@ -264,7 +267,7 @@ def cpu_oracle_rate_threads(w, traces, host_views, threads):
                             lay.writeback(traces[anchors[0]][1][t - 1][r:r + 1])
                         lay.set_newest_rows(new_rows[t, l, r:r + 1])
                 nw = traces[a][1][t][r:r + 1] if w.write_through else None
-                o.resolve(traces[a][0][t][r:r + 1], nw)
+                o.resolve(traces[a][0][t][r:r + 1], nw, union=union)
                 misses += int(o.miss_count.sum())
                 for _, lay in fls:
                     o.replay_into(lay)
@@ -365,7 +368,11 @@ def run_ours(args):
     anchor_of = w.anchor_of()
     groups = [(a, [l for l in range(w.L) if anchor_of[l] == a]) for a in w.anchors()]
     G = len(groups)
-    traces = all_traces(w)
+    if args.verify_rows > 1:   # speculative verify rows, resolved as one union list
+        from workload.traces import verify_row_traces
+        traces = verify_row_traces(w, args.verify_rows)
+    else:
+        traces = all_traces(w)
     sel_np = np.stack([traces[a][0] for a, _ in groups], axis=1)       # [T][G][R][k]
     sel = torch.from_numpy(sel_np).to(dev)
     newest = newest_np = None
@@ -380,7 +387,9 @@ def run_ours(args):
         wb = torch.from_numpy(wbn).to(dev)
         new_rows = torch.from_numpy(REC.new_token_records(w)).to(dev)
     out = torch.full((G, w.R, w.k), -1, dtype=torch.int32, device=dev)
-    runner = DecodeStep(hs, mem, groups, flags=H.FROM_MIRROR if args.mirror else 0,
+    runner = DecodeStep(hs, mem, groups,
+                        flags=(H.FROM_MIRROR if args.mirror else 0) |
+                        (H.UNION if args.verify_rows > 1 else 0),
                         fused=not args.unfused, sel_block_tokens=w.sel_block_tokens)
     miss_hist = torch.zeros((T, G, w.R), dtype=torch.int32, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)     # > 129 MB L2
@@ -547,7 +556,7 @@ def run_ours(args):
     flags, _ = hs.status()
 
     verify = None
-    if args.verify and not args.resident and w.sel_block_tokens == 1:
+    if args.verify and not args.resident and w.sel_block_tokens == 1 and args.verify_rows == 1:
         verify = verify_against_oracle(w, hs, mem, groups, traces, args.warmup + args.steps)
 
     # ---- pass 2 (per-kernel durations for the roofline): the same steps from
@@ -640,7 +649,8 @@ def run_ours(args):
                 for gi, (a, _) in enumerate(groups):
                     hs.resolve_ex(a, sel[t_last, gi], out[gi], None,
                                   newest[t_last] if newest is not None else None,
-                                  sel_block_tokens=w.sel_block_tokens, flags=H.SKIP_IO,
+                                  sel_block_tokens=w.sel_block_tokens,
+                                  flags=H.SKIP_IO | (H.UNION if args.verify_rows > 1 else 0),
                                   stream=torch.cuda.current_stream())
         torch.cuda.synchronize()
         hit_ms = []
@@ -777,10 +787,11 @@ def run_ours(args):
     if rank == 0 and not args.no_cpu and not args.resident:
         views = {l: mem.host_view(l) for l in range(w.L)}
         ttr = token_traces(w, traces)
-        cpu = cpu_oracle_rate(w, ttr, host_views=views, budget_s=20.0)
+        uni = args.verify_rows > 1
+        cpu = cpu_oracle_rate(w, ttr, host_views=views, budget_s=20.0, union=uni)
         cpu.pop("seconds", None)
         cpu.pop("steps", None)
-        cpu_mt = cpu_oracle_rate_threads(w, ttr, views, os.cpu_count() or 1)
+        cpu_mt = cpu_oracle_rate_threads(w, ttr, views, os.cpu_count() or 1, union=uni)
         cpu_mt.pop("seconds", None)
 
     hp_frac_end = mem.pool.hugepage_fraction()
@@ -803,6 +814,7 @@ def run_ours(args):
                        "write_through_launch": "separate" if args.unfused else "fused into RESOLVE",
                        "host_pool": args.pool,
                        "fetch_source": "HBM mirror of the host pool" if args.mirror else "host pool",
+                       "verify_rows": args.verify_rows,
                        "resident_tier": (dict(zip(("full_requests", "window", "tokens_per_block"),
                                                   (int(x) for x in args.resident.split(","))))
                                          if args.resident else None),

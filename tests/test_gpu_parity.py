@@ -375,17 +375,8 @@ def test_block_selection_errors():
 # Union mode: speculative verify rows resolved together                   #
 # ---------------------------------------------------------------------- #
 def _verify_row_traces(w, V):
-    """Verify rows of V draft tokens: the row for draft d at step t is the
-    top-k of step t + d of a trace with k / V selections per row, so rows
-    overlap as consecutive steps do (87 % reuse)."""
-    from workload.traces import all_traces
-    wr = w.scaled(k=w.k // V, steps=w.steps + V - 1, W_loc=min(w.W_loc, w.k // V // 4))
-    tr = all_traces(wr)
-    out = {}
-    for a, (sel, nw) in tr.items():
-        rows = np.concatenate([sel[d:d + w.steps] for d in range(V)], axis=-1)  # [T][R][k]
-        out[a] = (np.ascontiguousarray(rows), None if nw is None else nw[:w.steps])
-    return out
+    from workload.traces import verify_row_traces
+    return verify_row_traces(w, V)
 
 
 @pytest.mark.parametrize("cs", [0, 1, 3])

@@ -152,3 +152,18 @@ def all_traces(w):
                       sel_block_tokens=1)
         return {l: layer_traces(wb, l) for l in w.anchors()}
     return {l: layer_traces(w, l) for l in w.anchors()}
+
+
+def verify_row_traces(w, V):
+    """Speculative verify rows: {anchor: (sel [steps][R][k], newest)} where each
+    request's list is V rows of k / V selections, the row of draft token d at
+    step t being the top-k of step t + d of a trace with k / V selections per
+    step (so rows overlap as consecutive decode steps do).  The local window is
+    capped at a quarter of a row."""
+    import numpy as np
+    wr = w.scaled(k=w.k // V, steps=w.steps + V - 1, W_loc=min(w.W_loc, w.k // V // 4))
+    out = {}
+    for a, (sel, nw) in all_traces(wr).items():
+        rows = np.concatenate([sel[d:d + w.steps] for d in range(V)], axis=-1)
+        out[a] = (np.ascontiguousarray(rows), None if nw is None else nw[:w.steps])
+    return out

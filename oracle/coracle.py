@@ -120,6 +120,33 @@ class OracleLayer:
         for rr in (range(self.R) if r is None else [r]):
             self._lib.hso_reset_unit(ctypes.byref(self._s), rr)
 
+    def admit(self, r, n, io=True):
+        """Admission of unit r with its first n positions preloaded (reading
+        R16 of oracle/tiny.py: the state resolving positions 0..n-1 in order
+        from the reset state gives), as consecutive lists of k."""
+        if not 0 <= n <= min(self.B, self.P):
+            raise ValueError("preload length outside [0, min(B, P)]")
+        self._lib.hso_reset_unit(ctypes.byref(self._s), r)
+        out = np.empty(self.k, np.int32)
+        pos, cnt = [], 0
+        for c0 in range(0, n, self.k):
+            chunk = np.full(self.k, -1, np.int32)
+            m = min(n, c0 + self.k) - c0
+            chunk[:m] = np.arange(c0, c0 + m, dtype=np.int32)
+            e = self._lib.hso_resolve_unit(ctypes.byref(self._s), r, _p(chunk), -1,
+                                           int(bool(io)), _p(out))
+            assert e == 0
+            cnt += int(self.plan_count[r])
+        self.miss_count[r] = 0
+        self.plan_count[r] = 0
+        return cnt
+
+    def preload_bytes(self, r, n):
+        """A shared-index layer's side of an admission: its slots move in
+        lockstep with the anchor's, so slot s < n holds its own host row s."""
+        for s in range(n):
+            self.hot[r, s] = self._host_keep[r, s] if s < self.host_split else self.host_tail[r, s - self.host_split]
+
     def resolve(self, sel, newest=None, num_reqs=None, io=True, res_blocks=None, res_tok=1,
                 union=False):
         """sel int32 [R][k]; newest int32 [R] or None; res_blocks int32

@@ -188,6 +188,33 @@ class Unit:
         return out, plan, 0
 
     # ------------------------------------------------------------------ #
+    def admit(self, n, k=None):
+        """Admission of a request (gentlecold.top §5.3, direct admission:
+        a long request starts with every token marked absent -- the reset
+        state, n = 0 -- and a short one, host length <= the buffer, is
+        preloaded).  Reading R16: preloading the first ``n`` positions gives
+        the state that resolving positions 0, 1, ..., n-1 in order from the
+        reset state gives, whether in one list or in consecutive lists of
+        ``k``: slot s holds position s, and the LRU order is the empty slots
+        (ascending) followed by the preloaded ones (ascending)."""
+        B = self.B
+        if not 0 <= n <= min(B, self.P):
+            raise ValueError("preload length outside [0, min(B, P)]")
+        self.slot_pos = [-1] * B
+        self.lru = list(range(B))
+        self.page_table = {}
+        self.hot = [None] * (B + 1)
+        self.miss_count = 0
+        k = k or max(1, n)
+        plan = []
+        for c0 in range(0, n, k):
+            chunk = list(range(c0, min(n, c0 + k)))
+            out, pl, err = self.resolve(chunk + [-1] * (k - len(chunk)))
+            assert err == 0
+            plan += pl
+        self.miss_count = 0                # an admission is not a decode step
+        return plan
+
     def set_newest(self, record):
         """The caller writes the new token's KV into row B ([P1] §3.4 step 4)."""
         self.hot[self.B] = record

@@ -347,3 +347,41 @@ def test_block_selection_resolves_like_its_positions():
     assert err == 0 and u.miss_count == 8 and sorted(p for p, _ in plan) == list(range(8, 12)) + list(range(28, 32))
     out, plan, err = u.resolve(expand_blocks([7, -3], 4))
     assert err == ERR_RANGE and out == [-1] * 8
+
+
+# ---------------------------------------------------------------------- #
+# Admission with preload (reading R16)                                     #
+# ---------------------------------------------------------------------- #
+@pytest.mark.parametrize("k", [1, 3, 8])
+def test_admit_closed_form(k):
+    """Preloading n positions: slot s holds position s, LRU = empties then the
+    preloaded slots, bytes equal the host rows -- for any list length used to
+    get there; n = 0 is the reset state."""
+    B, P = 8, 20
+    host = lambda p: bytes([p] * 4)  # noqa: E731
+    for n in range(0, B + 1):
+        u = Unit(B, P, k=k, host=host)
+        u.resolve([5] + [-1] * (k - 1))               # some prior state
+        plan = u.admit(n, k=k)
+        assert u.slot_pos == list(range(n)) + [-1] * (B - n)
+        assert u.lru == list(range(n, B)) + list(range(n))
+        assert u.page_table == {s: s for s in range(n)} and u.miss_count == 0
+        assert [u.hot[s] for s in range(n)] == [host(s) for s in range(n)]
+        assert sorted(plan) == [(s, s) for s in range(n)]
+
+
+def test_admit_c_equals_python():
+    from oracle.coracle import OracleLayer
+    R, k, B, P, rec = 3, 4, 12, 40, 8
+    host = np.random.default_rng(3).integers(0, 256, size=(R, P, rec), dtype=np.uint8)
+    c = OracleLayer(R, k, B, P, rec, host=host)
+    c.reset()
+    c.resolve(np.array([[1, 2, 3, 4]] * R, np.int32))
+    for r, n in enumerate([0, 7, 12]):
+        c.admit(r, n)
+        u = Unit(B, P, k=k, host=lambda p, r=r: bytes(host[r, p]))
+        u.admit(n, k=k)
+        assert list(c.slot_pos[r]) == u.slot_pos and list(c.lru[r]) == u.lru
+        assert c.miss_count[r] == 0
+        for s in range(n):
+            assert bytes(c.hot[r, s]) == u.hot[s]

@@ -1569,6 +1569,79 @@ __global__ void reset_kernel(int32_t *slot_pos, int16_t *lru, int64_t n_units, i
   }
 }
 
+// ---------------------------------------------------------------------------
+// Admission ([DD] §5.3, direct admission): listed requests go to the reset
+// state; a short request's first n positions are preloaded into slots 0..n-1
+// in order, the state that resolving positions 0..n-1 in order from the reset
+// state gives (slot s holds position s; LRU: empty slots, then the preloaded
+// ones).  Grid (listed requests, C): block (i, c) does the c-th share of the
+// request's page table and of its preload copy.
+// ---------------------------------------------------------------------------
+struct AdmitArgs {
+  const int32_t *reqs, *preload;
+  int32_t R, B, rec16;
+  int64_t P;
+  int32_t *slot_pos;  // metadata of a RESOLVE layer; NULL for a shared-index layer
+  int16_t *lru;
+  int32_t *page_table, *miss_count, *unit_err, *plan_count;
+  uint32_t *status;
+  const char *src;
+  int64_t src_req_stride, src_row_stride;
+  char *hot;
+  int64_t hot_req_stride, hot_row_stride;
+};
+constexpr int kAdmitThreads = 256;
+
+__global__ void __launch_bounds__(kAdmitThreads) admit_kernel(const AdmitArgs a) {
+  const int i = blockIdx.x, c = blockIdx.y, C = gridDim.y, tid = threadIdx.x;
+  const int r = a.reqs[i];
+  const int n = a.preload ? a.preload[i] : 0;
+  if (r < 0 || r >= a.R || n < 0 || n > a.B || n > a.P) {
+    if (c == 0 && tid == 0) atomicOr(a.status, HISPARSE_ERR_RANGE);
+    return;
+  }
+  if (a.slot_pos) {
+    int32_t *pt = a.page_table + static_cast<int64_t>(r) * a.P;
+    for (int64_t p = static_cast<int64_t>(c) * kAdmitThreads + tid; p < a.P;
+         p += static_cast<int64_t>(C) * kAdmitThreads)
+      pt[p] = p < n ? static_cast<int32_t>(p) : -1;
+    if (c == 0) {
+      int32_t *sp = a.slot_pos + static_cast<int64_t>(r) * a.B;
+      int16_t *lru = a.lru + static_cast<int64_t>(r) * a.B;
+      for (int s = tid; s < a.B; s += kAdmitThreads) {
+        sp[s] = s < n ? s : -1;
+        lru[s] = static_cast<int16_t>(s < a.B - n ? n + s : s - (a.B - n));
+      }
+      if (tid == 0) {
+        a.miss_count[r] = 0;
+        a.unit_err[r] = 0;
+        a.plan_count[r] = 0;
+      }
+    }
+  }
+  const char *src = a.src + static_cast<int64_t>(r) * a.src_req_stride;
+  char *dst = a.hot + static_cast<int64_t>(r) * a.hot_req_stride;
+  const int64_t total = static_cast<int64_t>(n) * a.rec16;
+  const int64_t T = static_cast<int64_t>(C) * kAdmitThreads;
+  for (int64_t b0 = static_cast<int64_t>(c) * kAdmitThreads + tid; b0 < total; b0 += T * kUnroll) {
+    uint4 v[kUnroll];
+    char *d[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t q = b0 + u * T;
+      d[u] = nullptr;
+      if (q < total) {
+        const int64_t s = q / a.rec16, o = q - s * a.rec16;
+        v[u] = ld_nc_v4(src + s * a.src_row_stride + 16 * o);
+        d[u] = dst + s * a.hot_row_stride + 16 * o;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+      if (d[u]) st_v4(d[u], v[u]);
+  }
+}
+
 }  // namespace
 
 // ===========================================================================
@@ -1998,6 +2071,32 @@ int hisparse_reset(hisparse_handle *h, int32_t layer, void *stream) {
     const int64_t n = static_cast<int64_t>(h->R) * h->B;
     const int grid = static_cast<int>(std::min<int64_t>((n + 255) / 256, 4096));
     reset_kernel<<<grid, 256, 0, s>>>(m.slot_pos, m.lru, h->R, h->B);
+    HS_CUDA(cudaGetLastError());
+  }
+  return HISPARSE_OK;
+}
+
+int hisparse_admit(hisparse_handle *h, int32_t layer, const int32_t *d_reqs, int32_t n,
+                   const int32_t *d_preload, void *stream) {
+  if (!h || !d_reqs || n < 0) return HISPARSE_EINVAL;
+  if (layer != -1 && layer_ok(h, layer)) return HISPARSE_EINVAL;
+  if (n == 0) return HISPARSE_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int l = 0; l < h->L; ++l) {
+    if (layer != -1 && l != layer) continue;
+    const LayerDev &Ld = h->layers[l];
+    AdmitArgs a = {};
+    a.reqs = d_reqs; a.preload = d_preload;
+    a.R = h->R; a.B = h->B; a.rec16 = h->rec / 16; a.P = h->P;
+    if (h->anchor_of[l] == -1) {
+      const AnchorMeta &m = h->meta[l];
+      a.slot_pos = m.slot_pos; a.lru = m.lru; a.page_table = m.page_table;
+      a.miss_count = m.miss_count; a.unit_err = m.unit_err; a.plan_count = m.plan_count;
+    }
+    a.status = h->d_status;
+    a.src = Ld.host; a.src_req_stride = Ld.host_req_stride; a.src_row_stride = Ld.host_row_stride;
+    a.hot = Ld.hot; a.hot_req_stride = Ld.hot_req_stride; a.hot_row_stride = Ld.hot_row_stride;
+    admit_kernel<<<dim3(static_cast<unsigned>(n), 16), kAdmitThreads, 0, s>>>(a);
     HS_CUDA(cudaGetLastError());
   }
   return HISPARSE_OK;

@@ -48,6 +48,7 @@ SIGNATURES = [
     ("hisparse_resolve_resident", _i32, [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _vp,
                                          _u32, _vp]),
     ("hisparse_resolve_ex", _i32, [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _u32, _vp]),
+    ("hisparse_admit", _i32, [_vp, _i32, _vp, _i32, _vp, _vp]),
     ("hisparse_writeback", _i32, [_vp, _i32, _vp, _vp, _vp, _vp]),
     ("hisparse_prefetch_plan", _i32, [_vp, _i32, _i32, _vp, _vp]),
     ("hisparse_copy_miss_counts", _i32, [_vp, _i32, _vp, _vp]),
@@ -205,3 +206,7 @@ def hisparse_host_hugepage_bytes(p, nbytes):
     v = ctypes.c_size_t()
     rc = load().hisparse_host_hugepage_bytes(p, nbytes, ctypes.byref(v))
     return rc, v.value
+
+
+def hisparse_admit(h, layer, d_reqs, n, d_preload, stream):
+    return load().hisparse_admit(h, layer, d_reqs, n, d_preload, stream)

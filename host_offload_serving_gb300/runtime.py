@@ -118,6 +118,13 @@ class HiSparse:
         H.check(H.hisparse_resolve_ex(self.h, layer, _ptr(sel), _ptr(num_reqs), _ptr(newest), o,
                                       _ptr(out), flags, _stream(stream)), "hisparse_resolve_ex")
 
+    def admit(self, layer, reqs, preload=None, stream=None):
+        """Reset the listed requests (device int32 [n]) of ``layer`` (-1: all)
+        and preload the first ``preload[i]`` positions of each (device int32
+        [n], or None for none)."""
+        H.check(H.hisparse_admit(self.h, layer, _ptr(reqs), int(reqs.numel()), _ptr(preload),
+                                 _stream(stream)), "hisparse_admit")
+
     def writeback(self, layer, pos, num_reqs=None, stream=None, new_rows=None):
         H.check(H.hisparse_writeback(self.h, layer, _ptr(pos), _ptr(new_rows), _ptr(num_reqs),
                                      _stream(stream)), "hisparse_writeback")

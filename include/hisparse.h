@@ -251,6 +251,22 @@ int hisparse_resolve_resident(hisparse_handle *h, int32_t layer, const int32_t *
                               int32_t res_block_tokens, int32_t *d_out, uint32_t flags,
                               void *stream);
 
+/* Admission of requests into the cache ([DD] §5.3, direct admission: a long
+ * request starts with every token absent and misses everything on its first
+ * step; a short one, whose host length fits the buffer, is preloaded).  For
+ * i < n, request d_reqs[i] (device int32 [n]) of `layer` (-1: every layer)
+ * goes to the reset state, and, when d_preload (device int32 [n]) is given,
+ * its first d_preload[i] positions are copied from the layer's host pool into
+ * slots 0 .. d_preload[i]-1: slot s holds position s and the LRU order is the
+ * empty slots then the preloaded ones -- the state that resolving positions
+ * 0, 1, ... in order from the reset state gives.  Shared-index layers get the
+ * bytes (their slots move with the anchor's).  An entry outside [0, R), or a
+ * preload outside [0, min(B, P)], sets HISPARSE_ERR_RANGE and is skipped; a
+ * request listed twice gives unspecified contents.  Graph-capturable; order
+ * it between decode steps.  Errors: EINVAL, ECUDA. */
+int hisparse_admit(hisparse_handle *h, int32_t layer, const int32_t *d_reqs, int32_t n,
+                   const int32_t *d_preload, void *stream);
+
 /* Write-through of the newest row ([DD] §3.4 step 4, §5.4 eager backup):
  * for r < *d_num_reqs with d_pos[r] >= 0, copy hot row B of (layer, r) to
  * host row d_pos[r] of (layer, r); then, if d_new_rows is not NULL, place the

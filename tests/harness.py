@@ -109,6 +109,20 @@ class Run:
             for f in fl:
                 self.oracle[a].replay_into(self.oracle[f], num_reqs=nr)
 
+    def admit(self, reqs, preload):
+        """Admit requests on every layer: GPU through hisparse_admit, oracle
+        through its admission (anchors) and the lockstep bytes (shared)."""
+        dev = self.out.device
+        self.hs.admit(-1, torch.tensor(reqs, dtype=torch.int32, device=dev),
+                      torch.tensor(preload, dtype=torch.int32, device=dev))
+        anchor_of = self.w.anchor_of()
+        for l, o in self.oracle.items():
+            for r, n in zip(reqs, preload):
+                if anchor_of[l] < 0:
+                    o.admit(r, n)
+                else:
+                    o.preload_bytes(r, n)
+
     def step(self):
         self.gpu_step(self.t)
         self.oracle_step(self.t)

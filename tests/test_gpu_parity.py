@@ -414,6 +414,50 @@ def test_union_repeats_are_not_errors():
     hs.close(); mem.close()
 
 
+# ---------------------------------------------------------------------- #
+# Admission with preload                                                   #
+# ---------------------------------------------------------------------- #
+@pytest.mark.parametrize("name", ["shared", "dsa"])
+def test_admit_between_steps(name):
+    """Requests admitted mid-run (one preloaded, one direct with nothing
+    preloaded, one preloaded to the full buffer) then decoded: every field
+    equals the oracle's after the admission and after each later step."""
+    w = get(name).scaled(R=4, groups=2, L_ctx=8192, steps=8, k=256, B=512)
+    run = Run(w)
+    try:
+        for t in range(3):
+            run.step()
+        run.admit([1, 3, 0], [300, 0, 512])
+        run.compare()
+        for t in range(3, w.steps):
+            run.step()
+            run.compare()
+    finally:
+        run.close()
+
+
+def test_admit_rejects_bad_entries():
+    R, k, B, P = 3, 4, 8, 64
+    mem, hs = _instance(R, k, B, P)
+    out = torch.empty((R, k), dtype=torch.int32, device="cuda")
+    hs.resolve(0, _dev(np.array([[1, 2, 3, 4]] * R, np.int32)), out)
+    before = hs.export_state(0)
+    hs.admit(0, _dev(np.array([5, 1], np.int32)), _dev(np.array([2, 9], np.int32)))
+    flags, _ = hs.status()
+    assert flags == H.ERR_RANGE                      # request 5 >= R, preload 9 > B
+    after = hs.export_state(0)
+    for x, y in zip(before[:3], after[:3]):
+        np.testing.assert_array_equal(x, y)
+    hs.admit(0, _dev(np.array([2], np.int32)), _dev(np.array([3], np.int32)))
+    sp, lru, pt, mc = hs.export_state(0)
+    assert sp[2].tolist() == [0, 1, 2, -1, -1, -1, -1, -1]
+    assert lru[2].tolist() == [3, 4, 5, 6, 7, 0, 1, 2] and mc[2] == 0
+    assert pt[2, :4].tolist() == [0, 1, 2, -1] and (pt[2, 4:] == -1).all()
+    host = mem.host_view(0)
+    np.testing.assert_array_equal(mem.hot[0, 2, :3].cpu().numpy(), host[2, :3])
+    hs.close(); mem.close()
+
+
 def test_import_rejects_inconsistent_state():
     mem, hs = _instance(1, 2, 4, 16)
     sp = np.array([[3, -1, 5, -1]], np.int32)

@@ -759,6 +759,35 @@ def run_ours(args):
             "launch_us_p50_p90_p99_max": [round(pct(0.5), 2), round(pct(0.9), 2),
                                           round(pct(0.99), 2), round(srt[-1] * 1e3, 2)],
             "writeback_us_avg": round(1e3 * sum(wb_ms) / len(wb_ms), 2) if wb_ms else None}
+    # ---- admission: every request of every layer reset with its first
+    #      min(B, P) positions preloaded (the short-request path of direct
+    #      admission), and reset alone (the long-request path) ----
+    admission = None
+    if not args.no_allhit:
+        reqs_d = torch.arange(w.R, dtype=torch.int32, device=dev)
+        npre = min(w.B, w.P)
+        pre_d = torch.full((w.R,), npre, dtype=torch.int32, device=dev)
+        ms_pre, ms_rst = [], []
+        for i in range(5):
+            for pre, acc in ((pre_d, ms_pre), (None, ms_rst)):
+                flush.fill_(i)
+                a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a0.record(cur)
+                hs.admit(-1, reqs_d, pre, stream=cur)
+                a1.record(cur)
+                torch.cuda.synchronize()
+                acc.append(a0.elapsed_time(a1))
+        ab = w.R * w.L * npre * w.rec
+        t_pre = sorted(ms_pre)[len(ms_pre) // 2]
+        admission = {"preload_positions": npre, "bytes": ab,
+                     "us_preload_all": round(t_pre * 1e3, 1),
+                     "preload_gbs": round(ab / (t_pre / 1e3) / 1e9, 2),
+                     "preload_frac_of_link": round(ab / (t_pre / 1e3) / 1e9 / h2d_gbs, 4),
+                     "us_reset_all": round(sorted(ms_rst)[len(ms_rst) // 2] * 1e3, 1),
+                     "timing": "hisparse_admit of every request on every layer, median of 5, "
+                               "L2 flushed before each"}
+        flags |= hs.status()[0]
+
     # step 0 from the admission state: every selection but the newest misses,
     # so each launch moves R x k records -- the fetch path at full size
     cold = None
@@ -830,6 +859,7 @@ def run_ours(args):
             "us_per_layer_step": round(launch_ms * 1e3, 2),
             "all_hit_no_io": allhit,
             "cold_step0": cold,
+            "admission": admission,
             "replay": replay,
             "e2e": e2e,
             "cpu_baseline": cpu,

@@ -56,6 +56,10 @@ def parse():
     ap.add_argument("--verify-rows", type=int, default=1,
                     help="V > 1: each request's list is V speculative verify rows of top_k / V "
                          "selections, resolved as one union (HISPARSE_UNION)")
+    ap.add_argument("--interleave", action="store_true",
+                    help="host rows of each shared-index group (anchor + followers) "
+                         "interleaved row by row, so replays read the pages the anchor's "
+                         "fetch just read")
     ap.add_argument("--mirror", action="store_true",
                     help="fetch missed records from an HBM mirror of the host pool "
                          "(FROM_MIRROR): the same kernels with HBM as the source; the "
@@ -345,8 +349,9 @@ def run_ours(args):
 
     t_setup = time.perf_counter()
     mem = WorkloadMemory(w.R, w.L, w.B, w.P, w.rec, mirror=args.mirror,
-                         pool_kind=H.HOST_HUGE if args.pool == "huge" else H.HOST_PINNED)
-    REC.fill_host_pool(w, mem.pool.ptr, mem.layer_stride, mem.req_stride)
+                         pool_kind=H.HOST_HUGE if args.pool == "huge" else H.HOST_PINNED,
+                         group=(1 + w.followers) if args.interleave else 1)
+    REC.fill_host_pool(w, mem.geometry)
     if args.mirror:
         mem.fill_mirror()
     hs = HiSparse(w.R, w.L, w.k, w.B, w.P, w.rec, mem.layer_buffers(), anchor_of=w.anchor_of(),
@@ -842,6 +847,8 @@ def run_ours(args):
                        "lookup": ["page_table", "hash"][info["lookup"]],
                        "write_through_launch": "separate" if args.unfused else "fused into RESOLVE",
                        "host_pool": args.pool,
+                       "host_layout": ("rows of each shared-index group interleaved"
+                                       if args.interleave else "one block of rows per layer"),
                        "fetch_source": "HBM mirror of the host pool" if args.mirror else "host pool",
                        "verify_rows": args.verify_rows,
                        "resident_tier": (dict(zip(("full_requests", "window", "tokens_per_block"),

@@ -185,39 +185,63 @@ class HiSparse:
 class WorkloadMemory:
     """Host pools, hot buffers and optional HBM mirrors for a workload.
 
-    Host pool of layer l: ``pool + l*layer_stride``, rows [R][P][rec].
+    Host pools: one pinned allocation.  With ``group = 1`` layer l's rows are
+    ``[R][P][rec]`` at ``pool + l*layer_stride``.  With ``group = m > 1``
+    (shared-index groups of m layers: an anchor and its followers) the m
+    layers of a group are interleaved row by row, ``[L/m][R][P][m][rec]``, so
+    a position's records for the whole group are adjacent and a follower's
+    replay reads the same host pages as its anchor's fetch just did.  The
+    RESOLVE calls see only each layer's base and strides.
     Hot buffer of layer l: ``hot[l]`` (uint8 [R][B+1][rec], device).
     """
 
-    def __init__(self, R, L, B, P, rec, device="cuda", mirror=False, pool_kind=H.HOST_PINNED):
-        self.R, self.L, self.B, self.P, self.rec = R, L, B, P, rec
-        self.req_stride = P * rec
-        self.layer_stride = R * P * rec
+    def __init__(self, R, L, B, P, rec, device="cuda", mirror=False, pool_kind=H.HOST_PINNED,
+                 group=1):
+        if L % group:
+            raise ValueError("the layer count must be a multiple of the group size")
+        self.R, self.L, self.B, self.P, self.rec, self.group = R, L, B, P, rec, group
+        self.req_stride = P * rec * group
+        self.row_stride = rec * group
+        self.layer_stride = R * P * rec            # bytes of one layer's rows
         self.pool = HostPool(L * self.layer_stride, kind=pool_kind)
         self.hot = torch.zeros((L, R, B + 1, rec), dtype=torch.uint8, device=device)
         self.mirror = None
         if mirror:
             self.mirror = torch.empty((L, R, P, rec), dtype=torch.uint8, device=device)
 
+    def layer_offset(self, layer):
+        """Byte offset of layer ``layer``'s row (0, 0) in the pool."""
+        g, j = divmod(layer, self.group)
+        return g * self.group * self.layer_stride + j * self.rec
+
+    def geometry(self, layer):
+        """(address of row (0, 0), request stride, row stride) of a layer."""
+        return self.pool.ptr + self.layer_offset(layer), self.req_stride, self.row_stride
+
     def host_view(self, layer):
-        """numpy uint8 [R][P][rec] view of one layer's host pool."""
+        """numpy uint8 [R][P][rec] view of one layer's host rows."""
         a = self.pool.numpy()
-        return a[layer * self.layer_stride:(layer + 1) * self.layer_stride].reshape(
-            self.R, self.P, self.rec)
+        return np.lib.stride_tricks.as_strided(
+            a[self.layer_offset(layer):], shape=(self.R, self.P, self.rec),
+            strides=(self.req_stride, self.row_stride, 1), writeable=True)
 
     def layer_buffers(self):
         out = []
         for l in range(self.L):
+            base, rs, ws = self.geometry(l)
             out.append(H.LayerBuffers(
-                self.pool.ptr + l * self.layer_stride, self.req_stride, self.rec,
-                self.hot[l].data_ptr(), (self.B + 1) * self.rec, self.rec,
+                base, rs, ws, self.hot[l].data_ptr(), (self.B + 1) * self.rec, self.rec,
                 self.mirror[l].data_ptr() if self.mirror is not None else None))
         return out
 
     def fill_mirror(self):
         """Copy the host pool into the HBM mirror (pinned -> device)."""
-        src = torch.from_numpy(self.pool.numpy()).view(self.L, self.R, self.P, self.rec)
-        self.mirror.copy_(src, non_blocking=False)
+        if self.group == 1:
+            src = torch.from_numpy(self.pool.numpy()).view(self.L, self.R, self.P, self.rec)
+            self.mirror.copy_(src, non_blocking=False)
+        else:
+            for l in range(self.L):
+                self.mirror[l].copy_(torch.from_numpy(np.ascontiguousarray(self.host_view(l))))
 
     def close(self):
         self.pool.close()

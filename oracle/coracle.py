@@ -42,7 +42,7 @@ class _Layer(ctypes.Structure):
         ("plan_count", ctypes.c_void_p), ("mark", ctypes.c_void_p),
         ("mark_gen", ctypes.c_int32), ("hit", ctypes.c_void_p),
         ("misses", ctypes.c_void_p), ("ev", ctypes.c_void_p),
-        ("first", ctypes.c_void_p),
+        ("first", ctypes.c_void_p), ("host_row_stride", ctypes.c_int64),
     ]
 
 
@@ -88,9 +88,13 @@ class OracleLayer:
         self.R, self.k, self.B, self.P, self.rec = R, k, B, P, rec
         self.host_split = P if host_split is None else host_split
         self._host_keep = host
+        host_row_stride = 0
         if host is not None:
             host_ptr = host.ctypes.data
             host_req_stride = host.strides[0]
+            host_row_stride = host.strides[1]
+            if host.strides[2] != 1:
+                raise ValueError("host rows must be contiguous bytes")
         m = metadata
         self.slot_pos = np.full((R, B), -1, np.int32) if m else None
         self.lru = np.tile(np.arange(B, dtype=np.int16), (R, 1)) if m else None
@@ -113,7 +117,8 @@ class OracleLayer:
                          ctypes.c_void_p(host_ptr) if host_ptr else None, host_req_stride,
                          self.host_split, _p(self.host_tail), _p(self.plan_pos),
                          _p(self.plan_slot), _p(self.plan_count), _p(self._mark), 0,
-                         _p(self._hit), _p(self._misses), _p(self._ev), _p(self._first))
+                         _p(self._hit), _p(self._misses), _p(self._ev), _p(self._first),
+                         host_row_stride)
         self._lib = _load()
 
     def reset(self, r=None):

@@ -59,7 +59,7 @@ typedef struct {
   /* host pool: rows [0, host_split) read from `host` (shared, read-only);
      rows [host_split, P) live in `host_tail`, which this model owns and
      updates on write-back. */
-  const uint8_t *host;       /* row (r, p) at host + r*host_req_stride + p*rec */
+  const uint8_t *host;       /* row (r, p) at host + r*host_req_stride + p*host_row_stride */
   int64_t host_req_stride;
   int64_t host_split;
   uint8_t *host_tail;        /* [R][P - host_split][rec] or NULL */
@@ -72,11 +72,13 @@ typedef struct {
   int32_t *misses;           /* [k] scratch */
   int16_t *ev;               /* [B] scratch */
   int32_t *first;            /* [P] scratch: first list index of each position */
+  int64_t host_row_stride;   /* bytes between consecutive host rows (0: rec) */
 } hso_layer;
 
 static const uint8_t *host_row(const hso_layer *L, int32_t r, int64_t p) {
   if (p < L->host_split)
-    return L->host + (int64_t)r * L->host_req_stride + p * (int64_t)L->rec;
+    return L->host + (int64_t)r * L->host_req_stride +
+           p * (L->host_row_stride ? L->host_row_stride : (int64_t)L->rec);
   return L->host_tail + ((int64_t)r * (L->P - L->host_split) + (p - L->host_split)) * (int64_t)L->rec;
 }
 

@@ -17,15 +17,16 @@ from workload.traces import all_traces
 class Run:
     def __init__(self, w, flags=0, mirror=False, ctas_per_request=0, replay_ctas=0,
                  num_reqs=None, oracle_bytes=True, traces=None, lookup=0, pool_kind=H.HOST_PINNED,
-                 fused=True, resident=None):
+                 fused=True, resident=None, group=1):
         """``resident`` = (int32 [steps][R][nblk] block tables, tokens per
         block) runs every anchor through the three-tier resolve, with the
         table of step t in place before step t."""
         self.w = w
         self.flags = flags
         dev = torch.device("cuda", 0)
-        self.mem = WorkloadMemory(w.R, w.L, w.B, w.P, w.rec, mirror=mirror, pool_kind=pool_kind)
-        REC.fill_host_pool(w, self.mem.pool.ptr, self.mem.layer_stride, self.mem.req_stride)
+        self.mem = WorkloadMemory(w.R, w.L, w.B, w.P, w.rec, mirror=mirror, pool_kind=pool_kind,
+                                  group=group)
+        REC.fill_host_pool(w, self.mem.geometry)
         if mirror:
             self.mem.fill_mirror()
         self.hs = HiSparse(w.R, w.L, w.k, w.B, w.P, w.rec, self.mem.layer_buffers(),

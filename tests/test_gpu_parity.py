@@ -458,6 +458,20 @@ def test_admit_rejects_bad_entries():
     hs.close(); mem.close()
 
 
+# ---------------------------------------------------------------------- #
+# Host pools with a shared-index group's layers interleaved row by row    #
+# ---------------------------------------------------------------------- #
+def test_group_interleaved_host_layout_shared():
+    """Anchor + 3 shared layers with their host rows interleaved: same results."""
+    _run_all(get("shared").scaled(R=4, groups=2, L_ctx=16384, steps=8), group=4)
+
+
+def test_group_interleaved_host_layout_write_through():
+    """Interleaved rows with the fused write-through and shared-layer write-backs."""
+    _run_all(get("shared").scaled(R=3, groups=2, L_ctx=8192, steps=6, write_through=True),
+             group=4)
+
+
 def test_import_rejects_inconsistent_state():
     mem, hs = _instance(1, 2, 4, 16)
     sp = np.array([[3, -1, 5, -1]], np.int32)

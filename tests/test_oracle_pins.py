@@ -385,3 +385,29 @@ def test_admit_c_equals_python():
         assert c.miss_count[r] == 0
         for s in range(n):
             assert bytes(c.hot[r, s]) == u.hot[s]
+
+
+def test_strided_host_rows_give_the_same_result():
+    """The C model reads host row p at req_stride*r + row_stride*p: a pool
+    whose rows are interleaved with another layer's gives the same state and
+    bytes as a contiguous copy of the same rows."""
+    from oracle.coracle import OracleLayer
+    R, k, B, P, rec = 2, 5, 9, 30, 16
+    rng = np.random.default_rng(11)
+    big = rng.integers(0, 256, size=(R, P, 3, rec), dtype=np.uint8)
+    strided = big[:, :, 1, :]                 # rows 48 bytes apart
+    flat = np.ascontiguousarray(strided)
+    a = OracleLayer(R, k, B, P, rec, host=strided)
+    b = OracleLayer(R, k, B, P, rec, host=flat)
+    a.reset(); b.reset()
+    for t in range(10):
+        sel = np.stack([rng.choice(P, size=k, replace=False) for _ in range(R)]).astype(np.int32)
+        oa, _ = a.resolve(sel)
+        ob, _ = b.resolve(sel)
+        np.testing.assert_array_equal(oa, ob)
+        np.testing.assert_array_equal(a.hot, b.hot)
+    for r in range(R):
+        for s in range(B):
+            p = a.slot_pos[r, s]
+            if p >= 0:
+                assert bytes(a.hot[r, s]) == bytes(flat[r, p])

@@ -83,19 +83,24 @@ def records(w, layer, req, positions):
     return out
 
 
-def fill_host_pool(w, base_ptr, layer_stride, req_stride, layers=None):
+def fill_host_pool(w, geometry, layers=None):
     """Fill rows [0, L_ctx) of every (layer, request) unit; poison the rest.
 
-    Row (l, r, p) lives at base_ptr + l*layer_stride + r*req_stride + p*rec.
+    ``geometry(l)`` gives layer l's (address of row (0, 0), request stride,
+    row stride) in bytes: row (l, r, p) lives at addr + r*req_stride +
+    p*row_stride.
     """
     layers = range(w.L) if layers is None else layers
     for l in layers:
+        base, req_stride, row_stride = geometry(l)
         for r in range(w.R):
-            unit = base_ptr + l * layer_stride + r * req_stride
-            fill(unit, w.L_ctx, w.rec, w.rec, w.seed, l, r, 0)
-            tail = (w.P - w.L_ctx) * w.rec
-            if tail:
-                ctypes.memset(unit + w.L_ctx * w.rec, POISON, tail)
+            unit = base + r * req_stride
+            fill(unit, w.L_ctx, row_stride, w.rec, w.seed, l, r, 0)
+            if row_stride == w.rec and w.P > w.L_ctx:
+                ctypes.memset(unit + w.L_ctx * w.rec, POISON, (w.P - w.L_ctx) * w.rec)
+            else:
+                for p in range(w.L_ctx, w.P):
+                    ctypes.memset(unit + p * row_stride, POISON, w.rec)
 
 
 def new_token_records(w):

@@ -10,22 +10,27 @@
 //   [VD] docs.vllm.ai, "HiSparse local KV offload architecture":
 //        "Hot lookup and LRU", "Performance invariants".
 //
-// GB300 design (what differs from the pages' one-CTA-per-request kernel):
-//   * One thread-block CLUSTER per request.  CTA 0 of the cluster (the
-//     leader) runs stages 1-3 and 5 on its shared memory; then every CTA of
-//     the cluster reads the miss list out of the leader's shared memory
-//     (distributed shared memory) and takes a share of stage 4.  A batch of 8
-//     requests thus fetches with 8 x 16 SMs instead of 8 SMs, which keeps
-//     enough 16-byte loads in flight to cover the host link's latency.
-//   * Stage 4 treats the misses of a request as one flat run of 16-byte
-//     chunks (miss j, chunk o), so no lane idles on records that are not a
-//     multiple of 512 bytes (1152-byte records are 72 chunks).
-//   * The scans of stage 3 give each warp one contiguous segment: warps count
-//     with __ballot_sync/__popc, one barrier publishes the 32 warp totals,
-//     each warp prefix-sums them with shuffles, and a second ballot pass writes
-//     the compacted lists -- two block barriers for all three scans.
-//   * No spin-waits: the only cross-CTA waits are hardware cluster barriers,
-//     and hash probing is bounded by the table size.
+// Kernels:
+//   resolve_pt_kernel (default, HISPARSE_LOOKUP_PAGE_TABLE): one thread-block
+//     CLUSTER per request.  Worker CTAs classify slices of the selection list
+//     through the published page table and issue the host loads of their
+//     first missed records into registers before any victim is known; the
+//     leader CTA merges the slices through distributed shared memory, checks
+//     duplicates, picks victims and the new LRU order, writes each worker's
+//     victims into that worker's shared memory, and publishes.  Two hardware
+//     cluster barriers, no spin-waits.  The write-through of the previous
+//     token is fused in; the launch uses programmatic dependent launch.  A
+//     second instantiation adds the resident tier, block-id selections and
+//     the union of speculative verify rows.
+//   resolve_kernel (HISPARSE_LOOKUP_HASH): the pages' stage order (hash
+//     staging, mark, scans, fetch by the whole cluster), kept as an ablation.
+//   replay_kernel, writeback_kernel, admit_kernel, reset_kernel: plan replay
+//     for shared-index layers, the separate write-through, admission with
+//     preload, and the reset state.
+// Common to the fetches: the misses of a request are one flat run of 16-byte
+// chunks (miss j, chunk o), so no lane idles on records that are not a
+// multiple of 512 bytes (1152-byte records are 72 chunks), read with
+// non-coherent 16-byte loads from mapped pinned host memory.
 #include <cuda_runtime.h>
 #include <sys/mman.h>
 

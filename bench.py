@@ -564,6 +564,28 @@ def run_ours(args):
     if args.verify and not args.resident and w.sel_block_tokens == 1 and args.verify_rows == 1:
         verify = verify_against_oracle(w, hs, mem, groups, traces, args.warmup + args.steps)
 
+    # ---- repeats: the whole trace 5 more times from the admission state (the
+    #      same warm-up and timed steps), so the spread between repeats of the
+    #      headline is on the line ----
+    rep_ms = []
+    for rep in range(5):
+        hs.reset()
+        mem.hot.zero_()
+        torch.cuda.synchronize()
+        for t in range(args.warmup):
+            plain[t].replay()
+        tot = 0.0
+        for i in range(args.steps):
+            t = args.warmup + i
+            flush.fill_(i & 0xFF)
+            r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            r0.record(cur)
+            plain[t].replay()
+            r1.record(cur)
+            torch.cuda.synchronize()
+            tot += r0.elapsed_time(r1)
+        rep_ms.append(tot / args.steps)
+
     # ---- pass 2 (per-kernel durations for the roofline): the same steps from
     #      the admission state, with events inside the graphs around every
     #      RESOLVE and write-back launch ----
@@ -881,6 +903,10 @@ def run_ours(args):
             "us_per_layer_step": round(launch_ms * 1e3, 2),
             "all_hit_no_io": allhit,
             "cold_step0": cold,
+            "repeats": {"ms_per_step": [round(x, 4) for x in rep_ms],
+                        "median_ms_per_step": round(sorted(rep_ms)[len(rep_ms) // 2], 4),
+                        "timing": "the whole trace 5 more times from the admission state, "
+                                  "each timed step between events (synchronised per step)"},
             "admission": admission,
             "replay": replay,
             "e2e": e2e,

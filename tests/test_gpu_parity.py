@@ -472,6 +472,24 @@ def test_group_interleaved_host_layout_write_through():
              group=4)
 
 
+def test_hash_lookup_rejects_extended_options():
+    """The hash-lookup kernel has no resident tier, block ids or union mode."""
+    R, k, B, P = 2, 8, 16, 64
+    mem, hs = _instance(R, k, B, P, lookup=H.LOOKUP_HASH)
+    out = torch.empty((R, k), dtype=torch.int32, device="cuda")
+    sel = _dev(np.array([[1, 2, 3, 4, 5, 6, 7, 8]] * R, np.int32))
+    blocks = _dev(np.full((R, 4), -1, np.int32))
+    with pytest.raises(H.HiSparseError):
+        hs.resolve_ex(0, sel, out, res_blocks=blocks, res_block_tokens=16)
+    with pytest.raises(H.HiSparseError):
+        hs.resolve_ex(0, _dev(np.array([[1, 2]] * R, np.int32)), out, sel_block_tokens=4)
+    with pytest.raises(H.HiSparseError):
+        hs.resolve(0, sel, out, flags=H.UNION)
+    hs.resolve(0, sel, out)                       # the plain call still works
+    assert hs.status()[0] == 0
+    hs.close(); mem.close()
+
+
 def test_import_rejects_inconsistent_state():
     mem, hs = _instance(1, 2, 4, 16)
     sp = np.array([[3, -1, 5, -1]], np.int32)

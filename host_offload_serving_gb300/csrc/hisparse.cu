@@ -1726,7 +1726,16 @@ int configure_resolve(hisparse_handle *h, int want_cs) {
   }
   uint32_t smax = 0;
   for (int cs = 1; cs <= 16; ++cs) smax = std::max(smax, resolve_smem(h, cs));
-  if (smax > 227u * 1024u) return HISPARSE_EBOUND;
+  // dynamic + static shared memory within the device's opt-in limit per block
+  int optin = 0;
+  HS_CUDA(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device));
+  size_t stat = 0;
+  for (int i = 0; i < nf; ++i) {
+    cudaFuncAttributes fa;
+    HS_CUDA(cudaFuncGetAttributes(&fa, fns[i]));
+    stat = std::max(stat, fa.sharedSizeBytes);
+  }
+  if (static_cast<size_t>(smax) + stat > static_cast<size_t>(optin)) return HISPARSE_EBOUND;
   for (int i = 0; i < nf; ++i) {
     HS_CUDA(cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smax));
     HS_CUDA(cudaFuncSetAttribute(fns[i], cudaFuncAttributeNonPortableClusterSizeAllowed, 1));

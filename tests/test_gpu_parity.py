@@ -535,3 +535,99 @@ def test_cuda_graph_replay_equals_eager():
     finally:
         eager.close()
         graph.close()
+
+
+# ---------------------------------------------------------------------- #
+def _largest_buffer(R, k, P_of, lookup):
+    """The largest B that hisparse_init accepts for (R, k) (shared memory is
+    the binding limit below the int16 LRU bound of 32767)."""
+    def fits(B):
+        mem = WorkloadMemory(R, 1, B, P_of(B), 16)
+        try:
+            hs = HiSparse(R, 1, k, B, P_of(B), 16, mem.layer_buffers(), lookup=lookup)
+        except H.HiSparseError as e:
+            assert e.code == H.EBOUND
+            return False
+        finally:
+            mem.close()
+        hs.close()
+        return True
+    lo, hi = k, 32767       # fits(lo) holds; find the last B that fits
+    assert fits(lo)
+    if fits(hi):
+        return hi
+    while hi - lo > 1:
+        mid = (lo + hi) // 2
+        if fits(mid):
+            lo = mid
+        else:
+            hi = mid
+    return lo
+
+
+@pytest.mark.parametrize("lookup", LOOKUPS)
+@pytest.mark.parametrize("k", [64, 2048])
+def test_largest_buffer_that_fits(k, lookup):
+    """At the largest accepted B, from a full imported state (every slot
+    occupied, LRU a random permutation), steps that mix hits and misses match
+    the oracle; B + 1 is refused with EBOUND."""
+    R = 2
+    P_of = lambda B: 3 * B
+    B = _largest_buffer(R, k, P_of, lookup)
+    print(f"largest accepted B at k={k}, lookup={lookup}: {B}")
+    P = P_of(B)
+    rng = np.random.default_rng(B * 7 + k)
+    mem, hs = _instance(R, k, B, P, lookup=lookup)
+    o = OracleLayer(R, k, B, P, 16, host=mem.host_view(0))
+    o.reset()
+    sp = np.stack([rng.permutation(P)[:B] for _ in range(R)]).astype(np.int32)
+    lru = np.stack([rng.permutation(B) for _ in range(R)]).astype(np.int16)
+    pt = np.full((R, P), -1, np.int32)
+    for r in range(R):
+        pt[r, sp[r]] = np.arange(B, dtype=np.int32)
+    assert hs.import_state(0, sp, lru, pt) == 0
+    o.slot_pos[:] = sp
+    o.lru[:] = lru
+    o.page_table[:] = pt
+    out = torch.empty((R, k), dtype=torch.int32, device="cuda")
+    for t in range(6):
+        sel = np.empty((R, k), np.int32)
+        for r in range(R):
+            resident = o.slot_pos[r][o.slot_pos[r] >= 0]
+            absent = np.setdiff1d(np.arange(P, dtype=np.int32), resident)
+            nh = int(rng.integers(0, k + 1))
+            row = np.concatenate([rng.choice(resident, nh, replace=False),
+                                  rng.choice(absent, k - nh, replace=False)])
+            sel[r] = rng.permutation(row)
+        hs.resolve(0, _dev(sel), out)
+        oo, e = o.resolve(sel)
+        assert e == 0
+        np.testing.assert_array_equal(out.cpu().numpy(), oo)
+    sp2, lru2, pt2, mc = hs.export_state(0)
+    np.testing.assert_array_equal(sp2, o.slot_pos)
+    np.testing.assert_array_equal(lru2, o.lru)
+    np.testing.assert_array_equal(pt2, o.page_table)
+    np.testing.assert_array_equal(mc, o.miss_count)
+    np.testing.assert_array_equal(mem.hot[0].cpu().numpy()[:, :B], o.hot[:, :B])
+    hs.close(); mem.close()
+    if B < 32767:
+        mem = WorkloadMemory(R, 1, B + 1, P_of(B + 1), 16)
+        with pytest.raises(H.HiSparseError) as ei:
+            HiSparse(R, 1, k, B + 1, P_of(B + 1), 16, mem.layer_buffers(), lookup=lookup)
+        assert ei.value.code == H.EBOUND
+        mem.close()
+
+
+def test_num_reqs_zero_touches_nothing():
+    """A graph padded down to no live request: every unit, slot vector and
+    host row stays as it was (write-through included)."""
+    run = Run(get("dsa").scaled(R=2, groups=1, L_ctx=8192, steps=3), num_reqs=0)
+    try:
+        for _ in range(3):
+            run.step()
+        run.compare()
+        assert (run.out.cpu().numpy() == -7).all()
+        sp, lru, pt, mc = run.hs.export_state(0)
+        assert (sp == -1).all() and (pt == -1).all() and (mc == 0).all()
+    finally:
+        run.close()

@@ -70,6 +70,9 @@ def parse():
     ap.add_argument("--L-ctx", type=int, default=0,
                     help="override the workload's prefill length (host pool size)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--replay", choices=("group", "layer"), default="group",
+                    help="shared-index layers: one replay launch per anchor (group) or one "
+                         "per layer (layer, as the pages describe)")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-allhit", action="store_true")
     ap.add_argument("--verify", action="store_true",
@@ -395,7 +398,8 @@ def run_ours(args):
     runner = DecodeStep(hs, mem, groups,
                         flags=(H.FROM_MIRROR if args.mirror else 0) |
                         (H.UNION if args.verify_rows > 1 else 0),
-                        fused=not args.unfused, sel_block_tokens=w.sel_block_tokens)
+                        fused=not args.unfused, sel_block_tokens=w.sel_block_tokens,
+                        group_replay=args.replay == "group")
     miss_hist = torch.zeros((T, G, w.R), dtype=torch.int32, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)     # > 129 MB L2
     setup_s = time.perf_counter() - t_setup
@@ -572,7 +576,9 @@ def run_ours(args):
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    launches = args.steps * (G + sum(len(f) for _, f in groups) +
+    replay_launches = sum((-(-len(f) // 8) if args.replay == "group" else len(f))
+                          for _, f in groups if f)
+    launches = args.steps * (G + replay_launches +
                              (1 if (wb is not None and args.unfused) else 0))
     if passg is not None:
         passg[0].replay()
@@ -878,7 +884,8 @@ def run_ours(args):
                   "us_avg": round(1e3 * sum(rp_ms) / len(rp_ms), 2),
                   "fetch_gbs": round(rp_bytes / (sum(rp_ms) / 1e3) / 1e9, 2),
                   "frac_of_link": round(rp_bytes / (sum(rp_ms) / 1e3) / 1e9 / h2d_gbs, 4),
-                  "followers_per_step": nf}
+                  "followers_per_step": nf,
+                  "layers_per_launch": round(nf * args.steps / len(rp_ms), 2)}
     if allhit:
         allhit["hbm_peak_gbs"] = peaks.get("hbm_gbs")
         allhit["hbm_frac"] = round(allhit["hbm_gbs"] / peaks.get("hbm_gbs"), 5)
@@ -914,6 +921,8 @@ def run_ours(args):
                        "lookup": ["page_table", "hash"][info["lookup"]],
                        "write_through_launch": "separate" if args.unfused else "fused into RESOLVE",
                        "host_pool": args.pool,
+                       "replay_launch": ("one per anchor for all its shared-index layers"
+                                         if args.replay == "group" else "one per shared-index layer"),
                        "host_layout": ("rows of each shared-index group interleaved"
                                        if args.interleave else "one block of rows per layer"),
                        "fetch_source": "HBM mirror of the host pool" if args.mirror else "host pool",

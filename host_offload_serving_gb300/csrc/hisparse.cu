@@ -133,14 +133,19 @@ struct WritebackArgs {
   uint32_t *status;
 };
 
-struct ReplayArgs {
-  int32_t R, k, rec16;
-  const int32_t *num_reqs;
-  const int32_t *plan_pos, *plan_slot, *plan_count;
+// One shared-index layer a replay fills: its host pool and hot buffer.
+struct ReplayTarget {
   const char *src;
   int64_t src_req_stride, src_row_stride;
   char *hot;
   int64_t hot_req_stride, hot_row_stride;
+};
+constexpr int kMaxReplayTargets = 8;  // shared-index layers one replay launch fills
+struct ReplayArgs {
+  int32_t R, k, rec16, nf;
+  const int32_t *num_reqs;
+  const int32_t *plan_pos, *plan_slot, *plan_count;
+  ReplayTarget f[kMaxReplayTargets];  // nf of them
 };
 
 // ---------------------------------------------------------------------------
@@ -1502,8 +1507,8 @@ __host__ __device__ inline int replay_pref_bytes(int R) { return ((R + 1) * 4 + 
 __global__ void __launch_bounds__(kReplayThreads) replay_kernel(const ReplayArgs a) {
   extern __shared__ __align__(16) unsigned char rsm[];
   int32_t *s_pref = reinterpret_cast<int32_t *>(rsm);  // [R + 1] exclusive prefix of plan counts
-  int64_t *s_src = reinterpret_cast<int64_t *>(rsm + replay_pref_bytes(a.R));  // [kReplayBatch]
-  int64_t *s_dst = s_src + kReplayBatch;
+  const char **s_src = reinterpret_cast<const char **>(rsm + replay_pref_bytes(a.R));  // [kReplayBatch]
+  char **s_dst = reinterpret_cast<char **>(rsm + replay_pref_bytes(a.R) + sizeof(char *) * kReplayBatch);
   const int tid = threadIdx.x;
   const int nreq = a.num_reqs ? min(*a.num_reqs, a.R) : a.R;
   if (tid < 32) {
@@ -1522,24 +1527,29 @@ __global__ void __launch_bounds__(kReplayThreads) replay_kernel(const ReplayArgs
     if (tid == 0) s_pref[nreq] = run;
   }
   __syncthreads();
-  const int M = s_pref[nreq];
-  const int m0 = static_cast<int>(static_cast<int64_t>(M) * blockIdx.x / gridDim.x);
-  const int m1 = static_cast<int>(static_cast<int64_t>(M) * (blockIdx.x + 1) / gridDim.x);
+  // Work items are (plan record, target) pairs, the targets of one record
+  // next to each other: with the group's layers interleaved in the host pool,
+  // consecutive items read adjacent host rows of one page.
+  const int nf = a.nf;
+  const int64_t W = static_cast<int64_t>(s_pref[nreq]) * nf;
+  const int64_t w0 = W * blockIdx.x / gridDim.x, w1 = W * (blockIdx.x + 1) / gridDim.x;
   const uint32_t rec16 = static_cast<uint32_t>(a.rec16);
-  for (int b0 = m0; b0 < m1; b0 += kReplayBatch) {
-    const int nb = min(kReplayBatch, m1 - b0);
+  for (int64_t b0 = w0; b0 < w1; b0 += kReplayBatch) {
+    const int nb = static_cast<int>(min(static_cast<int64_t>(kReplayBatch), w1 - b0));
     for (int i = tid; i < nb; i += kReplayThreads) {
-      const int m = b0 + i;
+      const int64_t item = b0 + i;
+      const int m = static_cast<int>(item / nf), f = static_cast<int>(item - int64_t(m) * nf);
       int lo = 0, hi = nreq - 1;  // the request: last r with s_pref[r] <= m
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
         if (s_pref[mid] <= m) lo = mid; else hi = mid - 1;
       }
       const int64_t pk = static_cast<int64_t>(lo) * a.k + (m - s_pref[lo]);
-      s_src[i] = static_cast<int64_t>(lo) * a.src_req_stride +
-                 static_cast<int64_t>(a.plan_pos[pk]) * a.src_row_stride;
-      s_dst[i] = static_cast<int64_t>(lo) * a.hot_req_stride +
-                 static_cast<int64_t>(a.plan_slot[pk]) * a.hot_row_stride;
+      const ReplayTarget &T = a.f[f];
+      s_src[i] = T.src + static_cast<int64_t>(lo) * T.src_req_stride +
+                 static_cast<int64_t>(a.plan_pos[pk]) * T.src_row_stride;
+      s_dst[i] = T.hot + static_cast<int64_t>(lo) * T.hot_req_stride +
+                 static_cast<int64_t>(a.plan_slot[pk]) * T.hot_row_stride;
     }
     __syncthreads();
     const uint32_t n = static_cast<uint32_t>(nb) * rec16;
@@ -1552,8 +1562,8 @@ __global__ void __launch_bounds__(kReplayThreads) replay_kernel(const ReplayArgs
         d[u] = nullptr;
         if (q < n) {
           const uint32_t i = q / rec16, o = q - i * rec16;
-          v[u] = ld_nc_v4(a.src + s_src[i] + 16 * o);
-          d[u] = a.hot + s_dst[i] + 16 * o;
+          v[u] = ld_nc_v4(s_src[i] + 16 * o);
+          d[u] = s_dst[i] + 16 * o;
         }
       }
 #pragma unroll
@@ -2270,19 +2280,35 @@ int hisparse_writeback(hisparse_handle *h, int32_t layer, const int32_t *d_pos,
 
 int hisparse_prefetch_plan(hisparse_handle *h, int32_t anchor_layer, int32_t follower_layer,
                            const int32_t *d_num_reqs, void *stream) {
-  if (layer_ok(h, anchor_layer) || layer_ok(h, follower_layer)) return HISPARSE_EINVAL;
-  if (h->anchor_of[anchor_layer] != -1 || h->anchor_of[follower_layer] != anchor_layer)
-    return HISPARSE_EROLE;
+  if (layer_ok(h, anchor_layer) || (follower_layer != -1 && layer_ok(h, follower_layer)))
+    return HISPARSE_EINVAL;
+  if (h->anchor_of[anchor_layer] != -1) return HISPARSE_EROLE;
+  if (follower_layer != -1 && h->anchor_of[follower_layer] != anchor_layer) return HISPARSE_EROLE;
+  // the layers to fill: the one named, or every shared-index layer of the anchor
+  std::vector<int32_t> fl;
+  if (follower_layer != -1) fl.push_back(follower_layer);
+  else
+    for (int32_t l = 0; l < h->L; ++l)
+      if (h->anchor_of[l] == anchor_layer) fl.push_back(l);
   const AnchorMeta &m = h->meta[anchor_layer];
-  const LayerDev &Lf = h->layers[follower_layer];
-  ReplayArgs a;
-  a.R = h->R; a.k = h->k; a.rec16 = h->rec / 16; a.num_reqs = d_num_reqs;
-  a.plan_pos = m.plan_pos; a.plan_slot = m.plan_slot; a.plan_count = m.plan_count;
-  a.src = Lf.host; a.src_req_stride = Lf.host_req_stride; a.src_row_stride = Lf.host_row_stride;
-  a.hot = Lf.hot; a.hot_req_stride = Lf.hot_req_stride; a.hot_row_stride = Lf.hot_row_stride;
-  const size_t smem = replay_pref_bytes(h->R) + 2 * sizeof(int64_t) * kReplayBatch;
-  replay_kernel<<<h->replay_ctas, kReplayThreads, smem, static_cast<cudaStream_t>(stream)>>>(a);
-  HS_CUDA(cudaGetLastError());
+  const size_t smem = replay_pref_bytes(h->R) + 2 * sizeof(char *) * kReplayBatch;
+  for (size_t f0 = 0; f0 < fl.size(); f0 += kMaxReplayTargets) {
+    ReplayArgs a;
+    a.R = h->R; a.k = h->k; a.rec16 = h->rec / 16; a.num_reqs = d_num_reqs;
+    a.plan_pos = m.plan_pos; a.plan_slot = m.plan_slot; a.plan_count = m.plan_count;
+    a.nf = static_cast<int32_t>(std::min(fl.size() - f0, static_cast<size_t>(kMaxReplayTargets)));
+    for (int i = 0; i < a.nf; ++i) {
+      const LayerDev &Lf = h->layers[fl[f0 + i]];
+      a.f[i].src = Lf.host;
+      a.f[i].src_req_stride = Lf.host_req_stride;
+      a.f[i].src_row_stride = Lf.host_row_stride;
+      a.f[i].hot = Lf.hot;
+      a.f[i].hot_req_stride = Lf.hot_req_stride;
+      a.f[i].hot_row_stride = Lf.hot_row_stride;
+    }
+    replay_kernel<<<h->replay_ctas, kReplayThreads, smem, static_cast<cudaStream_t>(stream)>>>(a);
+    HS_CUDA(cudaGetLastError());
+  }
   return HISPARSE_OK;
 }
 

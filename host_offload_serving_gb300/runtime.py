@@ -262,6 +262,11 @@ class DecodeStep:
     first; ``sel_block_tokens`` > 1 means ``sel`` holds block ids of that many
     positions each (both through ``hisparse_resolve_ex``).
 
+    ``group_replay=True`` (default) fills all of an anchor's shared-index
+    layers with one ``hisparse_prefetch_plan(anchor, -1)`` launch, reading
+    each plan record's rows for all of them back to back; ``False`` issues one
+    replay per layer, as the pages do.
+
     ``fused=True`` (default) writes each anchor's previous token through, and
     installs its new token, inside that anchor's RESOLVE launch
     (``hisparse_resolve_step``); shared-index layers get a write-back launch on
@@ -271,8 +276,9 @@ class DecodeStep:
     """
 
     def __init__(self, hs, mem, groups, flags=0, num_reqs=None, fused=True, resident=None,
-                 sel_block_tokens=1):
+                 sel_block_tokens=1, group_replay=True):
         self.hs, self.mem, self.groups = hs, mem, groups
+        self.group_replay = group_replay
         self.flags = flags
         self.num_reqs = num_reqs
         self.fused = fused
@@ -326,12 +332,22 @@ class DecodeStep:
             if followers:
                 self.ev_anchor[gi].record(self.compute)
                 self.side.wait_event(self.ev_anchor[gi])
-                for fi, fl in enumerate(followers):
-                    if through and self.fused:   # the shared layer's own write-through first
-                        hs.writeback(fl, pos[fl:fl + 1], self.num_reqs, stream=self.side,
-                                     new_rows=new_rows[fl] if new_rows is not None else None)
-                    hs.prefetch_plan(anchor, fl, self.num_reqs, stream=self.side)
-                    self.ev_follow[gi][fi].record(self.side)
+                every = sorted(followers) == [l for l in range(hs.L) if hs.anchor_of[l] == anchor]
+                if self.group_replay and every:
+                    if through and self.fused:   # the shared layers' own write-through first
+                        for fl in followers:
+                            hs.writeback(fl, pos[fl:fl + 1], self.num_reqs, stream=self.side,
+                                         new_rows=new_rows[fl] if new_rows is not None else None)
+                    hs.prefetch_plan(anchor, -1, self.num_reqs, stream=self.side)
+                    for fi in range(len(followers)):
+                        self.ev_follow[gi][fi].record(self.side)
+                else:
+                    for fi, fl in enumerate(followers):
+                        if through and self.fused:   # the shared layer's own write-through first
+                            hs.writeback(fl, pos[fl:fl + 1], self.num_reqs, stream=self.side,
+                                         new_rows=new_rows[fl] if new_rows is not None else None)
+                        hs.prefetch_plan(anchor, fl, self.num_reqs, stream=self.side)
+                        self.ev_follow[gi][fi].record(self.side)
         # a shared layer's attention would wait on its own event; at the end of
         # the step the caller's stream waits for everything
         for gi, (_, followers) in enumerate(self.groups):

@@ -287,7 +287,13 @@ int hisparse_writeback(hisparse_handle *h, int32_t layer, const int32_t *d_pos,
  * follower's slots stay in lockstep with the anchor's, so the anchor's d_out
  * rows are also the follower's.  Order it after the anchor's resolve (same
  * stream or an event) and before the anchor's next resolve.
- * Errors: EINVAL, EROLE, ECUDA. */
+ * follower_layer == -1 fills every shared-index layer of the anchor: one
+ * launch per 8 such layers, each reading a plan record's rows for all its
+ * layers back to back (with the group's layers interleaved in the host pool,
+ * rows of one page).  The bytes written are the same as one call per layer.
+ * An anchor without shared-index layers then launches nothing.
+ * Errors: EINVAL (bad layer id), EROLE (anchor_layer is a shared-index
+ * layer, or follower_layer is not one of its layers), ECUDA. */
 int hisparse_prefetch_plan(hisparse_handle *h, int32_t anchor_layer, int32_t follower_layer,
                            const int32_t *d_num_reqs, void *stream);
 

@@ -17,7 +17,7 @@ from workload.traces import all_traces
 class Run:
     def __init__(self, w, flags=0, mirror=False, ctas_per_request=0, replay_ctas=0,
                  num_reqs=None, oracle_bytes=True, traces=None, lookup=0, pool_kind=H.HOST_PINNED,
-                 fused=True, resident=None, group=1):
+                 fused=True, resident=None, group=1, group_replay=True):
         """``resident`` = (int32 [steps][R][nblk] block tables, tokens per
         block) runs every anchor through the three-tier resolve, with the
         table of step t in place before step t."""
@@ -67,7 +67,8 @@ class Run:
         self.step_runner = DecodeStep(self.hs, self.mem, self.groups, flags=flags,
                                       num_reqs=self.num_reqs, fused=fused,
                                       resident=None if resident is None else
-                                      (self.res_dev, self.res_tok), sel_block_tokens=bt)
+                                      (self.res_dev, self.res_tok), sel_block_tokens=bt,
+                                      group_replay=group_replay)
         # oracle
         self.oracle = {}
         for l in range(w.L):

@@ -157,9 +157,11 @@ def test_separate_writeback_launch(lookup):
     _run_all(get("dsa").scaled(R=4, groups=2, L_ctx=32768, steps=8), lookup=lookup, fused=False)
 
 
-def test_write_through_with_shared_layers():
+@pytest.mark.parametrize("group_replay", [True, False])
+def test_write_through_with_shared_layers(group_replay):
     """Write-through on anchors (fused) and on shared layers (own launch)."""
-    _run_all(get("shared").scaled(R=3, groups=2, L_ctx=8192, steps=6, write_through=True))
+    _run_all(get("shared").scaled(R=3, groups=2, L_ctx=8192, steps=6, write_through=True),
+             group_replay=group_replay)
 
 
 def test_quest_workload_scaled():
@@ -167,9 +169,37 @@ def test_quest_workload_scaled():
     _run_all(get("quest").scaled(R=4, groups=2, L_ctx=2048, steps=12))
 
 
-def test_shared_workload_scaled():
-    """Anchor + 3 shared layers replaying the plan (fewer requests, shorter context)."""
-    _run_all(get("shared").scaled(R=6, groups=2, L_ctx=16384, steps=10))
+@pytest.mark.parametrize("group_replay", [True, False])
+def test_shared_workload_scaled(group_replay):
+    """Anchor + 3 shared layers replaying the plan (fewer requests, shorter
+    context); one replay launch per group, or one per shared layer."""
+    _run_all(get("shared").scaled(R=6, groups=2, L_ctx=16384, steps=10), group_replay=group_replay)
+
+
+@pytest.mark.parametrize("followers", [1, 8, 11])
+def test_group_replay_many_layers(followers):
+    """One anchor with 1, 8 (one launch) and 11 (two launches) shared layers."""
+    _run_all(get("shared").scaled(R=3, groups=1, followers=followers, L_ctx=4096, steps=5),
+             replay_ctas=3)
+
+
+def test_group_replay_roles():
+    """follower -1 on an anchor without shared layers launches nothing; a
+    shared layer as the anchor, or another anchor's layer, is refused."""
+    w = get("shared").scaled(R=2, groups=2, L_ctx=1024, steps=2)
+    mem = WorkloadMemory(w.R, w.L, w.B, w.P, w.rec)
+    hs = HiSparse(w.R, w.L, w.k, w.B, w.P, w.rec, mem.layer_buffers(), anchor_of=w.anchor_of())
+    assert H.hisparse_prefetch_plan(hs.h, 1, -1, None, None) == H.EROLE
+    assert H.hisparse_prefetch_plan(hs.h, 0, 5, None, None) == H.EROLE
+    assert H.hisparse_prefetch_plan(hs.h, 0, -2, None, None) == H.EINVAL
+    assert H.hisparse_prefetch_plan(hs.h, w.L, -1, None, None) == H.EINVAL
+    hs.close(); mem.close()
+    w = get("dsa").scaled(R=2, groups=2, L_ctx=1024, steps=2)
+    mem = WorkloadMemory(w.R, w.L, w.B, w.P, w.rec)
+    hs = HiSparse(w.R, w.L, w.k, w.B, w.P, w.rec, mem.layer_buffers(), anchor_of=w.anchor_of())
+    assert H.hisparse_prefetch_plan(hs.h, 0, -1, None, None) == H.OK
+    torch.cuda.synchronize()
+    hs.close(); mem.close()
 
 
 @pytest.mark.parametrize("B", [2048, 4096, 8192])
@@ -461,9 +491,11 @@ def test_admit_rejects_bad_entries():
 # ---------------------------------------------------------------------- #
 # Host pools with a shared-index group's layers interleaved row by row    #
 # ---------------------------------------------------------------------- #
-def test_group_interleaved_host_layout_shared():
+@pytest.mark.parametrize("group_replay", [True, False])
+def test_group_interleaved_host_layout_shared(group_replay):
     """Anchor + 3 shared layers with their host rows interleaved: same results."""
-    _run_all(get("shared").scaled(R=4, groups=2, L_ctx=16384, steps=8), group=4)
+    _run_all(get("shared").scaled(R=4, groups=2, L_ctx=16384, steps=8), group=4,
+             group_replay=group_replay)
 
 
 def test_group_interleaved_host_layout_write_through():

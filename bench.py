@@ -70,9 +70,10 @@ def parse():
     ap.add_argument("--L-ctx", type=int, default=0,
                     help="override the workload's prefill length (host pool size)")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--replay", choices=("group", "layer"), default="group",
-                    help="shared-index layers: one replay launch per anchor (group) or one "
-                         "per layer (layer, as the pages describe)")
+    ap.add_argument("--replay", choices=("group", "layer", "inline"), default="group",
+                    help="shared-index layers: one replay launch per anchor (group), one "
+                         "per layer (layer, as the pages describe), or filled inside the "
+                         "anchor's RESOLVE launch (inline, HISPARSE_WITH_SHARED)")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-allhit", action="store_true")
     ap.add_argument("--verify", action="store_true",
@@ -399,7 +400,8 @@ def run_ours(args):
                         flags=(H.FROM_MIRROR if args.mirror else 0) |
                         (H.UNION if args.verify_rows > 1 else 0),
                         fused=not args.unfused, sel_block_tokens=w.sel_block_tokens,
-                        group_replay=args.replay == "group")
+                        group_replay=args.replay == "group",
+                        inline_shared=args.replay == "inline")
     miss_hist = torch.zeros((T, G, w.R), dtype=torch.int32, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)     # > 129 MB L2
     setup_s = time.perf_counter() - t_setup
@@ -576,7 +578,8 @@ def run_ours(args):
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    replay_launches = sum((-(-len(f) // 8) if args.replay == "group" else len(f))
+    replay_launches = sum((-(-len(f) // 8) if args.replay == "group" else
+                           0 if args.replay == "inline" else len(f))
                           for _, f in groups if f)
     launches = args.steps * (G + replay_launches +
                              (1 if (wb is not None and args.unfused) else 0))
@@ -666,7 +669,9 @@ def run_ours(args):
     # fused, no shared-index layers), the average launch over the timed region
     # is the pass-1 step time over the launches per step: the same CUDA events,
     # without the extra event nodes the per-launch windows put between kernels.
-    only_resolve = all(not f for _, f in groups) and not (args.unfused and wb is not None)
+    inline = args.replay == "inline"
+    only_resolve = (all(not f for _, f in groups) or (inline and wb is None)) and \
+        not (args.unfused and wb is not None)
     if only_resolve:
         launch_ms = (sum(step_ms) / len(step_ms)) / G
         timing_note = ("average RESOLVE launch over the timed region = pass-1 step time (CUDA "
@@ -677,6 +682,9 @@ def run_ours(args):
     else:
         launch_ms = resolve_avg_ms
     miss_bytes = int(miss.sum()) * w.rec
+    if inline:   # a RESOLVE launch also moves every miss's rows of its shared-index layers
+        miss_bytes = sum(int(miss[:, gi].sum()) * (1 + len(f))
+                         for gi, (_, f) in enumerate(groups)) * w.rec
     fetch_gbs = miss_bytes / (launch_ms * args.steps * G / 1e3) / 1e9
     miss_rate = float(miss.sum()) / (args.steps * G * w.R * w.k)
 
@@ -921,8 +929,10 @@ def run_ours(args):
                        "lookup": ["page_table", "hash"][info["lookup"]],
                        "write_through_launch": "separate" if args.unfused else "fused into RESOLVE",
                        "host_pool": args.pool,
-                       "replay_launch": ("one per anchor for all its shared-index layers"
-                                         if args.replay == "group" else "one per shared-index layer"),
+                       "replay_launch": {"group": "one per anchor for all its shared-index layers",
+                                         "layer": "one per shared-index layer",
+                                         "inline": "none: shared-index layers filled inside "
+                                                   "the anchor's RESOLVE"}[args.replay],
                        "host_layout": ("rows of each shared-index group interleaved"
                                        if args.interleave else "one block of rows per layer"),
                        "fetch_source": "HBM mirror of the host pool" if args.mirror else "host pool",

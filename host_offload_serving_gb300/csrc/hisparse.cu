@@ -668,6 +668,10 @@ struct PtArgs {
   // Union mode (speculative verify rows resolved as one list): a repeated
   // position is resolved at its first reference and shares its row.
   int32_t union_mode;
+  // Shared-index layers filled in the same launch (HISPARSE_WITH_SHARED):
+  // every missed record's row of each, at the anchor's victim slot.
+  int32_t nfl;
+  ReplayTarget fl[kMaxReplayTargets];
   int64_t P;
   const int32_t *sel, *num_reqs, *newest;
   int32_t *out;
@@ -1288,6 +1292,38 @@ __device__ void pt_worker_finish(const PtArgs &a, int r, int i0, int n, int32_t 
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u)
         if (d[u]) st_v4(d[u], x[u]);
+    }
+    // the shared-index layers: a miss's rows of all of them back to back
+    // (adjacent host rows when the group's rows are interleaved)
+    if (a.nfl > 0) {
+      const uint32_t rec16 = static_cast<uint32_t>(a.rec16);
+      const uint32_t per = static_cast<uint32_t>(a.nfl) * rec16;
+      const int64_t totf = static_cast<int64_t>(mw) * per;
+      for (int64_t b0 = tid; b0 < totf; b0 += static_cast<int64_t>(kThreads) * kUnroll) {
+        uint4 x[kUnroll];
+        char *d[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          const int64_t q = b0 + static_cast<int64_t>(u) * kThreads;
+          d[u] = nullptr;
+          if (q < totf) {
+            const uint32_t q32 = static_cast<uint32_t>(q);
+            const uint32_t j = q32 / per, rem = q32 - j * per;
+            const uint32_t f = rem / rec16, o = rem - f * rec16;
+            const int32_t vj = w_vict[j];
+            if (!(vj & kAlias)) {
+              const ReplayTarget &T = a.fl[f];
+              x[u] = ld_nc_v4(T.src + static_cast<int64_t>(r) * T.src_req_stride +
+                              static_cast<int64_t>(w_mp[j]) * T.src_row_stride + 16 * o);
+              d[u] = T.hot + static_cast<int64_t>(r) * T.hot_req_stride +
+                     static_cast<int64_t>(vj) * T.hot_row_stride + 16 * o;
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+          if (d[u]) st_v4(d[u], x[u]);
+      }
     }
   }
   // the slice's slot vector ([DD] §3.5 stage 5: aligned with the list)
@@ -2177,13 +2213,27 @@ int hisparse_resolve_ex(hisparse_handle *h, int32_t layer, const int32_t *d_sel,
     return HISPARSE_EINVAL;
   if (d_new_rows && !aligned16(d_new_rows)) return HISPARSE_EINVAL;
   if (!d_sel || !d_out) return HISPARSE_EINVAL;
-  if (flags & ~(HISPARSE_RECORD_PLAN | HISPARSE_SKIP_IO | HISPARSE_FROM_MIRROR | HISPARSE_UNION))
+  if (flags & ~(HISPARSE_RECORD_PLAN | HISPARSE_SKIP_IO | HISPARSE_FROM_MIRROR | HISPARSE_UNION |
+                HISPARSE_WITH_SHARED))
     return HISPARSE_EINVAL;
-  if ((flags & HISPARSE_UNION) && h->lookup == HISPARSE_LOOKUP_HASH) return HISPARSE_EINVAL;
+  if ((flags & (HISPARSE_UNION | HISPARSE_WITH_SHARED)) && h->lookup == HISPARSE_LOOKUP_HASH)
+    return HISPARSE_EINVAL;
   if (h->anchor_of[layer] != -1) return HISPARSE_EROLE;
   const LayerDev &Ld = h->layers[layer];
   const AnchorMeta &m = h->meta[layer];
   if ((flags & HISPARSE_FROM_MIRROR) && !Ld.mirror) return HISPARSE_EINVAL;
+  std::vector<int32_t> shared_layers;  // filled in this launch (HISPARSE_WITH_SHARED)
+  if (flags & HISPARSE_WITH_SHARED) {
+    for (int32_t l = 0; l < h->L; ++l)
+      if (h->anchor_of[l] == layer) shared_layers.push_back(l);
+    if (shared_layers.size() > static_cast<size_t>(kMaxReplayTargets)) return HISPARSE_EBOUND;
+    // a slice's (miss, layer, chunk) index stays below 2^31 (32-bit index math)
+    if (static_cast<int64_t>(h->k) * static_cast<int64_t>(shared_layers.size()) * (h->rec / 16) >=
+        (int64_t(1) << 31))
+      return HISPARSE_EBOUND;
+    for (int32_t l : shared_layers)
+      if ((flags & HISPARSE_FROM_MIRROR) && !h->layers[l].mirror) return HISPARSE_EINVAL;
+  }
   const bool plan = flags & HISPARSE_RECORD_PLAN;
 
   cudaLaunchConfig_t lc = {};
@@ -2249,6 +2299,16 @@ int hisparse_resolve_ex(hisparse_handle *h, int32_t layer, const int32_t *d_sel,
     a.src = (flags & HISPARSE_FROM_MIRROR) ? Ld.mirror : Ld.host;
     a.src_req_stride = Ld.host_req_stride; a.src_row_stride = Ld.host_row_stride;
     a.hot = Ld.hot; a.hot_req_stride = Ld.hot_req_stride; a.hot_row_stride = Ld.hot_row_stride;
+    a.nfl = static_cast<int32_t>(shared_layers.size());
+    for (int i = 0; i < a.nfl; ++i) {
+      const LayerDev &Lf = h->layers[shared_layers[i]];
+      a.fl[i].src = (flags & HISPARSE_FROM_MIRROR) ? Lf.mirror : Lf.host;
+      a.fl[i].src_req_stride = Lf.host_req_stride;
+      a.fl[i].src_row_stride = Lf.host_row_stride;
+      a.fl[i].hot = Lf.hot;
+      a.fl[i].hot_req_stride = Lf.hot_req_stride;
+      a.fl[i].hot_row_stride = Lf.hot_row_stride;
+    }
     lc.numAttrs = 2;  // cluster shape + programmatic dependent launch
     if (d_res_blocks || sel_bt > 1 || a.union_mode)  // the extended instantiation
       e = plan ? cudaLaunchKernelEx(&lc, resolve_pt_kernel<true, true>, a)

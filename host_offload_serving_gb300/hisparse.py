@@ -12,7 +12,7 @@ from . import _build
 
 OK, EINVAL, EBOUND, ENOMEM, ECUDA, EROLE = 0, -1, -2, -3, -4, -5
 ERR_RANGE, ERR_DUP = 1, 2
-RECORD_PLAN, SKIP_IO, FROM_MIRROR, UNION = 1, 2, 4, 8
+RECORD_PLAN, SKIP_IO, FROM_MIRROR, UNION, WITH_SHARED = 1, 2, 4, 8, 16
 LOOKUP_PAGE_TABLE, LOOKUP_HASH = 0, 1
 HOST_HUGE, HOST_PINNED = 0, 1
 

@@ -206,8 +206,8 @@ class WorkloadMemory:
         self.pool = HostPool(L * self.layer_stride, kind=pool_kind)
         self.hot = torch.zeros((L, R, B + 1, rec), dtype=torch.uint8, device=device)
         self.mirror = None
-        if mirror:
-            self.mirror = torch.empty((L, R, P, rec), dtype=torch.uint8, device=device)
+        if mirror:   # byte for byte the pool's layout, so it shares the pool's strides
+            self.mirror = torch.empty(L * self.layer_stride, dtype=torch.uint8, device=device)
 
     def layer_offset(self, layer):
         """Byte offset of layer ``layer``'s row (0, 0) in the pool."""
@@ -231,17 +231,13 @@ class WorkloadMemory:
             base, rs, ws = self.geometry(l)
             out.append(H.LayerBuffers(
                 base, rs, ws, self.hot[l].data_ptr(), (self.B + 1) * self.rec, self.rec,
-                self.mirror[l].data_ptr() if self.mirror is not None else None))
+                self.mirror.data_ptr() + self.layer_offset(l) if self.mirror is not None else None))
         return out
 
     def fill_mirror(self):
         """Copy the host pool into the HBM mirror (pinned -> device)."""
-        if self.group == 1:
-            src = torch.from_numpy(self.pool.numpy()).view(self.L, self.R, self.P, self.rec)
-            self.mirror.copy_(src, non_blocking=False)
-        else:
-            for l in range(self.L):
-                self.mirror[l].copy_(torch.from_numpy(np.ascontiguousarray(self.host_view(l))))
+        self.mirror.copy_(torch.from_numpy(self.pool.numpy()[:self.mirror.numel()]),
+                          non_blocking=False)
 
     def close(self):
         self.pool.close()
@@ -267,6 +263,11 @@ class DecodeStep:
     each plan record's rows for all of them back to back; ``False`` issues one
     replay per layer, as the pages do.
 
+    ``inline_shared=True`` fills an anchor's shared-index layers inside the
+    anchor's own RESOLVE launch (``HISPARSE_WITH_SHARED``) instead of replaying
+    its plan on the side stream; their write-backs then go first, on the
+    compute stream.
+
     ``fused=True`` (default) writes each anchor's previous token through, and
     installs its new token, inside that anchor's RESOLVE launch
     (``hisparse_resolve_step``); shared-index layers get a write-back launch on
@@ -276,9 +277,10 @@ class DecodeStep:
     """
 
     def __init__(self, hs, mem, groups, flags=0, num_reqs=None, fused=True, resident=None,
-                 sel_block_tokens=1, group_replay=True):
+                 sel_block_tokens=1, group_replay=True, inline_shared=False):
         self.hs, self.mem, self.groups = hs, mem, groups
         self.group_replay = group_replay
+        self.inline_shared = inline_shared
         self.flags = flags
         self.num_reqs = num_reqs
         self.fused = fused
@@ -313,7 +315,16 @@ class DecodeStep:
             self.ev_wb.record(self.backup)
             self.compute.wait_event(self.ev_wb)
         for gi, (anchor, followers) in enumerate(self.groups):
-            f = self.flags | (H.RECORD_PLAN if followers else 0)
+            every = sorted(followers) == [l for l in range(hs.L) if hs.anchor_of[l] == anchor]
+            inline = bool(followers) and self.inline_shared and every
+            if inline:
+                f = self.flags | H.WITH_SHARED
+                if through and self.fused:   # the shared layers' write-through before they are read
+                    for fl in followers:
+                        hs.writeback(fl, pos[fl:fl + 1], self.num_reqs, stream=self.compute,
+                                     new_rows=new_rows[fl] if new_rows is not None else None)
+            else:
+                f = self.flags | (H.RECORD_PLAN if followers else 0)
             if self.resident is not None or self.sel_block_tokens > 1:
                 fused = through and self.fused
                 res = self.resident
@@ -329,10 +340,12 @@ class DecodeStep:
                                 stream=self.compute)
             else:
                 hs.resolve(anchor, sel[gi], out[gi], self.num_reqs, newest, f, stream=self.compute)
-            if followers:
+            if inline:
+                for fi in range(len(followers)):
+                    self.ev_follow[gi][fi].record(self.compute)
+            elif followers:
                 self.ev_anchor[gi].record(self.compute)
                 self.side.wait_event(self.ev_anchor[gi])
-                every = sorted(followers) == [l for l in range(hs.L) if hs.anchor_of[l] == anchor]
                 if self.group_replay and every:
                     if through and self.fused:   # the shared layers' own write-through first
                         for fl in followers:

@@ -73,6 +73,16 @@ extern "C" {
                                    same row (no HISPARSE_ERR_DUP); misses take victims
                                    in first-reference order and are fetched, counted
                                    and planned once.  Page-table lookup only. */
+#define HISPARSE_WITH_SHARED 16u /* also fill the layer's shared-index layers
+                                   (anchor_of == layer; 8 at most) in the same
+                                   launch: each missed record's row of every such
+                                   layer is read from that layer's host pool (its
+                                   mirror with FROM_MIRROR) into its hot buffer at
+                                   the same slot -- the bytes hisparse_prefetch_plan
+                                   would copy, without a plan replay.  Their
+                                   write-backs must come first.  With SKIP_IO
+                                   nothing is filled.  Page-table lookup only;
+                                   more than 8 shared-index layers: EBOUND. */
 
 /* ---- lookup strategies (hisparse_config.lookup) ------------------------- */
 #define HISPARSE_LOOKUP_PAGE_TABLE 0

@@ -17,7 +17,7 @@ from workload.traces import all_traces
 class Run:
     def __init__(self, w, flags=0, mirror=False, ctas_per_request=0, replay_ctas=0,
                  num_reqs=None, oracle_bytes=True, traces=None, lookup=0, pool_kind=H.HOST_PINNED,
-                 fused=True, resident=None, group=1, group_replay=True):
+                 fused=True, resident=None, group=1, group_replay=True, inline_shared=False):
         """``resident`` = (int32 [steps][R][nblk] block tables, tokens per
         block) runs every anchor through the three-tier resolve, with the
         table of step t in place before step t."""
@@ -68,7 +68,7 @@ class Run:
                                       num_reqs=self.num_reqs, fused=fused,
                                       resident=None if resident is None else
                                       (self.res_dev, self.res_tok), sel_block_tokens=bt,
-                                      group_replay=group_replay)
+                                      group_replay=group_replay, inline_shared=inline_shared)
         # oracle
         self.oracle = {}
         for l in range(w.L):
@@ -146,7 +146,7 @@ class Run:
             np.testing.assert_array_equal(mc[:nr], o.miss_count[:nr], err_msg=f"miss count {a}")
             if check_page_table:
                 np.testing.assert_array_equal(pt, o.page_table, err_msg=f"page table {a}")
-            if fl:  # the recorded plan: the same (pos, slot) fetches, by position
+            if fl and not self.step_runner.inline_shared:  # the recorded plan, by position
                 c, pp, ps = self.hs.export_plan(a)
                 for r in range(nr):
                     got = sorted(zip(pp[r, :c[r]].tolist(), ps[r, :c[r]].tolist()))

@@ -157,11 +157,11 @@ def test_separate_writeback_launch(lookup):
     _run_all(get("dsa").scaled(R=4, groups=2, L_ctx=32768, steps=8), lookup=lookup, fused=False)
 
 
-@pytest.mark.parametrize("group_replay", [True, False])
-def test_write_through_with_shared_layers(group_replay):
+@pytest.mark.parametrize("mode", ["group", "layer", "inline"])
+def test_write_through_with_shared_layers(mode):
     """Write-through on anchors (fused) and on shared layers (own launch)."""
     _run_all(get("shared").scaled(R=3, groups=2, L_ctx=8192, steps=6, write_through=True),
-             group_replay=group_replay)
+             group_replay=mode == "group", inline_shared=mode == "inline")
 
 
 def test_quest_workload_scaled():
@@ -169,11 +169,13 @@ def test_quest_workload_scaled():
     _run_all(get("quest").scaled(R=4, groups=2, L_ctx=2048, steps=12))
 
 
-@pytest.mark.parametrize("group_replay", [True, False])
-def test_shared_workload_scaled(group_replay):
-    """Anchor + 3 shared layers replaying the plan (fewer requests, shorter
-    context); one replay launch per group, or one per shared layer."""
-    _run_all(get("shared").scaled(R=6, groups=2, L_ctx=16384, steps=10), group_replay=group_replay)
+@pytest.mark.parametrize("mode", ["group", "layer", "inline"])
+def test_shared_workload_scaled(mode):
+    """Anchor + 3 shared layers (fewer requests, shorter context): one replay
+    launch per group, one per shared layer, or the shared layers filled
+    inside the anchor's RESOLVE."""
+    _run_all(get("shared").scaled(R=6, groups=2, L_ctx=16384, steps=10),
+             group_replay=mode == "group", inline_shared=mode == "inline")
 
 
 @pytest.mark.parametrize("followers", [1, 8, 11])
@@ -181,6 +183,34 @@ def test_group_replay_many_layers(followers):
     """One anchor with 1, 8 (one launch) and 11 (two launches) shared layers."""
     _run_all(get("shared").scaled(R=3, groups=1, followers=followers, L_ctx=4096, steps=5),
              replay_ctas=3)
+
+
+@pytest.mark.parametrize("cs", [1, 3, 0])
+@pytest.mark.parametrize("followers", [1, 8])
+def test_inline_shared_layers(followers, cs):
+    """Shared layers filled inside the anchor's launch, every cluster shape."""
+    _run_all(get("shared").scaled(R=3, groups=2, followers=followers, L_ctx=4096, steps=5),
+             inline_shared=True, ctas_per_request=cs)
+
+
+def test_inline_shared_from_mirror_and_limits():
+    """FROM_MIRROR reads every layer's mirror; 9 shared layers are refused
+    (EBOUND); the hash lookup refuses the flag (EINVAL)."""
+    _run_all(get("shared").scaled(R=2, groups=1, L_ctx=2048, steps=4), inline_shared=True,
+             flags=H.FROM_MIRROR, mirror=True)
+    for followers, lookup, code in ((9, H.LOOKUP_PAGE_TABLE, H.EBOUND),
+                                    (2, H.LOOKUP_HASH, H.EINVAL)):
+        w = get("shared").scaled(R=2, groups=1, followers=followers, L_ctx=1024, steps=2)
+        mem = WorkloadMemory(w.R, w.L, w.B, w.P, w.rec)
+        hs = HiSparse(w.R, w.L, w.k, w.B, w.P, w.rec, mem.layer_buffers(),
+                      anchor_of=w.anchor_of(), lookup=lookup)
+        sel = torch.full((w.R, w.k), -1, dtype=torch.int32, device="cuda")
+        out = torch.empty((w.R, w.k), dtype=torch.int32, device="cuda")
+        with pytest.raises(H.HiSparseError) as ei:
+            hs.resolve(0, sel, out, flags=H.WITH_SHARED)
+        assert ei.value.code == code
+        torch.cuda.synchronize()
+        hs.close(); mem.close()
 
 
 def test_group_replay_roles():
@@ -491,11 +521,11 @@ def test_admit_rejects_bad_entries():
 # ---------------------------------------------------------------------- #
 # Host pools with a shared-index group's layers interleaved row by row    #
 # ---------------------------------------------------------------------- #
-@pytest.mark.parametrize("group_replay", [True, False])
-def test_group_interleaved_host_layout_shared(group_replay):
+@pytest.mark.parametrize("mode", ["group", "layer", "inline"])
+def test_group_interleaved_host_layout_shared(mode):
     """Anchor + 3 shared layers with their host rows interleaved: same results."""
     _run_all(get("shared").scaled(R=4, groups=2, L_ctx=16384, steps=8), group=4,
-             group_replay=group_replay)
+             group_replay=mode == "group", inline_shared=mode == "inline")
 
 
 def test_group_interleaved_host_layout_write_through():
@@ -663,3 +693,10 @@ def test_num_reqs_zero_touches_nothing():
         assert (sp == -1).all() and (pt == -1).all() and (mc == 0).all()
     finally:
         run.close()
+
+
+@pytest.mark.parametrize("mode", ["group", "inline"])
+def test_interleaved_rows_from_mirror(mode):
+    """The HBM mirror of an interleaved pool has the pool's layout and strides."""
+    _run_all(get("shared").scaled(R=2, groups=2, L_ctx=2048, steps=4), group=4, mirror=True,
+             flags=H.FROM_MIRROR, inline_shared=mode == "inline")

@@ -1770,9 +1770,10 @@ int configure_resolve(hisparse_handle *h, int want_cs) {
     fns[3] = reinterpret_cast<const void *>(&resolve_pt_kernel<true, true>);
     nf = 4;
   }
-  uint32_t smax = 0;
-  for (int cs = 1; cs <= 16; ++cs) smax = std::max(smax, resolve_smem(h, cs));
-  // dynamic + static shared memory within the device's opt-in limit per block
+  // Dynamic + static shared memory must stay within the device's opt-in limit
+  // per block.  The layout shrinks with the cluster size (a worker's slice is
+  // k / (cs - 1) selections), so a cluster size is a candidate only if its
+  // layout fits; the attribute covers the largest candidate.
   int optin = 0;
   HS_CUDA(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device));
   size_t stat = 0;
@@ -1781,7 +1782,13 @@ int configure_resolve(hisparse_handle *h, int want_cs) {
     HS_CUDA(cudaFuncGetAttributes(&fa, fns[i]));
     stat = std::max(stat, fa.sharedSizeBytes);
   }
-  if (static_cast<size_t>(smax) + stat > static_cast<size_t>(optin)) return HISPARSE_EBOUND;
+  auto fits = [&](int cs) {
+    return static_cast<size_t>(resolve_smem(h, cs)) + stat <= static_cast<size_t>(optin);
+  };
+  uint32_t smax = 0;
+  for (int cs = 1; cs <= 16; ++cs)
+    if (fits(cs)) smax = std::max(smax, resolve_smem(h, cs));
+  if (smax == 0) return HISPARSE_EBOUND;
   for (int i = 0; i < nf; ++i) {
     HS_CUDA(cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smax));
     HS_CUDA(cudaFuncSetAttribute(fns[i], cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
@@ -1805,18 +1812,24 @@ int configure_resolve(hisparse_handle *h, int want_cs) {
     }
     return n;
   };
-  int cs = 1;
+  int cs = 0;
   if (want_cs > 0) {
-    if (want_cs > 16) return HISPARSE_EBOUND;
+    if (want_cs > 16 || !fits(want_cs)) return HISPARSE_EBOUND;
     if (active_clusters(want_cs) < 1) return HISPARSE_EBOUND;
     cs = want_cs;
   } else {
     for (int c = std::min(16, h->sm_count / h->R); c >= 2; --c) {
-      if (active_clusters(c) >= h->R) {
+      if (fits(c) && active_clusters(c) >= h->R) {
         cs = c;
         break;
       }
     }
+    // else one CTA per request; with a layout too large for that, the largest
+    // cluster that fits and runs at all
+    if (cs == 0 && fits(1)) cs = 1;
+    for (int c = 16; cs == 0 && c >= 2; --c)
+      if (fits(c) && active_clusters(c) >= 1) cs = c;
+    if (cs == 0) return HISPARSE_EBOUND;
   }
   h->cs = cs;
   h->smem = resolve_smem(h, cs);

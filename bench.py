@@ -70,6 +70,9 @@ def parse():
     ap.add_argument("--L-ctx", type=int, default=0,
                     help="override the workload's prefill length (host pool size)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-copy", choices=("sm", "engine"), default="sm",
+                    help="end-to-end pass: copy each step's inputs and results with SM "
+                         "threads (hisparse_copy) or with the copy engines (cudaMemcpyAsync)")
     ap.add_argument("--replay", choices=("group", "layer", "inline"), default="group",
                     help="shared-index layers: one replay launch per anchor (group), one "
                          "per layer (layer, as the pages describe), or filled inside the "
@@ -335,7 +338,7 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
     from host_offload_serving_gb300 import hisparse as H
-    from host_offload_serving_gb300.runtime import HiSparse, WorkloadMemory, DecodeStep
+    from host_offload_serving_gb300.runtime import HiSparse, WorkloadMemory, DecodeStep, sm_copy
     from workload import get, records as REC, sweep_workload
     from workload.traces import all_traces
 
@@ -784,14 +787,20 @@ def run_ours(args):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.stream(cap):
                 with torch.cuda.graph(g, stream=cap):
-                    d_pack.copy_(h_pack[t], non_blocking=True)
+                    if args.e2e_copy == "sm":
+                        sm_copy(d_pack, h_pack[t])
+                    else:
+                        d_pack.copy_(h_pack[t], non_blocking=True)
                     if res_all is not None:
                         runner.resident = (res_all[t], res_tok)
                     runner.issue(view(d_pack, "sel"), out,
                                  newest=view(d_pack, "newest") if wt else None,
                                  wb_pos=view(d_pack, "wb") if (wt and t > 0) else None,
                                  new_rows=view(d_pack, "new") if wt else None)
-                    h_out[t].copy_(out, non_blocking=True)
+                    if args.e2e_copy == "sm":
+                        sm_copy(h_out[t], out)
+                    else:
+                        h_out[t].copy_(out, non_blocking=True)
             e_graphs.append(g)
         for burn in range(0 if args.no_burn_in else args.burn_in):   # as for pass 1
             hs.reset()
@@ -819,7 +828,9 @@ def run_ours(args):
                "unit": "selections/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
                "mode": "per-step CUDA graph built through the C ABI; the step's inputs packed "
                        "in one pinned buffer copied up, and its slot vectors copied back, inside "
-                       "the timed region"}
+                       "the timed region, " + ("by SM threads (hisparse_copy)"
+                                              if args.e2e_copy == "sm" else
+                                              "by the copy engines (cudaMemcpyAsync)")}
         flags |= hs.status()[0]
 
     peaks, peak_src = measured_peaks()

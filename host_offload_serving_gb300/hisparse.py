@@ -51,6 +51,7 @@ SIGNATURES = [
     ("hisparse_admit", _i32, [_vp, _i32, _vp, _i32, _vp, _vp]),
     ("hisparse_writeback", _i32, [_vp, _i32, _vp, _vp, _vp, _vp]),
     ("hisparse_prefetch_plan", _i32, [_vp, _i32, _i32, _vp, _vp]),
+    ("hisparse_copy", _i32, [_vp, _vp, _i64, _vp]),
     ("hisparse_copy_miss_counts", _i32, [_vp, _i32, _vp, _vp]),
     ("hisparse_get_status", _i32, [_vp, ctypes.POINTER(_u32), _vp]),
     ("hisparse_export_state", _i32, [_vp, _i32, _vp, _vp, _vp, _vp]),
@@ -152,6 +153,10 @@ def hisparse_writeback(h, layer, d_pos, d_new_rows, d_num_reqs, stream):
 
 def hisparse_prefetch_plan(h, anchor_layer, follower_layer, d_num_reqs, stream):
     return load().hisparse_prefetch_plan(h, anchor_layer, follower_layer, d_num_reqs, stream)
+
+
+def hisparse_copy(dst, src, nbytes, stream):
+    return load().hisparse_copy(dst, src, nbytes, stream)
 
 
 def hisparse_copy_miss_counts(h, layer, d_dst, stream):

@@ -71,6 +71,15 @@ def _stream(s):
     return s.cuda_stream
 
 
+def sm_copy(dst, src, stream=None):
+    """Copy tensor ``src`` into tensor ``dst`` (same byte size, a multiple of
+    16) with SM threads (``hisparse_copy``); either may be pinned host memory."""
+    nb = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != nb:
+        raise ValueError("sm_copy: sizes differ")
+    H.check(H.hisparse_copy(_ptr(dst), _ptr(src), nb, _stream(stream)), "hisparse_copy")
+
+
 class HiSparse:
     """One instance of the C library (R requests, L layers, k, B, P, record)."""
 

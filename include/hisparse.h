@@ -307,6 +307,16 @@ int hisparse_writeback(hisparse_handle *h, int32_t layer, const int32_t *d_pos,
 int hisparse_prefetch_plan(hisparse_handle *h, int32_t anchor_layer, int32_t follower_layer,
                            const int32_t *d_num_reqs, void *stream);
 
+/* Copy `bytes` (a multiple of 16) from src to dst with SM threads, on
+ * `stream`, after the stream's previous work (graph-capturable, no
+ * synchronisation).  Either side may be device memory or pinned host memory
+ * mapped for the device (hisparse_host_alloc, cudaHostAlloc); both 16-byte
+ * aligned, not overlapping.  This is not part of the pages' method: it moves a
+ * decode step's inputs and results between host and HBM over the coherent
+ * host link with less latency than a copy engine for transfers of a few
+ * hundred KB.  Errors: EINVAL (NULL, misaligned, bad size), ECUDA. */
+int hisparse_copy(void *dst, const void *src, int64_t bytes, void *stream);
+
 /* Copy the per-request miss counts of one anchor layer's last resolve
  * (int32 [R]) to device memory d_dst, asynchronously on `stream` (no
  * synchronisation; graph-capturable).  Errors: EINVAL, EROLE, ECUDA. */

@@ -700,3 +700,28 @@ def test_interleaved_rows_from_mirror(mode):
     """The HBM mirror of an interleaved pool has the pool's layout and strides."""
     _run_all(get("shared").scaled(R=2, groups=2, L_ctx=2048, steps=4), group=4, mirror=True,
              flags=H.FROM_MIRROR, inline_shared=mode == "inline")
+
+
+def test_sm_copy_between_host_and_device():
+    """hisparse_copy moves bytes exactly host->device, device->host and
+    device->device, for sizes from one 16-byte chunk to several MB; bad
+    sizes and alignments are refused."""
+    from host_offload_serving_gb300.runtime import sm_copy
+    rng = np.random.default_rng(5)
+    for nb in (16, 4096 + 16, 299_168, 3 << 20):
+        h = torch.from_numpy(rng.integers(0, 256, nb, dtype=np.uint8)).pin_memory()
+        d = torch.empty(nb, dtype=torch.uint8, device="cuda")
+        d2 = torch.empty(nb, dtype=torch.uint8, device="cuda")
+        back = torch.zeros(nb, dtype=torch.uint8).pin_memory()
+        sm_copy(d, h)
+        sm_copy(d2, d)
+        sm_copy(back, d2)
+        torch.cuda.synchronize()
+        assert torch.equal(back, h)
+        assert torch.equal(d.cpu(), h)
+    d = torch.empty(64, dtype=torch.uint8, device="cuda")
+    assert H.hisparse_copy(d.data_ptr(), d.data_ptr() + 32, 24, None) == H.EINVAL
+    assert H.hisparse_copy(d.data_ptr() + 8, d.data_ptr() + 32, 16, None) == H.EINVAL
+    assert H.hisparse_copy(None, d.data_ptr(), 16, None) == H.EINVAL
+    assert H.hisparse_copy(d.data_ptr(), d.data_ptr() + 32, 0, None) == H.OK
+    torch.cuda.synchronize()

@@ -21,12 +21,15 @@
 //     cluster barriers, no spin-waits.  The write-through of the previous
 //     token is fused in; the launch uses programmatic dependent launch.  A
 //     second instantiation adds the resident tier, block-id selections and
-//     the union of speculative verify rows.
+//     the union of speculative verify rows.  With HISPARSE_WITH_SHARED the
+//     workers also fill the anchor's shared-index layers at the same slots.
 //   resolve_kernel (HISPARSE_LOOKUP_HASH): the pages' stage order (hash
 //     staging, mark, scans, fetch by the whole cluster), kept as an ablation.
-//   replay_kernel, writeback_kernel, admit_kernel, reset_kernel: plan replay
-//     for shared-index layers, the separate write-through, admission with
-//     preload, and the reset state.
+//   replay_kernel: plan replay into one or several shared-index layers of an
+//     anchor (a record's rows for all of them back to back).
+//   writeback_kernel, admit_kernel, reset_kernel, copy_kernel: the separate
+//     write-through, admission with preload, the reset state, and copies by
+//     SM threads between pinned host memory and HBM.
 // Common to the fetches: the misses of a request are one flat run of 16-byte
 // chunks (miss j, chunk o), so no lane idles on records that are not a
 // multiple of 512 bytes (1152-byte records are 72 chunks), read with

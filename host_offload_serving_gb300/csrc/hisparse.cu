@@ -1621,6 +1621,7 @@ __global__ void __launch_bounds__(kReplayThreads) replay_kernel(const ReplayArgs
 // previous kernel of the stream, and lets the next one be set up at once.
 // ---------------------------------------------------------------------------
 constexpr int kCopyThreads = 256;
+constexpr int kCopyMaxCtas = 128;  // 2 MB in flight at most (32 CTAs measured no better)
 __global__ void __launch_bounds__(kCopyThreads) copy_kernel(uint4 *dst, const uint4 *src, int64_t n) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -2419,7 +2420,7 @@ int hisparse_copy(void *dst, const void *src, int64_t bytes, void *stream) {
   const int64_t n = bytes / 16;
   const int64_t per_cta = static_cast<int64_t>(kCopyThreads) * 4;
   cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3(static_cast<unsigned>(std::min<int64_t>((n + per_cta - 1) / per_cta, 128)));
+  lc.gridDim = dim3(static_cast<unsigned>(std::min<int64_t>((n + per_cta - 1) / per_cta, kCopyMaxCtas)));
   lc.blockDim = dim3(kCopyThreads);
   lc.stream = static_cast<cudaStream_t>(stream);
   cudaLaunchAttribute at[1];

@@ -725,3 +725,17 @@ def test_sm_copy_between_host_and_device():
     assert H.hisparse_copy(None, d.data_ptr(), 16, None) == H.EINVAL
     assert H.hisparse_copy(d.data_ptr(), d.data_ptr() + 32, 0, None) == H.OK
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("name", ["quest", "shared"])
+def test_full_size_config(name):
+    """The Quest-style and shared-index configs at full size (every request,
+    layer and step; 53.7 GB and 77.3 GB host pools): slot vectors, state, plans
+    and every hot byte equal the oracle's at the first and the last step."""
+    _run_all(get(name), every=10 ** 9)
+
+
+def test_capacity_sweep_point_at_bench_size():
+    """A capacity-sweep point at the size the bench runs it (64 requests x 2
+    layers, 16 steps, a quarter of the 1M context: 38.6 GB host pool)."""
+    _run_all(sweep_workload(4096, 0.87, L_ctx=262144), every=10 ** 9)

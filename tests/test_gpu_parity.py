@@ -352,10 +352,12 @@ def test_resident_tier_dsa_full_size():
     _run_all(w, every=4, resident=(resident_tables(w, 64, full=4, window=4096), 64))
 
 
-def test_resident_tier_shared_layers():
-    """Anchors resolved with the resident tier; shared layers replay their plans."""
+@pytest.mark.parametrize("inline", [False, True])
+def test_resident_tier_shared_layers(inline):
+    """Anchors resolved with the resident tier; shared layers replay their
+    plans, or are filled inside the anchor's launch."""
     w = get("shared").scaled(R=3, groups=2, L_ctx=8192, steps=6)
-    _run_all(w, resident=(resident_tables(w, 16, full=1, window=512), 16))
+    _run_all(w, resident=(resident_tables(w, 16, full=1, window=512), 16), inline_shared=inline)
 
 
 def test_resident_all_and_errors():
@@ -452,10 +454,12 @@ def test_union_verify_rows_full_size():
     _run_all(w, every=4, traces=_verify_row_traces(w, 4), flags=H.UNION)
 
 
-def test_union_with_shared_layers_and_resident_tier():
+@pytest.mark.parametrize("inline", [False, True])
+def test_union_with_shared_layers_and_resident_tier(inline):
+    """Repeated misses (union) are fetched once for the shared layers too."""
     w = get("shared").scaled(R=3, groups=2, L_ctx=8192, steps=6, k=512, B=1024)
     _run_all(w, traces=_verify_row_traces(w, 2), flags=H.UNION,
-             resident=(resident_tables(w, 16, full=0, window=256), 16))
+             resident=(resident_tables(w, 16, full=0, window=256), 16), inline_shared=inline)
 
 
 def test_union_repeats_are_not_errors():

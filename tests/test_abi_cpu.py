@@ -133,3 +133,16 @@ def test_resolve_ex_without_a_handle_is_rejected():
     o = H.ResolveOptions(None, None, 0x1000, 4, 64, 1)
     assert H.hisparse_resolve_ex(None, 0, 0x10, None, None, o, 0x20, 0, None) == H.EINVAL
     assert H.hisparse_resolve_ex(None, 0, 0x10, None, None, None, 0x20, 0, None) == H.EINVAL
+
+
+def test_copy_argument_checks_need_no_gpu():
+    """hisparse_copy refuses bad sizes and alignments before touching CUDA;
+    zero bytes is a no-op.  A shared-layer replay on no handle is refused."""
+    lib = H.load()
+    assert H.hisparse_copy(0x1000, 0x2000, 24, None) == H.EINVAL      # not a multiple of 16
+    assert H.hisparse_copy(0x1008, 0x2000, 32, None) == H.EINVAL      # misaligned destination
+    assert H.hisparse_copy(0x1000, 0x2004, 32, None) == H.EINVAL      # misaligned source
+    assert H.hisparse_copy(None, 0x2000, 32, None) == H.EINVAL
+    assert H.hisparse_copy(0x1000, 0x2000, -16, None) == H.EINVAL
+    assert H.hisparse_copy(0x1000, 0x2000, 0, None) == H.OK
+    assert lib.hisparse_prefetch_plan(None, 0, -1, None, None) == H.EINVAL

@@ -183,11 +183,13 @@ int hisparse_destroy(hisparse_handle *h);
  * The host pool rows fetched must be complete when this runs (order any
  * write-back before it with an event), and hot row B must already hold the
  * newest token's KV.  flags: HISPARSE_RECORD_PLAN | HISPARSE_SKIP_IO |
- * HISPARSE_FROM_MIRROR.  With the page-table lookup the kernel is launched
+ * HISPARSE_FROM_MIRROR | HISPARSE_UNION | HISPARSE_WITH_SHARED (the last two
+ * with the page-table lookup only; EINVAL otherwise, and EBOUND for
+ * WITH_SHARED on more than 8 shared-index layers).  With the page-table lookup the kernel is launched
  * with programmatic dependent launch: it may be set up while the previous
  * kernel of `stream` finishes but reads no memory before that kernel is done,
  * and the next kernel, if launched the same way, may be set up while this one
- * runs.  Errors: EINVAL, EROLE (layer is a follower), ECUDA. */
+ * runs.  Errors: EINVAL, EBOUND, EROLE (layer is a follower), ECUDA. */
 int hisparse_resolve(hisparse_handle *h, int32_t layer, const int32_t *d_sel,
                      const int32_t *d_num_reqs, const int32_t *d_newest, int32_t *d_out,
                      uint32_t flags, void *stream);

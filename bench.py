@@ -190,11 +190,15 @@ def token_traces(w, traces):
     return out
 
 
-def cpu_oracle_rate(w, traces, host_views=None, budget_s=10.0, union=False):
+def cpu_oracle_rate(w, traces, host_views=None, budget_s=10.0, union=False, warmup=0,
+                    steps=None):
     """The C oracle (single thread) on the same workload's steps: selections/s.
 
     ``host_views[l]`` is a uint8 [R][>=L_ctx][rec] view of layer l's host rows
     (rows below L_ctx are read-only input); without it the rows are generated.
+    With ``steps``, the first ``warmup`` steps run untimed and exactly the next
+    ``steps`` are timed; otherwise steps from 0 are timed until the trace or
+    ``budget_s`` ends.
     """
     import numpy as np
     from oracle.coracle import OracleLayer
@@ -218,7 +222,10 @@ def cpu_oracle_rate(w, traces, host_views=None, budget_s=10.0, union=False):
     sel_total, miss_bytes, steps_done, t_total = 0, 0, 0, 0.0
     t_start = time.perf_counter()
     t = 0
+    timed_from = warmup if steps is not None else 0
     while True:
+        if t == timed_from:
+            sel_total, miss_bytes, steps_done, t_total = 0, 0, 0, 0.0
         t0 = time.perf_counter()
         if w.write_through:
             for l in range(w.L):
@@ -235,10 +242,15 @@ def cpu_oracle_rate(w, traces, host_views=None, budget_s=10.0, union=False):
         sel_total += len(anchors) * w.R * w.k
         steps_done += 1
         t += 1
-        if t >= w.steps or time.perf_counter() - t_start > budget_s:
+        if steps is not None:
+            if t >= warmup + steps:
+                break
+        elif t >= w.steps or time.perf_counter() - t_start > budget_s:
             break
+    which = (f"decode steps {timed_from}..{timed_from + steps_done - 1} (after {timed_from} "
+             f"untimed)" if steps is not None else f"first {steps_done} decode steps")
     return {"value": sel_total / t_total, "unit": "selections/s", "cores": 1, "kind": "oracle",
-            "sample": f"first {steps_done} decode steps of the {w.name} workload "
+            "sample": f"{which} of the {w.name} workload "
                       f"({w.R} requests x {w.L} layers, k={w.k}, B={w.B}), plain C oracle, "
                       f"one thread, record copies included, trace generation excluded",
             "miss_bytes_per_s": miss_bytes / t_total, "seconds": t_total,
@@ -306,12 +318,15 @@ def run_reference(args):
     from workload import get
     from workload.traces import all_traces
     w = get(args.workload)
-    w = w.scaled(steps=max(w.steps, args.warmup + args.steps)) if w.write_through else w
+    if args.L_ctx:
+        w = w.scaled(L_ctx=args.L_ctx)
+    w = w.scaled(steps=max(w.steps, args.warmup + args.steps))
     traces = all_traces(w)
-    res = cpu_oracle_rate(w, token_traces(w, traces), budget_s=60.0)
+    # the same warm-up and timed steps as the GPU arm, the oracle as it stands
+    res = cpu_oracle_rate(w, token_traces(w, traces), warmup=args.warmup, steps=args.steps)
     steps = res["steps"]
     line = {"impl": "reference", "metric": METRIC, "value": res["value"], "unit": "selections/s",
-            "n_gpus": args.gpus, "steps": steps, "warmup": 0,
+            "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * res["seconds"] / res["steps"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
             "data": "synthetic", "config": {"workload": w.name, "requests": w.R, "layers": w.L,

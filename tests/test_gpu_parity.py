@@ -743,3 +743,43 @@ def test_capacity_sweep_point_at_bench_size():
     """A capacity-sweep point at the size the bench runs it (64 requests x 2
     layers, 16 steps, a quarter of the 1M context: 38.6 GB host pool)."""
     _run_all(sweep_workload(4096, 0.87, L_ctx=262144), every=10 ** 9)
+
+
+def test_graph_with_host_inputs_and_outputs_by_sm_copy():
+    """A step graph that copies its selections up from pinned host memory and
+    its slot vectors back with hisparse_copy (the end-to-end form): every
+    step's host-side slot vector equals the oracle's."""
+    from host_offload_serving_gb300.runtime import sm_copy
+    from workload.traces import layer_traces
+    w = get("tiny").scaled(steps=12)
+    mem = WorkloadMemory(w.R, w.L, w.B, w.P, w.rec)
+    from workload import records as REC
+    REC.fill_host_pool(w, mem.geometry)
+    hs = HiSparse(w.R, w.L, w.k, w.B, w.P, w.rec, mem.layer_buffers())
+    o = OracleLayer(w.R, w.k, w.B, w.P, w.rec, host=mem.host_view(0))
+    o.reset()
+    sel, _ = layer_traces(w, 0)
+    h_sel = torch.from_numpy(np.ascontiguousarray(sel)).pin_memory()        # [T][R][k]
+    h_out = torch.full((w.steps, w.R, w.k), -7, dtype=torch.int32).pin_memory()
+    d_sel = torch.empty((w.R, w.k), dtype=torch.int32, device="cuda")
+    d_out = torch.empty((w.R, w.k), dtype=torch.int32, device="cuda")
+    cap = torch.cuda.Stream()
+    graphs = []
+    for t in range(w.steps):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                s = torch.cuda.current_stream()
+                sm_copy(d_sel, h_sel[t], stream=s)
+                hs.resolve(0, d_sel, d_out, stream=s)
+                sm_copy(h_out[t], d_out, stream=s)
+        graphs.append(g)
+    torch.cuda.synchronize()
+    for t in range(w.steps):
+        graphs[t].replay()
+        ref, e = o.resolve(sel[t])
+        assert e == 0
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(h_out[t].numpy(), ref)
+    assert np.array_equal(mem.hot[0].cpu().numpy(), o.hot)
+    hs.close(); mem.close()

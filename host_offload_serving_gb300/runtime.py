@@ -10,10 +10,14 @@
                  compute stream: wait for the write-through, place the new
                                  token's KV in row B, RESOLVE each anchor
                                  (recording its plan when it has followers)
-                 side stream   : after each anchor, replay its plan into each
-                                 follower, one event per follower
-               No call in a step allocates or reads device values on the host,
-               so a whole step can be captured in a CUDA graph.
+                 side stream   : after each anchor, replay its plan into its
+                                 followers (one launch for all of them, or one
+                                 per follower), events per follower
+               or, with ``inline_shared``, the followers filled inside the
+               anchor's RESOLVE launch.  No call in a step allocates or reads
+               device values on the host, so a whole step can be captured in a
+               CUDA graph.
+``sm_copy``    host <-> HBM copies by SM threads (``hisparse_copy``).
 
 torch is used for device memory, streams, events and graphs only; every byte
 and index of the hot path is produced by the kernels in ``libhisparse.so``.

@@ -731,18 +731,34 @@ def test_sm_copy_between_host_and_device():
     torch.cuda.synchronize()
 
 
+def _need_host_memory(nbytes):
+    """Skip (with the reason) when the host cannot pin a pool of nbytes plus
+    a margin; the pool is pinned memory, which the kernel cannot swap."""
+    avail = 0
+    with open("/proc/meminfo") as f:
+        for line in f:
+            if line.startswith("MemAvailable:"):
+                avail = int(line.split()[1]) * 1024
+    if avail < nbytes + (16 << 30):
+        pytest.skip(f"needs {nbytes / 2**30:.1f} GiB of host memory plus 16 GiB, "
+                    f"{avail / 2**30:.1f} GiB available")
+
+
 @pytest.mark.parametrize("name", ["quest", "shared"])
 def test_full_size_config(name):
     """The Quest-style and shared-index configs at full size (every request,
     layer and step; 53.7 GB and 77.3 GB host pools): slot vectors, state, plans
     and every hot byte equal the oracle's at the first and the last step."""
+    _need_host_memory(get(name).host_bytes())
     _run_all(get(name), every=10 ** 9)
 
 
 def test_capacity_sweep_point_at_bench_size():
     """A capacity-sweep point at the size the bench runs it (64 requests x 2
     layers, 16 steps, a quarter of the 1M context: 38.6 GB host pool)."""
-    _run_all(sweep_workload(4096, 0.87, L_ctx=262144), every=10 ** 9)
+    w = sweep_workload(4096, 0.87, L_ctx=262144)
+    _need_host_memory(w.host_bytes())
+    _run_all(w, every=10 ** 9)
 
 
 def test_graph_with_host_inputs_and_outputs_by_sm_copy():

@@ -123,7 +123,8 @@ struct LayerDev {              // one layer's buffers, device-visible addresses
   int64_t host_req_stride, host_row_stride;
   char *hot;
   int64_t hot_req_stride, hot_row_stride;
-  const char *mirror;
+  char *mirror;                // HBM mirror of the host pool (same strides) or null;
+                               // every write-back stores to it as well
 };
 
 struct WritebackArgs {
@@ -658,6 +659,7 @@ struct PtArgs {
   const int32_t *prev_pos;
   const char *new_rows;
   char *host_w;
+  char *mirror_w;  // the layer's HBM mirror (null if none): written back alongside
   int64_t host_req_stride, host_row_stride;
   int32_t prev_from_row;
   // Resident tier (three-tier resolve): per request a block table
@@ -1189,6 +1191,11 @@ __device__ void pt_leader_publish(const PtArgs &a, int r, int32_t prev, int32_t 
     uint4 *hrow = reinterpret_cast<uint4 *>(a.host_w + static_cast<int64_t>(r) * a.host_req_stride +
                                             static_cast<int64_t>(prev) * a.host_row_stride);
     for (int c = tid; c < a.rec16; c += kThreads) st_v4(hrow + c, keep[c]);
+    if (a.mirror_w) {  // the mirror stays a byte-for-byte copy of the host pool
+      uint4 *mrow = reinterpret_cast<uint4 *>(a.mirror_w + static_cast<int64_t>(r) * a.host_req_stride +
+                                              static_cast<int64_t>(prev) * a.host_row_stride);
+      for (int c = tid; c < a.rec16; c += kThreads) st_v4(mrow + c, keep[c]);
+    }
   }
   const int32_t *l_slotpos = reinterpret_cast<const int32_t *>(smem + L.l_slotpos);
   const int16_t *l_newlru = reinterpret_cast<const int16_t *>(smem + L.l_newlru);
@@ -1522,9 +1529,17 @@ __global__ void __launch_bounds__(128) writeback_kernel(const WritebackArgs a) {
   const uint4 *nr = a.new_rows ? reinterpret_cast<const uint4 *>(
                                      a.new_rows + (static_cast<int64_t>(li) * a.R + r) * a.rec16 * 16)
                                : nullptr;
-  // each thread moves its own chunks: old row B out first, then the new token in
+  uint4 *m = Ld.mirror ? reinterpret_cast<uint4 *>(Ld.mirror + static_cast<int64_t>(r) * Ld.host_req_stride +
+                                                   static_cast<int64_t>(wb ? p : 0) * Ld.host_row_stride)
+                       : nullptr;
+  // each thread moves its own chunks: old row B out first (to the host pool and
+  // its HBM mirror), then the new token in
   for (int c = threadIdx.x; c < a.rec16; c += blockDim.x) {
-    if (wb) st_v4(d + c, row[c]);
+    const uint4 v = row[c];
+    if (wb) {
+      st_v4(d + c, v);
+      if (m) st_v4(m + c, v);
+    }
     if (nr) row[c] = nr[c];
   }
 }
@@ -1533,21 +1548,32 @@ __global__ void __launch_bounds__(128) writeback_kernel(const WritebackArgs a) {
 // Plan replay for a shared-index layer ([DD] §3.6, §5.6).  The plan's records
 // (every request's, back to back) are split evenly over a small grid; a CTA
 // resolves a batch of its records to source and destination rows once, into
-// shared memory, then streams the batch's 16-byte chunks with kReplayDepth
-// host loads in flight per thread.  Nothing on the load path waits on a global
+// shared memory, orders the batch by source address (so that records of
+// nearby host pages are read together, as RESOLVE orders each slice's
+// fetches), then streams the batch's 16-byte chunks with kReplayDepth host
+// loads in flight per thread.  Nothing on the load path waits on a global
 // read of the plan.
 // ---------------------------------------------------------------------------
 constexpr int kReplayThreads = 512;
-constexpr int kReplayBatch = 512;  // plan records resolved to rows per round
+constexpr int kReplayBatch = 512;  // plan records resolved to rows per round (== threads)
 constexpr int kReplayDepth = 8;    // 16-byte host loads in flight per thread
+static_assert(kReplayBatch == kReplayThreads, "one batch entry per thread in the ordering");
 
 __host__ __device__ inline int replay_pref_bytes(int R) { return ((R + 1) * 4 + 15) & ~15; }
+__host__ __device__ inline size_t replay_smem_bytes(int R) {
+  // prefix [R + 1], then source and destination rows of a batch in resolve
+  // order, then the same two in source-address order
+  return static_cast<size_t>(replay_pref_bytes(R)) + 4 * sizeof(char *) * kReplayBatch;
+}
 
 __global__ void __launch_bounds__(kReplayThreads) replay_kernel(const ReplayArgs a) {
   extern __shared__ __align__(16) unsigned char rsm[];
   int32_t *s_pref = reinterpret_cast<int32_t *>(rsm);  // [R + 1] exclusive prefix of plan counts
-  const char **s_src = reinterpret_cast<const char **>(rsm + replay_pref_bytes(a.R));  // [kReplayBatch]
-  char **s_dst = reinterpret_cast<char **>(rsm + replay_pref_bytes(a.R) + sizeof(char *) * kReplayBatch);
+  unsigned char *rows = rsm + replay_pref_bytes(a.R);  // four arrays of kReplayBatch pointers
+  const char **s_src0 = reinterpret_cast<const char **>(rows);
+  char **s_dst0 = reinterpret_cast<char **>(rows + sizeof(char *) * kReplayBatch);
+  const char **s_src = reinterpret_cast<const char **>(rows + 2 * sizeof(char *) * kReplayBatch);
+  char **s_dst = reinterpret_cast<char **>(rows + 3 * sizeof(char *) * kReplayBatch);
   const int tid = threadIdx.x;
   const int nreq = a.num_reqs ? min(*a.num_reqs, a.R) : a.R;
   if (tid < 32) {
@@ -1585,10 +1611,23 @@ __global__ void __launch_bounds__(kReplayThreads) replay_kernel(const ReplayArgs
       }
       const int64_t pk = static_cast<int64_t>(lo) * a.k + (m - s_pref[lo]);
       const ReplayTarget &T = a.f[f];
-      s_src[i] = T.src + static_cast<int64_t>(lo) * T.src_req_stride +
-                 static_cast<int64_t>(a.plan_pos[pk]) * T.src_row_stride;
-      s_dst[i] = T.hot + static_cast<int64_t>(lo) * T.hot_req_stride +
-                 static_cast<int64_t>(a.plan_slot[pk]) * T.hot_row_stride;
+      s_src0[i] = T.src + static_cast<int64_t>(lo) * T.src_req_stride +
+                  static_cast<int64_t>(a.plan_pos[pk]) * T.src_row_stride;
+      s_dst0[i] = T.hot + static_cast<int64_t>(lo) * T.hot_req_stride +
+                  static_cast<int64_t>(a.plan_slot[pk]) * T.hot_row_stride;
+    }
+    __syncthreads();
+    // entry i's rank among the batch by source address (ties by index: a
+    // permutation even if two entries read the same row)
+    if (tid < nb) {
+      const uintptr_t key = reinterpret_cast<uintptr_t>(s_src0[tid]);
+      int rnk = 0;
+      for (int x = 0; x < nb; ++x) {
+        const uintptr_t kx = reinterpret_cast<uintptr_t>(s_src0[x]);
+        rnk += kx < key || (kx == key && x < tid);
+      }
+      s_src[rnk] = s_src0[tid];
+      s_dst[rnk] = s_dst0[tid];
     }
     __syncthreads();
     const uint32_t n = static_cast<uint32_t>(nb) * rec16;
@@ -2076,7 +2115,7 @@ int hisparse_init(const hisparse_config *cfg, const hisparse_layer_buffers *laye
     d.hot = static_cast<char *>(b.hot);
     d.hot_req_stride = b.hot_req_stride;
     d.hot_row_stride = b.hot_row_stride;
-    d.mirror = static_cast<const char *>(b.mirror);
+    d.mirror = static_cast<char *>(b.mirror);
   }
 
   // Fetch-order buckets: about 2 MB of host rows each, at most kMaxBuckets.
@@ -2093,6 +2132,9 @@ int hisparse_init(const hisparse_config *cfg, const hisparse_layer_buffers *laye
 
   rc = configure_resolve(h, cfg->ctas_per_request);
   if (rc != HISPARSE_OK) return fail(rc);
+  e = cudaFuncSetAttribute(replay_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(replay_smem_bytes(R)));
+  if (e != cudaSuccess) return fail(cuda_fail(e));
 
   // one arena for all metadata
   auto al = [](int64_t x) { return (x + 255) & ~int64_t(255); };
@@ -2324,9 +2366,11 @@ int hisparse_resolve_ex(hisparse_handle *h, int32_t layer, const int32_t *d_sel,
     a.prev_pos = d_prev_pos;
     a.new_rows = static_cast<const char *>(d_new_rows);
     a.host_w = Ld.host_w;
+    a.mirror_w = Ld.mirror;
     a.host_req_stride = Ld.host_req_stride;
     a.host_row_stride = Ld.host_row_stride;
-    a.prev_from_row = (d_prev_pos && !(flags & HISPARSE_FROM_MIRROR)) ? 1 : 0;
+    // the host pool and its mirror hold the same bytes, so the kept row serves either source
+    a.prev_from_row = d_prev_pos ? 1 : 0;
     a.res_blocks = d_res_blocks;
     a.res_nblk = d_res_blocks ? res_max_blocks : 0;
     a.res_tok = d_res_blocks ? res_block_tokens : 1;
@@ -2392,7 +2436,7 @@ int hisparse_prefetch_plan(hisparse_handle *h, int32_t anchor_layer, int32_t fol
     for (int32_t l = 0; l < h->L; ++l)
       if (h->anchor_of[l] == anchor_layer) fl.push_back(l);
   const AnchorMeta &m = h->meta[anchor_layer];
-  const size_t smem = replay_pref_bytes(h->R) + 2 * sizeof(char *) * kReplayBatch;
+  const size_t smem = replay_smem_bytes(h->R);
   for (size_t f0 = 0; f0 < fl.size(); f0 += kMaxReplayTargets) {
     ReplayArgs a;
     a.R = h->R; a.k = h->k; a.rec16 = h->rec / 16; a.num_reqs = d_num_reqs;
@@ -2471,7 +2515,8 @@ int hisparse_export_state(hisparse_handle *h, int32_t layer, int32_t *slot_pos, 
 }
 
 int hisparse_import_state(hisparse_handle *h, int32_t layer, const int32_t *slot_pos,
-                          const int16_t *lru, const int32_t *page_table) {
+                          const int16_t *lru, const int32_t *page_table,
+                          const int32_t *miss_counts) {
   if (layer_ok(h, layer) || !slot_pos || !lru || !page_table) return HISPARSE_EINVAL;
   if (h->anchor_of[layer] != -1) return HISPARSE_EROLE;
   const int32_t B = h->B;
@@ -2501,6 +2546,7 @@ int hisparse_import_state(hisparse_handle *h, int32_t layer, const int32_t *slot
       ++mapped;
     }
     if (mapped != occupied) return HISPARSE_EINVAL;
+    if (miss_counts && (miss_counts[r] < 0 || miss_counts[r] > h->k)) return HISPARSE_EINVAL;
   }
   const AnchorMeta &m = h->meta[layer];
   HS_CUDA(cudaDeviceSynchronize());
@@ -2509,6 +2555,9 @@ int hisparse_import_state(hisparse_handle *h, int32_t layer, const int32_t *slot
   HS_CUDA(cudaMemcpy(m.lru, lru, 2 * RB, cudaMemcpyHostToDevice));
   HS_CUDA(cudaMemcpy(m.page_table, page_table, 4 * static_cast<size_t>(h->R) * P,
                      cudaMemcpyHostToDevice));
+  if (miss_counts)
+    HS_CUDA(cudaMemcpy(m.miss_count, miss_counts, 4 * static_cast<size_t>(h->R),
+                       cudaMemcpyHostToDevice));
   return HISPARSE_OK;
 }
 

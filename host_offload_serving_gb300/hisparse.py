@@ -55,7 +55,7 @@ SIGNATURES = [
     ("hisparse_copy_miss_counts", _i32, [_vp, _i32, _vp, _vp]),
     ("hisparse_get_status", _i32, [_vp, ctypes.POINTER(_u32), _vp]),
     ("hisparse_export_state", _i32, [_vp, _i32, _vp, _vp, _vp, _vp]),
-    ("hisparse_import_state", _i32, [_vp, _i32, _vp, _vp, _vp]),
+    ("hisparse_import_state", _i32, [_vp, _i32, _vp, _vp, _vp, _vp]),
     ("hisparse_export_plan", _i32, [_vp, _i32, _vp, _vp, _vp]),
     ("hisparse_reset", _i32, [_vp, _i32, _vp]),
     ("hisparse_get_info", _i32, [_vp, ctypes.POINTER(Info)]),
@@ -173,8 +173,8 @@ def hisparse_export_state(h, layer, slot_pos, lru, page_table, miss_counts):
     return load().hisparse_export_state(h, layer, slot_pos, lru, page_table, miss_counts)
 
 
-def hisparse_import_state(h, layer, slot_pos, lru, page_table):
-    return load().hisparse_import_state(h, layer, slot_pos, lru, page_table)
+def hisparse_import_state(h, layer, slot_pos, lru, page_table, miss_counts):
+    return load().hisparse_import_state(h, layer, slot_pos, lru, page_table, miss_counts)
 
 
 def hisparse_export_plan(h, layer, count, pos, slot):

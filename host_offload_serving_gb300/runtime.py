@@ -169,12 +169,14 @@ class HiSparse:
                                         pt.ctypes.data, mc.ctypes.data), "hisparse_export_state")
         return sp, lru, pt, mc
 
-    def import_state(self, layer, slot_pos, lru, page_table):
+    def import_state(self, layer, slot_pos, lru, page_table, miss_counts=None):
+        """Returns the C return code (validation failures are EINVAL)."""
         sp = np.ascontiguousarray(slot_pos, np.int32)
         lr = np.ascontiguousarray(lru, np.int16)
         pt = np.ascontiguousarray(page_table, np.int32)
+        mc = None if miss_counts is None else np.ascontiguousarray(miss_counts, np.int32)
         return H.hisparse_import_state(self.h, layer, sp.ctypes.data, lr.ctypes.data,
-                                       pt.ctypes.data)
+                                       pt.ctypes.data, None if mc is None else mc.ctypes.data)
 
     def export_plan(self, layer):
         c = np.empty(self.R, np.int32)

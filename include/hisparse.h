@@ -132,8 +132,12 @@ typedef struct {
   void *hot;                /* device memory, R x (B+1) rows */
   int64_t hot_req_stride;
   int64_t hot_row_stride;
-  const void *mirror;       /* optional device copy of host_pool with the host pool's
-                               strides (used only with HISPARSE_FROM_MIRROR); NULL if none */
+  void *mirror;             /* optional device copy of host_pool with the host pool's
+                               strides, read instead of the pool with
+                               HISPARSE_FROM_MIRROR; NULL if none.  The caller fills it;
+                               the library keeps it equal to the pool: every write-back
+                               (hisparse_writeback, the fused one of
+                               hisparse_resolve_step) stores the row to both. */
 } hisparse_layer_buffers;
 
 /* Read-only facts about an instance (for reporting). */
@@ -337,12 +341,17 @@ int hisparse_get_status(hisparse_handle *h, uint32_t *flags_out, int32_t *unit_e
 int hisparse_export_state(hisparse_handle *h, int32_t layer, int32_t *slot_pos, int16_t *lru,
                           int32_t *page_table, int32_t *miss_counts);
 
-/* Replace one anchor layer's state (checkpoint / test set-up).  The arrays
- * are validated first: every slot_pos in [-1, P) with no position twice, lru
- * a permutation of [0, B) per request, and page_table[p] == s exactly when
- * slot_pos[s] == p.  Synchronises.  Errors: EINVAL, EROLE, ECUDA. */
+/* Replace one anchor layer's state (checkpoint / test set-up): the arrays of
+ * hisparse_export_state.  slot_pos, lru and page_table are required;
+ * miss_counts may be NULL (the layer's miss counts are then left as they
+ * are).  The arrays are validated first: every slot_pos in [-1, P) with no
+ * position twice, lru a permutation of [0, B) per request, page_table[p] == s
+ * exactly when slot_pos[s] == p, and every miss count in [0, k].  Nothing is
+ * written unless all of it is valid.  Synchronises.
+ * Errors: EINVAL, EROLE, ECUDA. */
 int hisparse_import_state(hisparse_handle *h, int32_t layer, const int32_t *slot_pos,
-                          const int16_t *lru, const int32_t *page_table);
+                          const int16_t *lru, const int32_t *page_table,
+                          const int32_t *miss_counts);
 
 /* Copy one anchor layer's last miss plan to host arrays: count [R],
  * pos [R][k] int32, slot [R][k] int32 (only the first count[r] entries of a

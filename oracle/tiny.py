@@ -215,17 +215,6 @@ class Unit:
         self.miss_count = 0                # an admission is not a decode step
         return plan
 
-    def set_newest(self, record):
-        """The caller writes the new token's KV into row B ([P1] §3.4 step 4)."""
-        self.hot[self.B] = record
-
-    def writeback(self, pos, host_store):
-        """Write-through of the newest row to the host pool ([P1] §3.4 step 4)."""
-        host_store[pos] = self.hot[self.B]
-
-    def resident(self):
-        return {p for p in self.slot_pos if p >= 0}
-
 
 def expand_blocks(sel_blocks, block_tokens):
     """Token positions of a block-id selection list (gentlecold.top §5.5: a
@@ -241,17 +230,6 @@ def expand_blocks(sel_blocks, block_tokens):
         else:
             out.extend(b * block_tokens + j for j in range(block_tokens))
     return out
-
-
-def replay(plan, follower_hot, follower_host):
-    """Copy-only replay of an anchor's miss plan into a shared layer.
-
-    A shared layer keeps its slots in lockstep with its anchor, so the anchor's
-    ``(pos, slot)`` list is also the shared layer's list; only the bytes come
-    from the shared layer's own host pool ([P1] §3.6 and §5.6).
-    """
-    for p, s in plan:
-        follower_hot[s] = follower_host(p)
 
 
 # ---------------------------------------------------------------------- #

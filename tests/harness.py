@@ -23,6 +23,7 @@ class Run:
         table of step t in place before step t."""
         self.w = w
         self.flags = flags
+        self.lookup = lookup
         dev = torch.device("cuda", 0)
         self.mem = WorkloadMemory(w.R, w.L, w.B, w.P, w.rec, mirror=mirror, pool_kind=pool_kind,
                                   group=group)
@@ -131,8 +132,31 @@ class Run:
         self.t += 1
 
     # ------------------------------------------------------------------ #
-    def compare(self, check_bytes=True, check_page_table=True):
-        """Assert GPU == oracle on every field of every layer (synchronises)."""
+    def compare_light(self):
+        """Assert GPU == oracle on this step's slot vectors and miss counts
+        (the per-step outputs; cheap enough for every step at full size)."""
+        torch.cuda.synchronize()
+        nr = self.nreq_val
+        out = self.out.cpu().numpy()
+        np.testing.assert_array_equal(out[:, :nr], self.oracle_out[:, :nr],
+                                      err_msg=f"out slots after step {self.t - 1}")
+        mcd = torch.empty(self.w.R, dtype=torch.int32, device=self.out.device)
+        for a, _ in self.groups:
+            self.hs.copy_miss_counts(a, mcd)
+            mc = mcd.cpu().numpy()
+            np.testing.assert_array_equal(mc[:nr], self.oracle[a].miss_count[:nr],
+                                          err_msg=f"miss count {a} after step {self.t - 1}")
+
+    def compare(self, check_bytes=True, check_page_table=True, check_prefill=True):
+        """Assert GPU == oracle on every field of every layer (synchronises).
+
+        The plan is compared in list order with the page-table lookup (which
+        records it in list order) and as a set of (position, slot) pairs with
+        the hash lookup (which records it in host-row order).  With
+        ``check_prefill`` the host rows below L_ctx -- the rows the oracle
+        reads from the same pool -- are also checked against a fresh
+        generation of the records, so that a stray store into them cannot
+        pass unseen by changing both sides' input."""
         torch.cuda.synchronize()
         w = self.w
         nr = self.nreq_val
@@ -146,13 +170,18 @@ class Run:
             np.testing.assert_array_equal(mc[:nr], o.miss_count[:nr], err_msg=f"miss count {a}")
             if check_page_table:
                 np.testing.assert_array_equal(pt, o.page_table, err_msg=f"page table {a}")
-            if fl and not self.step_runner.inline_shared:  # the recorded plan, by position
+            if fl and not self.step_runner.inline_shared:  # the recorded plan
                 c, pp, ps = self.hs.export_plan(a)
+                in_order = self.lookup == H.LOOKUP_PAGE_TABLE
                 for r in range(nr):
-                    got = sorted(zip(pp[r, :c[r]].tolist(), ps[r, :c[r]].tolist()))
-                    exp = sorted(zip(o.plan_pos[r, :o.plan_count[r]].tolist(),
-                                     o.plan_slot[r, :o.plan_count[r]].tolist()))
+                    got = list(zip(pp[r, :c[r]].tolist(), ps[r, :c[r]].tolist()))
+                    exp = list(zip(o.plan_pos[r, :o.plan_count[r]].tolist(),
+                                   o.plan_slot[r, :o.plan_count[r]].tolist()))
+                    if not in_order:
+                        got, exp = sorted(got), sorted(exp)
                     assert got == exp, f"plan of layer {a} request {r}"
+        if check_prefill:
+            self.check_prefill_intact()
         if check_bytes:
             hot = self.mem.hot.cpu().numpy()
             for l in range(w.L):
@@ -163,6 +192,22 @@ class Run:
                                                   err_msg=f"host tail {l}")
         flags, ue = self.hs.status()
         assert flags == 0, f"status flags {flags}"
+
+    def check_prefill_intact(self, chunk_rows=16384):
+        """Host rows [0, L_ctx) of every (layer, request) equal a fresh
+        generation of their records (``workload.records``), chunk by chunk."""
+        w = self.w
+        buf = np.empty((min(chunk_rows, w.L_ctx), w.rec), np.uint8)
+        for l in range(w.L):
+            view = self.mem.host_view(l)
+            for r in range(w.R):
+                for p0 in range(0, w.L_ctx, chunk_rows):
+                    n = min(chunk_rows, w.L_ctx - p0)
+                    REC.fill(buf.ctypes.data, n, w.rec, w.rec, w.seed, l, r, p0)
+                    if not np.array_equal(view[r, p0:p0 + n], buf[:n]):
+                        bad = np.nonzero((view[r, p0:p0 + n] != buf[:n]).any(axis=1))[0]
+                        raise AssertionError(f"prefill host rows changed: layer {l} request {r} "
+                                             f"rows {(bad[:8] + p0).tolist()}")
 
     def close(self):
         self.hs.close()

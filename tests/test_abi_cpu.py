@@ -28,6 +28,38 @@ def test_library_exports_every_declared_symbol():
     assert set(names) == bound, set(names) ^ bound
 
 
+# Wrappers that return the C function's out-parameters instead of taking them.
+_OUT_PARAMS = {"hisparse_init": 1, "hisparse_get_status": 1, "hisparse_get_info": 1,
+               "hisparse_host_alloc": 1, "hisparse_host_alloc_kind": 1,
+               "hisparse_host_hugepage_bytes": 1}
+
+
+def declared_arity():
+    """Number of parameters of every function in include/hisparse.h."""
+    src = open(os.path.join(ROOT, "include", "hisparse.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    out = {}
+    for name, params in re.findall(r"\b(hisparse_[a-z_]+)\s*\(([^;{]*?)\)\s*;", src, flags=re.S):
+        params = params.strip()
+        out[name] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_arity_matches_the_header():
+    """Every C function's argtypes and every same-name Python wrapper take
+    the parameters the header declares (wrappers that return out-parameters
+    take that many fewer)."""
+    import inspect
+    arity = declared_arity()
+    for name, _, args in H.SIGNATURES:
+        assert len(args) == arity[name], (name, len(args), arity[name])
+        fn = getattr(H, name, None)
+        if fn is None:
+            continue
+        n = len(inspect.signature(fn).parameters)
+        assert n + _OUT_PARAMS.get(name, 0) == arity[name], (name, n, arity[name])
+
+
 def test_strerror_and_codes():
     lib = H.load()
     assert lib.hisparse_strerror(0) == b"ok"

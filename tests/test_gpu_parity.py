@@ -130,12 +130,19 @@ from harness import Run  # noqa: E402
 
 
 def _run_all(w, every=1, **kw):
+    """Run every step on both sides.  Slot vectors and miss counts are
+    compared after every step; the full state (slot map, LRU, page table,
+    plan, every hot byte, written-back rows) after every ``every``-th step and
+    the last; the untouched prefill host rows at the first full compare and
+    the last."""
     run = Run(w, **kw)
     try:
         for t in range(w.steps):
             run.step()
             if t % every == 0 or t == w.steps - 1:
-                run.compare()
+                run.compare(check_prefill=(t == 0 or t == w.steps - 1))
+            else:
+                run.compare_light()
     finally:
         run.close()
 
@@ -252,6 +259,35 @@ def test_skip_io_metadata_identical_bytes_stale(lookup):
 def test_from_mirror_bytes_identical():
     _run_all(get("quest").scaled(R=2, groups=1, L_ctx=1024, steps=5), flags=H.FROM_MIRROR,
              mirror=True)
+
+
+@pytest.mark.parametrize("lookup", LOOKUPS)
+@pytest.mark.parametrize("fused", [True, False])
+def test_from_mirror_with_write_through(lookup, fused):
+    """FROM_MIRROR with the write-through on (DSA-style: the previous token
+    sits in the local window, so it is selected again right after its
+    write-back): every write-back also lands in the HBM mirror, so the
+    mirror-fed fetches return the written bytes.  Every step is compared with
+    the oracle, and at the end the mirror equals the host pool byte for byte."""
+    w = get("dsa").scaled(R=3, groups=2, L_ctx=8192, steps=8)
+    run = Run(w, lookup=lookup, fused=fused, mirror=True, flags=H.FROM_MIRROR)
+    try:
+        for t in range(w.steps):
+            run.step()
+            run.compare(check_prefill=(t == w.steps - 1))
+        pool = run.mem.pool.numpy()[:run.mem.mirror.numel()]
+        assert np.array_equal(run.mem.mirror.cpu().numpy(), pool), "mirror differs from pool"
+    finally:
+        run.close()
+
+
+@pytest.mark.parametrize("mode", ["group", "inline"])
+def test_from_mirror_with_write_through_shared_layers(mode):
+    """The same on shared-index layers, whose write-backs are their own
+    launches (and the anchors' fused)."""
+    _run_all(get("shared").scaled(R=2, groups=2, L_ctx=4096, steps=6, write_through=True),
+             mirror=True, flags=H.FROM_MIRROR, inline_shared=mode == "inline",
+             group_replay=mode == "group")
 
 
 def test_huge_page_pool():
@@ -567,7 +603,44 @@ def test_import_rejects_inconsistent_state():
     assert hs.import_state(0, sp, lru, pt) == H.EINVAL
     pt[0, 5] = 2
     assert hs.import_state(0, sp, np.array([[0, 1, 1, 3]], np.int16), pt) == H.EINVAL
+    # miss counts: imported with the rest, validated against [0, k]
+    assert hs.import_state(0, sp, lru, pt, np.array([3], np.int32)) == H.EINVAL
+    assert hs.export_state(0)[3].tolist() == [0]
+    assert hs.import_state(0, sp, lru, pt, np.array([2], np.int32)) == 0
+    sp2, lru2, pt2, mc2 = hs.export_state(0)
+    assert sp2.tolist() == sp.tolist() and lru2.tolist() == lru.tolist()
+    assert pt2.tolist() == pt.tolist() and mc2.tolist() == [2]
     hs.close(); mem.close()
+
+
+def test_export_import_round_trip_mid_run():
+    """Checkpoint / resume: a run's state exported after some steps and
+    imported into a fresh instance (with the hot bytes copied) continues
+    exactly as the uninterrupted run does."""
+    w = get("dsa").scaled(R=3, groups=1, L_ctx=8192, steps=8, write_through=False)
+    a = Run(w)
+    b = Run(w)
+    try:
+        for t in range(4):
+            a.step()
+        for l, _ in a.groups:
+            assert b.hs.import_state(l, *a.hs.export_state(l)) == 0
+        b.mem.hot.copy_(a.mem.hot)
+        for l, _ in a.groups:
+            np.testing.assert_array_equal(b.hs.export_state(l)[3], a.hs.export_state(l)[3])
+        for t in range(4, w.steps):
+            a.step()
+            b.gpu_step(t)
+        a.compare()
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(b.out.cpu().numpy(), a.out.cpu().numpy())
+        for l, _ in a.groups:
+            for x, y in zip(a.hs.export_state(l), b.hs.export_state(l)):
+                np.testing.assert_array_equal(x, y)
+        assert torch.equal(a.mem.hot, b.mem.hot)
+    finally:
+        a.close()
+        b.close()
 
 
 def test_cuda_graph_replay_equals_eager():
@@ -747,8 +820,10 @@ def _need_host_memory(nbytes):
 @pytest.mark.parametrize("name", ["quest", "shared"])
 def test_full_size_config(name):
     """The Quest-style and shared-index configs at full size (every request,
-    layer and step; 53.7 GB and 77.3 GB host pools): slot vectors, state, plans
-    and every hot byte equal the oracle's at the first and the last step."""
+    layer and step; 53.7 GB and 77.3 GB host pools): slot vectors and miss
+    counts equal the oracle's after every step; slot maps, LRU order, page
+    tables, plans and every hot byte after the first and the last step; the
+    prefill host rows are unchanged."""
     _need_host_memory(get(name).host_bytes())
     _run_all(get(name), every=10 ** 9)
 

@@ -411,3 +411,70 @@ def test_strided_host_rows_give_the_same_result():
             p = a.slot_pos[r, s]
             if p >= 0:
                 assert bytes(a.hot[r, s]) == bytes(flat[r, p])
+
+
+def _preload_matches_replay(preload):
+    """Whether ``preload(layer, r, n)`` gives a shared-index layer the bytes
+    that replaying the anchor's admission plan into it gives, for several n
+    (rows above the prefill split included, up to the whole buffer)."""
+    from oracle.coracle import OracleLayer
+    k, B, P, split, rec = 4, 16, 40, 10, 8
+    rng = np.random.default_rng(21)
+    host_a = rng.integers(0, 256, size=(1, split, rec), dtype=np.uint8)
+    host_f = rng.integers(0, 256, size=(1, split, rec), dtype=np.uint8)
+    for n in (0, 1, 7, 10, 13, 16):
+        f1 = OracleLayer(1, k, B, P, rec, host=host_f, host_split=split, metadata=False)
+        f2 = OracleLayer(1, k, B, P, rec, host=host_f, host_split=split, metadata=False)
+        tail = rng.integers(0, 256, size=f1.host_tail[0].shape, dtype=np.uint8)
+        for f in (f1, f2):   # the same written-back tail rows, and stale hot rows
+            f.host_tail[0] = tail
+            f.hot[0] = 0x5C
+        preload(f1, 0, n)
+        a = OracleLayer(1, k, B, P, rec, host=host_a, host_split=split)
+        a.reset()
+        for c0 in range(0, n, k):   # the admission's consecutive lists of k positions
+            chunk = np.full((1, k), -1, np.int32)
+            m = min(n, c0 + k) - c0
+            chunk[0, :m] = np.arange(c0, c0 + m)
+            _, e = a.resolve(chunk)
+            assert e == 0
+            a.replay_into(f2)
+        if not np.array_equal(f1.hot, f2.hot):
+            return False
+        for s in range(n):             # slot s holds the shared layer's own row s
+            exp = host_f[0, s] if s < split else tail[s - split]
+            if not np.array_equal(f1.hot[0, s], exp):
+                return False
+    return True
+
+
+def test_shared_layer_preload_equals_replay_of_the_admission_plan():
+    """A shared-index layer's side of an admission (``preload_bytes``) holds
+    exactly the bytes that replaying the anchor's admission plan into it
+    gives (gentlecold.top §3.6: a shared layer keeps its slots in lockstep
+    with its anchor and takes the bytes of the anchor's plan from its own host
+    pool), including rows above the prefill split, which come from the
+    layer's own written-back tail."""
+    from oracle.coracle import OracleLayer
+    assert _preload_matches_replay(OracleLayer.preload_bytes)
+
+
+def _preload_off_by_one(o, r, n):
+    for s in range(n):
+        o.hot[r, s] = o.host_row(r, min(s + 1, o.P - 1))
+
+
+def _preload_ignores_split(o, r, n):
+    for s in range(n):
+        o.hot[r, s] = o._host_keep[r, min(s, o.host_split - 1)]
+
+
+def _preload_one_short(o, r, n):
+    for s in range(max(0, n - 1)):
+        o.hot[r, s] = o.host_row(r, s)
+
+
+@pytest.mark.parametrize("mutant", [_preload_off_by_one, _preload_ignores_split,
+                                    _preload_one_short])
+def test_preload_pin_catches_planted_mistakes(mutant):
+    assert not _preload_matches_replay(mutant)

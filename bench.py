@@ -63,8 +63,7 @@ def parse():
     ap.add_argument("--mirror", action="store_true",
                     help="fetch missed records from an HBM mirror of the host pool "
                          "(FROM_MIRROR): the same kernels with HBM as the source; the "
-                         "roofline is then against HBM (rows written back later are not "
-                         "mirrored)")
+                         "roofline is then against HBM (write-backs store to both)")
     ap.add_argument("--unfused", action="store_true",
                     help="write-through as its own launch instead of inside RESOLVE")
     ap.add_argument("--L-ctx", type=int, default=0,
@@ -79,8 +78,23 @@ def parse():
                          "anchor's RESOLVE launch (inline, HISPARSE_WITH_SHARED)")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-allhit", action="store_true")
-    ap.add_argument("--verify", action="store_true",
-                    help="after timing, compare the final GPU state with the oracle")
+    ap.add_argument("--verify", dest="verify", action="store_true", default=True,
+                    help="after the timed pass, compare its final state with the oracle "
+                         "(the default)")
+    ap.add_argument("--no-verify", dest="verify", action="store_false")
+    ap.add_argument("--workloads", default="tiny,quest,short,shared_inline,shared_anchor,sweep,"
+                                           "sweep_allhit",
+                    help="the other workloads measured after the headline, each on its own "
+                         "pool, reported in the line's `workloads` object (one GPU only)")
+    ap.add_argument("--no-workloads", action="store_true")
+    ap.add_argument("--skip-io", action="store_true",
+                    help="every RESOLVE with SKIP_IO: the metadata path with the trace's "
+                         "misses and no record copies (the pages' no-IO mode)")
+    ap.add_argument("--no-alt-burn-in", action="store_true",
+                    help="skip the timed pass after a burn-in over another trace")
+    ap.add_argument("--l2-persist", type=int, default=0,
+                    help="MB of L2 set aside to keep the RESOLVE layers' page tables "
+                         "persisting between steps (hisparse_set_l2_persisting; 0 = off)")
     return ap.parse_args()
 
 
@@ -217,6 +231,9 @@ def cpu_oracle_rate(w, traces, host_views=None, budget_s=10.0, union=False, warm
                                 metadata=l in anchors)
         if l in anchors:
             layers[l].reset()
+            if w.admit_preload:   # short requests start admitted with their prefill
+                for r in range(w.R):
+                    layers[l].admit(r, w.L_ctx)
     new_rows = REC.new_token_records(w)
     anchor_of = w.anchor_of()
     sel_total, miss_bytes, steps_done, t_total = 0, 0, 0, 0.0
@@ -234,7 +251,12 @@ def cpu_oracle_rate(w, traces, host_views=None, budget_s=10.0, union=False, warm
                 layers[l].set_newest_rows(new_rows[t, l])
         for a in anchors:
             nw = traces[a][1][t] if w.write_through else None
-            layers[a].resolve(traces[a][0][t], nw, union=union)
+            if w.admit_preload:
+                prev = traces[a][1][t - 1] if t > 0 else np.full(w.R, -1, np.int32)
+                layers[a].resolve_with_seq_lens(traces[a][0][t], nw, prev,
+                                                np.full(w.R, w.L_ctx + t + 1, np.int32))
+            else:
+                layers[a].resolve(traces[a][0][t], nw, union=union)
             miss_bytes += int(layers[a].miss_count.sum()) * w.rec
             for f in (l for l in range(w.L) if anchor_of[l] == a):
                 layers[a].replay_into(layers[f])
@@ -279,6 +301,8 @@ def cpu_oracle_rate_threads(w, traces, host_views, threads, union=False):
             units.append((a, r, mk(a, True), [(f, mk(f, False)) for f in fls]))
     for _, _, o, _ in units:
         o.reset()
+        if w.admit_preload:
+            o.admit(0, w.L_ctx)
 
     def run(chunk):
         sel = misses = 0
@@ -290,7 +314,12 @@ def cpu_oracle_rate_threads(w, traces, host_views, threads, union=False):
                             lay.writeback(traces[anchors[0]][1][t - 1][r:r + 1])
                         lay.set_newest_rows(new_rows[t, l, r:r + 1])
                 nw = traces[a][1][t][r:r + 1] if w.write_through else None
-                o.resolve(traces[a][0][t][r:r + 1], nw, union=union)
+                if w.admit_preload:
+                    prev = traces[a][1][t - 1][r:r + 1] if t > 0 else np.full(1, -1, np.int32)
+                    o.resolve_with_seq_lens(traces[a][0][t][r:r + 1], nw, prev,
+                                            np.full(1, w.L_ctx + t + 1, np.int32))
+                else:
+                    o.resolve(traces[a][0][t][r:r + 1], nw, union=union)
                 misses += int(o.miss_count.sum())
                 for _, lay in fls:
                     o.replay_into(lay)
@@ -308,6 +337,78 @@ def cpu_oracle_rate_threads(w, traces, host_views, threads, union=False):
                       f"{len(units)} independent (request, anchor layer) units spread over "
                       f"{threads} threads, plain C oracle, record copies included",
             "miss_bytes_per_s": sum(m for _, m in res) * w.rec / dt, "seconds": dt}
+
+
+# --------------------------------------------------------------------------- #
+TARGET_LINK_FRAC = 0.8   # the miss-fetch path's target share of the measured host link
+
+# The default line's other workloads (name -> how it is built and run).
+SUB_WORKLOADS = ("tiny", "quest", "short", "shared_inline", "shared_anchor", "sweep",
+                 "sweep_allhit")
+SWEEP_POINT = (4096, 0.87)           # (B, reuse fraction) of the capacity-sweep entry
+SWEEP_CONTEXTS = (1048576, 524288, 262144)
+HOST_MARGIN_GIB = 32                 # host memory left free beside a pinned pool
+
+
+def opts_for(args, **kw):
+    """A copy of the command-line options with some replaced."""
+    d = dict(vars(args))
+    d.update(kw)
+    return argparse.Namespace(**d)
+
+
+def workload_config(w, o, n_gpus):
+    """The line's config: the workload and the options that shape the run (the
+    same on both arms; facts of the run itself go elsewhere)."""
+    return {"workload": w.name, "requests": w.R, "layers": w.L, "anchors": len(w.anchors()),
+            "top_k": w.k, "B": w.B, "L_ctx": w.L_ctx, "record_bytes": w.rec,
+            "write_through": w.write_through, "parallelism": f"replicas{n_gpus}",
+            "l2": "flushed (256 MB write) before every timed step",
+            "lookup": ["page_table", "hash"][o.lookup],
+            "write_through_launch": "separate" if o.unfused else "fused into RESOLVE",
+            "host_pool": o.pool,
+            "replay_launch": {"group": "one per anchor for all its shared-index layers",
+                              "layer": "one per shared-index layer",
+                              "inline": "none: shared-index layers filled inside the "
+                                        "anchor's RESOLVE"}[o.replay],
+            "host_layout": ("rows of each shared-index group interleaved" if o.interleave
+                            else "one block of rows per layer"),
+            "fetch_source": "HBM mirror of the host pool" if o.mirror else "host pool",
+            "verify_rows": o.verify_rows,
+            "resident_tier": (dict(zip(("full_requests", "window", "tokens_per_block"),
+                                       (int(x) for x in o.resident.split(","))))
+                              if o.resident else None),
+            "burn_in": None if o.no_burn_in else
+            f"{o.burn_in} untimed passes over all steps, each from the admission state",
+            "l2_persisting_mb": o.l2_persist or None}
+
+
+def mem_available():
+    """Host MemAvailable in bytes (0 if unknown)."""
+    try:
+        for line in open("/proc/meminfo"):
+            if line.startswith("MemAvailable:"):
+                return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
+def pick_sweep_context(B, f):
+    """The largest capacity-sweep context whose pinned host pool leaves
+    HOST_MARGIN_GIB of host memory free; every candidate and the outcome."""
+    from workload import sweep_workload
+    avail = mem_available()
+    tried = []
+    for L in SWEEP_CONTEXTS:
+        need = sweep_workload(B, f, L_ctx=L).host_bytes()
+        ok = avail >= need + (HOST_MARGIN_GIB << 30)
+        tried.append({"L_ctx": L, "host_pool_gb": round(need / 1e9, 1), "fits": ok})
+        if ok:
+            return L, {"mem_available_gb": round(avail / 1e9, 1), "margin_gib": HOST_MARGIN_GIB,
+                       "candidates": tried}
+    return None, {"mem_available_gb": round(avail / 1e9, 1), "margin_gib": HOST_MARGIN_GIB,
+                  "candidates": tried}
 
 
 # --------------------------------------------------------------------------- #
@@ -329,9 +430,7 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * res["seconds"] / res["steps"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
-            "data": "synthetic", "config": {"workload": w.name, "requests": w.R, "layers": w.L,
-                                            "top_k": w.k, "B": w.B, "L_ctx": w.L_ctx,
-                                            "record_bytes": w.rec},
+            "data": "synthetic", "config": workload_config(w, args, args.gpus),
             "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": res["sample"],
                              "value": res["value"], "unit": "selections/s"},
             "e2e": {"value": res["value"], "unit": "selections/s", "h2d_bytes_per_step": 0,
@@ -341,373 +440,10 @@ def run_reference(args):
 
 
 # --------------------------------------------------------------------------- #
-def run_ours(args):
-    import numpy as np
+def h2d_probe(dev):
+    """Pinned cudaMemcpyAsync host->device, 1 GiB x 20, best of 3 rounds (a
+    transient dip must not flatter the fractions): GB/s."""
     import torch
-
-    rank, world, local = dist_env()
-    torch.cuda.set_device(local)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-
-    from host_offload_serving_gb300 import hisparse as H
-    from host_offload_serving_gb300.runtime import HiSparse, WorkloadMemory, DecodeStep, sm_copy
-    from workload import get, records as REC, sweep_workload
-    from workload.traces import all_traces
-
-    w = get(args.workload)
-    if args.L_ctx:
-        w = w.scaled(L_ctx=args.L_ctx)
-    if w.write_through:
-        w = w.scaled(steps=max(w.steps, args.warmup + args.steps))
-    from host_offload_serving_gb300.replicas import replica_seed, max_over_ranks, job_throughput
-    w = w.scaled(seed=replica_seed(w.seed, rank))     # each replica its own requests
-    T = args.warmup + args.steps
-    if not w.write_through and T > w.steps:
-        w = w.scaled(steps=T)
-    dev = torch.device("cuda", local)
-
-    t_setup = time.perf_counter()
-    mem = WorkloadMemory(w.R, w.L, w.B, w.P, w.rec, mirror=args.mirror,
-                         pool_kind=H.HOST_HUGE if args.pool == "huge" else H.HOST_PINNED,
-                         group=(1 + w.followers) if args.interleave else 1)
-    REC.fill_host_pool(w, mem.geometry)
-    if args.mirror:
-        mem.fill_mirror()
-    hs = HiSparse(w.R, w.L, w.k, w.B, w.P, w.rec, mem.layer_buffers(), anchor_of=w.anchor_of(),
-                  ctas_per_request=args.ctas, replay_ctas=args.replay_ctas, lookup=args.lookup)
-    info = hs.info()
-    hp_frac = mem.pool.hugepage_fraction()
-
-    def thp_splits():
-        d = {}
-        try:
-            for line in open("/proc/vmstat"):
-                k, v = line.split()
-                if k in ("thp_split_page", "thp_split_pmd"):
-                    d[k] = int(v)
-        except OSError:
-            pass
-        return d
-    splits0 = thp_splits()
-    anchor_of = w.anchor_of()
-    groups = [(a, [l for l in range(w.L) if anchor_of[l] == a]) for a in w.anchors()]
-    G = len(groups)
-    if args.verify_rows > 1:   # speculative verify rows, resolved as one union list
-        from workload.traces import verify_row_traces
-        traces = verify_row_traces(w, args.verify_rows)
-    else:
-        traces = all_traces(w)
-    sel_np = np.stack([traces[a][0] for a, _ in groups], axis=1)       # [T][G][R][k]
-    sel = torch.from_numpy(sel_np).to(dev)
-    newest = newest_np = None
-    wb = None
-    new_rows = None
-    if w.write_through:
-        newest_np = traces[groups[0][0]][1]
-        newest = torch.from_numpy(newest_np).to(dev)
-        wbn = np.full((w.steps, w.L, w.R), -1, np.int32)
-        for t in range(1, w.steps):
-            wbn[t] = newest_np[t - 1][None, :]
-        wb = torch.from_numpy(wbn).to(dev)
-        new_rows = torch.from_numpy(REC.new_token_records(w)).to(dev)
-    out = torch.full((G, w.R, w.k), -1, dtype=torch.int32, device=dev)
-    runner = DecodeStep(hs, mem, groups,
-                        flags=(H.FROM_MIRROR if args.mirror else 0) |
-                        (H.UNION if args.verify_rows > 1 else 0),
-                        fused=not args.unfused, sel_block_tokens=w.sel_block_tokens,
-                        group_replay=args.replay == "group",
-                        inline_shared=args.replay == "inline")
-    miss_hist = torch.zeros((T, G, w.R), dtype=torch.int32, device=dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)     # > 129 MB L2
-    setup_s = time.perf_counter() - t_setup
-
-    res_all = None
-    if args.resident:
-        from workload.resident import resident_tables
-        full, window, tok = (int(x) for x in args.resident.split(","))
-        res_all = torch.from_numpy(resident_tables(w, tok, full=full, window=window)).to(dev)
-        res_tok = tok
-
-    def issue(t):
-        if res_all is not None:          # step t's resident block table, by pointer
-            runner.resident = (res_all[t], res_tok)
-        runner.issue(sel[t], out, newest=newest[t] if newest is not None else None,
-                     wb_pos=wb[t] if (wb is not None and t > 0) else None,
-                     new_rows=new_rows[t] if new_rows is not None else None)
-
-    # Every step is captured once as a CUDA graph -- the form the pages deploy
-    # RESOLVE in (gentlecold.top deep dive §3.5: captured in the decode CUDA
-    # graph) -- so the timed region measures GPU work, not Python launch
-    # overhead.  The headline pass replays plain graphs; a second pass over the
-    # same steps replays graphs with timing events around every RESOLVE and
-    # write-back launch, on the stream each runs on.
-    def timing_event():
-        try:
-            return torch.cuda.Event(enable_timing=True, external=True), True
-        except TypeError:
-            return torch.cuda.Event(enable_timing=True), False
-
-    cap = torch.cuda.Stream()
-
-    def capture(t, instrument):
-        """Graph of step t; with `instrument`, timing events around every
-        RESOLVE and write-back launch and a copy of the miss counts."""
-        evs, wev, rpev = [], [], []
-        orig_resolve, orig_step = hs.resolve, hs.resolve_step
-        orig_res, orig_ex = hs.resolve_resident, hs.resolve_ex
-        orig_wb, orig_rp = hs.writeback, hs.prefetch_plan
-
-        def timed_resolve(layer, *a, **kw):
-            st = kw.get("stream")
-            e0, e1 = timing_event()[0], timing_event()[0]
-            e0.record(st)
-            orig_resolve(layer, *a, **kw)
-            e1.record(st)
-            evs.append((e0, e1))
-
-        def timed_step(layer, *a, **kw):
-            st = kw.get("stream")
-            e0, e1 = timing_event()[0], timing_event()[0]
-            e0.record(st)
-            orig_step(layer, *a, **kw)
-            e1.record(st)
-            evs.append((e0, e1))
-
-        def timed_res(layer, *a, **kw):
-            st = kw.get("stream")
-            e0, e1 = timing_event()[0], timing_event()[0]
-            e0.record(st)
-            orig_res(layer, *a, **kw)
-            e1.record(st)
-            evs.append((e0, e1))
-
-        def timed_ex(layer, *a, **kw):
-            st = kw.get("stream")
-            e0, e1 = timing_event()[0], timing_event()[0]
-            e0.record(st)
-            orig_ex(layer, *a, **kw)
-            e1.record(st)
-            evs.append((e0, e1))
-
-        def timed_wb(layer, *a, **kw):
-            st = kw.get("stream")
-            e0, e1 = timing_event()[0], timing_event()[0]
-            e0.record(st)
-            orig_wb(layer, *a, **kw)
-            e1.record(st)
-            wev.append((e0, e1))
-
-        def timed_rp(anchor, follower, *a, **kw):
-            st = kw.get("stream")
-            e0, e1 = timing_event()[0], timing_event()[0]
-            e0.record(st)
-            orig_rp(anchor, follower, *a, **kw)
-            e1.record(st)
-            rpev.append((e0, e1))
-
-        if instrument:
-            hs.resolve, hs.resolve_step = timed_resolve, timed_step
-            hs.resolve_resident, hs.resolve_ex = timed_res, timed_ex
-            hs.writeback, hs.prefetch_plan = timed_wb, timed_rp
-        g = torch.cuda.CUDAGraph()
-        try:
-            with torch.cuda.stream(cap):
-                with torch.cuda.graph(g, stream=cap):
-                    issue(t)
-                    if instrument:
-                        for gi, (a, _) in enumerate(groups):
-                            hs.copy_miss_counts(a, miss_hist[t, gi],
-                                                stream=torch.cuda.current_stream())
-        finally:
-            hs.resolve, hs.resolve_step = orig_resolve, orig_step
-            hs.resolve_resident, hs.resolve_ex = orig_res, orig_ex
-            hs.writeback, hs.prefetch_plan = orig_wb, orig_rp
-        return g, evs, wev, rpev
-
-    def capture_pass():
-        """One graph holding the K timed steps, each after the L2 flush and
-        between two events recorded inside the graph: the pass is one graph
-        launch, so no timed step carries a graph launch of its own (as in a
-        serving step, whose graph holds every layer of the model)."""
-        evs = [(timing_event()[0], timing_event()[0]) for _ in range(args.steps)]
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(cap):
-            with torch.cuda.graph(g, stream=cap):
-                s = torch.cuda.current_stream()
-                for i in range(args.steps):
-                    flush.fill_(i & 0xFF)
-                    evs[i][0].record(s)
-                    issue(args.warmup + i)
-                    evs[i][1].record(s)
-        return g, evs
-
-    ext_ok = timing_event()[1]
-    plain = [capture(t, False)[0] for t in range(T)]
-    instr = [capture(t, ext_ok) for t in range(T)] if ext_ok else None
-    passg = capture_pass() if ext_ok else None
-    torch.cuda.synchronize()
-
-    clocks = Clocks(local)
-    clocks.__enter__()
-    t_wait = time.time()
-    while not clocks.samples and time.time() - t_wait < 5:
-        time.sleep(0.05)
-
-    # ---- burn-in: untimed passes over every step on the fresh host pool, each
-    #      from the admission state.  The GPU's first accesses to host pages
-    #      of a new pool pay one-time address-translation work (tens of us to
-    #      ms per launch, measured to last about two passes over a trace); a
-    #      serving system pays that once at start-up, so it stays out of the
-    #      timed steps. ----
-    for _ in range(0 if args.no_burn_in else args.burn_in):
-        for t in range(T):
-            plain[t].replay()
-        torch.cuda.synchronize()
-        hs.reset()
-        mem.hot.zero_()
-        torch.cuda.synchronize()
-    splits_burn = {k: v - splits0.get(k, 0) for k, v in thp_splits().items()}
-    splits0 = thp_splits()
-
-    cur = torch.cuda.current_stream()
-
-    def per_step_graphs():
-        """The K timed steps as K graph launches, events outside the graphs
-        (each step pays its own graph launch); returns per-step ms."""
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
-        for i in range(args.steps):
-            flush.fill_(i & 0xFF)     # also keeps the GPU busy while the host enqueues
-            ev[i][0].record(cur)
-            plain[args.warmup + i].replay()
-            ev[i][1].record(cur)
-        torch.cuda.synchronize()
-        return [a.elapsed_time(b) for a, b in ev]
-
-    # ---- pass 1 (the headline): W warm-up steps, then exactly K timed steps,
-    #      L2 flushed before each, all K in one graph launch with an event pair
-    #      inside the graph around every step ----
-    for t in range(args.warmup):
-        plain[t].replay()
-    torch.cuda.synchronize()
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
-    replay_launches = sum((-(-len(f) // 8) if args.replay == "group" else
-                           0 if args.replay == "inline" else len(f))
-                          for _, f in groups if f)
-    launches = args.steps * (G + replay_launches +
-                             (1 if (wb is not None and args.unfused) else 0))
-    if passg is not None:
-        passg[0].replay()
-        torch.cuda.synchronize()
-        step_ms = [a.elapsed_time(b) for a, b in passg[1]]
-    else:   # no timing events inside graphs in this torch
-        step_ms = per_step_graphs()
-    if dist is not None:
-        dist.barrier()
-    time.sleep(0.25)               # one more clock sample after the timed region
-    clocks.__exit__()
-    flags, _ = hs.status()
-
-    verify = None
-    if args.verify and not args.resident and w.sel_block_tokens == 1 and args.verify_rows == 1:
-        verify = verify_against_oracle(w, hs, mem, groups, traces, args.warmup + args.steps)
-
-    # ---- repeats: the whole trace 5 more times from the admission state (the
-    #      same warm-up and timed steps), so the spread between repeats of the
-    #      headline is on the line ----
-    def from_admission():
-        hs.reset()
-        mem.hot.zero_()
-        torch.cuda.synchronize()
-        for t in range(args.warmup):
-            plain[t].replay()
-        torch.cuda.synchronize()
-
-    rep_ms = []
-    for rep in range(5):
-        from_admission()
-        if passg is not None:
-            passg[0].replay()
-            torch.cuda.synchronize()
-            rep_ms.append(sum(a.elapsed_time(b) for a, b in passg[1]) / args.steps)
-        else:
-            rep_ms.append(sum(per_step_graphs()) / args.steps)
-    # the same steps once more as one graph launch per step (the timing the
-    # headline used before the pass graph; the difference is the graph launch)
-    from_admission()
-    sg_ms = per_step_graphs()
-
-    # ---- pass 2 (per-kernel durations for the roofline): the same steps from
-    #      the admission state, with events inside the graphs around every
-    #      RESOLVE and write-back launch ----
-    hs.reset()
-    mem.hot.zero_()
-    torch.cuda.synchronize()
-    res_ms = wb_ms = rp_ms = cold_ms = None
-    if instr is not None:
-        for t in range(T):
-            flush.fill_(t & 0xFF)
-            instr[t][0].replay()
-            torch.cuda.synchronize()
-        res_ms = [[a.elapsed_time(b) for a, b in instr[args.warmup + i][1]] for i in range(args.steps)]
-        cold_ms = [a.elapsed_time(b) for a, b in instr[0][1]]
-        wb_ms = [a.elapsed_time(b) for i in range(args.steps) for a, b in instr[args.warmup + i][2]]
-        rp_ms = [a.elapsed_time(b) for i in range(args.steps) for a, b in instr[args.warmup + i][3]]
-    else:   # no in-graph timing events in this torch: count misses eagerly
-        for t in range(T):
-            plain[t].replay()
-            for gi, (a, _) in enumerate(groups):
-                hs.copy_miss_counts(a, miss_hist[t, gi], stream=cur)
-        torch.cuda.synchronize()
-    flags |= hs.status()[0]
-    miss = miss_hist[args.warmup:].cpu().numpy().astype(np.int64)       # [K][G][R]
-
-    total_ms = sum(step_ms)
-    sel_per_step = G * w.R * w.k
-    value_local = sel_per_step * args.steps / (total_ms / 1e3)
-    total_ms_max = max_over_ranks(total_ms, dist, dev)
-    value = job_throughput(sel_per_step * args.steps, total_ms_max / 1e3, world)
-
-    if res_ms is not None:
-        res_flat = [x for r in res_ms for x in r]
-        timing_note = ("events inside the step graphs around every RESOLVE launch "
-                       "(second pass over the same steps)")
-    else:   # this torch cannot put timing events inside a graph
-        res_flat = [x / G for x in step_ms]
-        timing_note = "step graph time / anchors (includes write-back and row copy)"
-    resolve_avg_ms = sum(res_flat) / len(res_flat)
-    srt = sorted(res_flat)
-    pct = lambda q: srt[min(len(srt) - 1, int(q * (len(srt) - 1) + 0.5))] * 1e3
-    # When a step graph holds nothing but the RESOLVE launches (write-through
-    # fused, no shared-index layers), the average launch over the timed region
-    # is the pass-1 step time over the launches per step: the same CUDA events,
-    # without the extra event nodes the per-launch windows put between kernels.
-    inline = args.replay == "inline"
-    only_resolve = (all(not f for _, f in groups) or (inline and wb is None)) and \
-        not (args.unfused and wb is not None)
-    if only_resolve:
-        launch_ms = (sum(step_ms) / len(step_ms)) / G
-        timing_note = ("average RESOLVE launch over the timed region = pass-1 step time (CUDA "
-                       "events recorded inside the pass graph right before each step's first and "
-                       "after its last launch; the step holds only the RESOLVE launches) / "
-                       "launches per step; percentiles from per-launch event windows in a second "
-                       "pass over the same steps")
-    else:
-        launch_ms = resolve_avg_ms
-    miss_bytes = int(miss.sum()) * w.rec
-    if inline:   # a RESOLVE launch also moves every miss's rows of its shared-index layers
-        miss_bytes = sum(int(miss[:, gi].sum()) * (1 + len(f))
-                         for gi, (_, f) in enumerate(groups)) * w.rec
-    fetch_gbs = miss_bytes / (launch_ms * args.steps * G / 1e3) / 1e9
-    miss_rate = float(miss.sum()) / (args.steps * G * w.R * w.k)
-
-    # ---- host-link probe: pinned cudaMemcpyAsync H2D, 1 GiB x 20, best of
-    #      3 rounds (a transient dip must not flatter the fraction) ----
     nbytes = 1 << 30
     hbuf = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
     dbuf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
@@ -723,188 +459,405 @@ def run_ours(args):
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1)
         best_ms = ms if best_ms is None else min(best_ms, ms)
-    h2d_gbs = 20 * nbytes / (best_ms / 1e3) / 1e9
     del hbuf, dbuf
+    return 20 * nbytes / (best_ms / 1e3) / 1e9
 
-    # ---- all-hit / no-IO: the last step's selections again, with SKIP_IO.
-    #      Every selection is now resident, so this is the metadata path alone
-    #      (hash staging, marking, scans, publish) against HBM. ----
-    allhit = None
-    if not args.no_allhit:
-        t_last = args.warmup + args.steps - 1
-        gh = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(cap):
-            with torch.cuda.graph(gh, stream=cap):
-                for gi, (a, _) in enumerate(groups):
-                    hs.resolve_ex(a, sel[t_last, gi], out[gi], None,
-                                  newest[t_last] if newest is not None else None,
-                                  sel_block_tokens=w.sel_block_tokens,
-                                  flags=H.SKIP_IO | (H.UNION if args.verify_rows > 1 else 0),
-                                  stream=torch.cuda.current_stream())
-        torch.cuda.synchronize()
-        hit_ms = []
-        for i in range(10):
-            flush.fill_(i)
-            h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            h0.record(cur)
-            gh.replay()
-            h1.record(cur)
-            torch.cuda.synchronize()
-            hit_ms.append(h0.elapsed_time(h1) / G)
-        mc = np.stack([hs.export_state(a)[3] for a, _ in groups])
-        hit_avg = sum(hit_ms) / len(hit_ms)
-        alg = w.R * (4 * w.k + 4 * w.B + 2 * w.B + 2 * w.B + 4 * w.k)   # bytes per launch
-        allhit = {"us_per_layer_step": round(hit_avg * 1e3, 2), "misses": int(mc.sum()),
-                  "selections_per_s": round(w.R * w.k / (hit_avg / 1e3), 1),
-                  "algorithmic_bytes_per_launch": alg,
-                  "hbm_gbs": round(alg / (hit_avg / 1e3) / 1e9, 3),
-                  "timing": "graph of one SKIP_IO resolve per anchor, time / anchors"}
 
-    # ---- end to end through the C ABI with host buffers: every step copies
-    #      its selections (and write-back positions, new-token KV) from pinned
-    #      host memory and reads the slot vectors back, inside the timed
-    #      region.  Steps are captured as graphs, as a serving loop would. ----
-    e2e = None
-    if not args.no_e2e:
-        # A step's inputs (selections; with write-through also the newest
-        # positions, the write-back positions and the new tokens' KV) travel
-        # packed in one pinned buffer: one host-to-device copy per step, then
-        # the RESOLVE launches, then one device-to-host copy of the slot vectors.
-        parts = [("sel", tuple(sel_np.shape[1:]), 4)]
-        if w.write_through:
-            parts += [("newest", (w.R,), 4), ("wb", (w.L, w.R), 4), ("new", (w.L, w.R, w.rec), 1)]
-        offs, o = {}, 0
-        for name, shape, isz in parts:
-            offs[name] = o
-            o += -(-int(np.prod(shape)) * isz // 16) * 16
-        h_pack = torch.zeros((T, o), dtype=torch.uint8).pin_memory()
-        d_pack = torch.empty(o, dtype=torch.uint8, device=dev)
+def measure(o, w, dev, h2d_gbs, dist=None, world=1, headline=False, rank=0, clocks=None):
+    """One workload on this GPU: set-up, step graphs, burn-in, the timed pass,
+    per-launch windows, the oracle check of the timed run; with `headline`
+    also the repeats, the end-to-end pass, the all-hit and admission figures
+    and the burn-in over another trace.  Returns the figures as a dict."""
+    import numpy as np
+    import torch
 
-        def view(buf, name):
-            shape, isz = next((sh, z) for n, sh, z in parts if n == name)
-            nb = int(np.prod(shape)) * isz
-            return buf[offs[name]:offs[name] + nb].view(torch.int32 if isz == 4 else torch.uint8).view(shape)
+    from host_offload_serving_gb300 import hisparse as H
+    from host_offload_serving_gb300.runtime import HiSparse, WorkloadMemory, DecodeStep, sm_copy
+    from host_offload_serving_gb300.replicas import max_over_ranks, job_throughput
+    from workload import records as REC
+    from workload.traces import all_traces
 
-        h_new = REC.new_token_records(w) if w.write_through else None
-        wb_np = wb.cpu().numpy() if w.write_through else None
-        for t in range(T):
-            view(h_pack[t], "sel").copy_(torch.from_numpy(sel_np[t]))
-            if w.write_through:
-                view(h_pack[t], "newest").copy_(torch.from_numpy(newest_np[t]))
-                view(h_pack[t], "wb").copy_(torch.from_numpy(wb_np[t]))
-                view(h_pack[t], "new").copy_(torch.from_numpy(h_new[t]))
-        h_out = torch.empty((T, G, w.R, w.k), dtype=torch.int32).pin_memory()
-        wt = w.write_through
-        bi = o
-        bo = h_out[0].numel() * 4
-        e_graphs = []
-        for t in range(T):
-            g = torch.cuda.CUDAGraph()
+    K, W = o.steps, o.warmup
+    T = W + K
+    if T > w.steps:
+        w = w.scaled(steps=T)
+    t_setup = time.perf_counter()
+    mem = WorkloadMemory(w.R, w.L, w.B, w.P, w.rec, mirror=o.mirror,
+                         pool_kind=H.HOST_HUGE if o.pool == "huge" else H.HOST_PINNED,
+                         group=(1 + w.followers) if o.interleave else 1)
+    REC.fill_host_pool(w, mem.geometry)
+    if o.mirror:
+        mem.fill_mirror()
+    hs = HiSparse(w.R, w.L, w.k, w.B, w.P, w.rec, mem.layer_buffers(), anchor_of=w.anchor_of(),
+                  ctas_per_request=o.ctas, replay_ctas=o.replay_ctas, lookup=o.lookup)
+    if o.l2_persist:
+        hs.set_l2_persisting(o.l2_persist << 20)
+    info = hs.info()
+    hp_frac = mem.pool.hugepage_fraction()
+
+    def thp_splits():
+        d = {}
+        try:
+            for line in open("/proc/vmstat"):
+                k_, v = line.split()
+                if k_ in ("thp_split_page", "thp_split_pmd"):
+                    d[k_] = int(v)
+        except OSError:
+            pass
+        return d
+    splits0 = thp_splits()
+    anchor_of = w.anchor_of()
+    groups = [(a, [l for l in range(w.L) if anchor_of[l] == a]) for a in w.anchors()]
+    G = len(groups)
+    if o.verify_rows > 1:   # speculative verify rows, resolved as one union list
+        from workload.traces import verify_row_traces
+        trace_of = lambda ww: verify_row_traces(ww, o.verify_rows)  # noqa: E731
+    else:
+        trace_of = all_traces
+    traces = trace_of(w)
+    sel_np = np.stack([traces[a][0] for a, _ in groups], axis=1)       # [T][G][R][k]
+    sel = torch.from_numpy(sel_np).to(dev)
+    # another trace over the same pool (another selection seed), for a burn-in
+    # that does not touch exactly the timed accesses
+    sel_alt = None
+    if headline and not o.no_burn_in and not o.no_alt_burn_in:
+        tr_alt = trace_of(w.scaled(seed=w.seed + 7919))
+        sel_alt = torch.from_numpy(np.stack([tr_alt[a][0] for a, _ in groups], axis=1)).to(dev)
+    newest = newest_np = wb = new_rows = None
+    if w.write_through:
+        newest_np = traces[groups[0][0]][1]
+        newest = torch.from_numpy(newest_np).to(dev)
+        wbn = np.full((w.steps, w.L, w.R), -1, np.int32)
+        for t in range(1, w.steps):
+            wbn[t] = newest_np[t - 1][None, :]
+        wb = torch.from_numpy(wbn).to(dev)
+        new_rows = torch.from_numpy(REC.new_token_records(w)).to(dev)
+    out = torch.full((G, w.R, w.k), -1, dtype=torch.int32, device=dev)
+    seq_dev = None
+    if w.admit_preload:   # short requests: admitted preloaded, resolved with their lengths
+        seq_dev = torch.from_numpy(np.ascontiguousarray(
+            (w.L_ctx + 1 + np.arange(w.steps, dtype=np.int32))[:, None].repeat(w.R, axis=1))).to(dev)
+    admit_reqs = torch.arange(w.R, dtype=torch.int32, device=dev)
+    admit_pre = torch.full((w.R,), w.L_ctx, dtype=torch.int32, device=dev)
+
+    def admit_all():
+        if w.admit_preload:
+            hs.admit(-1, admit_reqs, admit_pre)
+
+    admit_all()
+    runner = DecodeStep(hs, mem, groups,
+                        flags=(H.FROM_MIRROR if o.mirror else 0) |
+                        (H.UNION if o.verify_rows > 1 else 0) |
+                        (H.SKIP_IO if o.skip_io else 0),
+                        fused=not o.unfused, sel_block_tokens=w.sel_block_tokens,
+                        group_replay=o.replay == "group", inline_shared=o.replay == "inline")
+    miss_hist = torch.zeros((T, G, w.R), dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)     # > 129 MB L2
+    setup_s = time.perf_counter() - t_setup
+
+    res_all = res_tok = None
+    if o.resident:
+        from workload.resident import resident_tables
+        full, window, tok = (int(x) for x in o.resident.split(","))
+        res_all = torch.from_numpy(resident_tables(w, tok, full=full, window=window)).to(dev)
+        res_tok = tok
+
+    def issue(t, sel_src=None):
+        s = sel if sel_src is None else sel_src
+        if res_all is not None:          # step t's resident block table, by pointer
+            runner.resident = (res_all[t], res_tok)
+        runner.issue(s[t], out, newest=newest[t] if newest is not None else None,
+                     wb_pos=wb[t] if (wb is not None and t > 0) else None,
+                     new_rows=new_rows[t] if new_rows is not None else None,
+                     seq_lens=seq_dev[t] if seq_dev is not None else None)
+
+    # Every step is captured once as a CUDA graph -- the form the pages deploy
+    # RESOLVE in (gentlecold.top deep dive §3.5: captured in the decode CUDA
+    # graph) -- so the timed region measures GPU work, not Python launch
+    # overhead.
+    def timing_event():
+        try:
+            return torch.cuda.Event(enable_timing=True, external=True), True
+        except TypeError:
+            return torch.cuda.Event(enable_timing=True), False
+
+    cap = torch.cuda.Stream()
+
+    def capture(t, instrument, sel_src=None):
+        """Graph of step t; with `instrument`, timing events around every
+        RESOLVE, write-back and replay launch and a copy of the miss counts."""
+        evs, wev, rpev = [], [], []
+        names = ("resolve", "resolve_step", "resolve_resident", "resolve_ex", "writeback",
+                 "prefetch_plan")
+        orig = {n: getattr(hs, n) for n in names}
+
+        def timed(fn, acc):
+            def call(*a, **kw):
+                st = kw.get("stream")
+                e0, e1 = timing_event()[0], timing_event()[0]
+                e0.record(st)
+                fn(*a, **kw)
+                e1.record(st)
+                acc.append((e0, e1))
+            return call
+
+        if instrument:
+            for n in names[:4]:
+                setattr(hs, n, timed(orig[n], evs))
+            hs.writeback = timed(orig["writeback"], wev)
+            hs.prefetch_plan = timed(orig["prefetch_plan"], rpev)
+        g = torch.cuda.CUDAGraph()
+        try:
             with torch.cuda.stream(cap):
                 with torch.cuda.graph(g, stream=cap):
-                    if args.e2e_copy == "sm":
-                        sm_copy(d_pack, h_pack[t])
-                    else:
-                        d_pack.copy_(h_pack[t], non_blocking=True)
-                    if res_all is not None:
-                        runner.resident = (res_all[t], res_tok)
-                    runner.issue(view(d_pack, "sel"), out,
-                                 newest=view(d_pack, "newest") if wt else None,
-                                 wb_pos=view(d_pack, "wb") if (wt and t > 0) else None,
-                                 new_rows=view(d_pack, "new") if wt else None)
-                    if args.e2e_copy == "sm":
-                        sm_copy(h_out[t], out)
-                    else:
-                        h_out[t].copy_(out, non_blocking=True)
-            e_graphs.append(g)
-        for burn in range(0 if args.no_burn_in else args.burn_in):   # as for pass 1
-            hs.reset()
-            mem.hot.zero_()
-            torch.cuda.synchronize()
-            for t in range(T):
-                e_graphs[t].replay()
-            torch.cuda.synchronize()
+                    issue(t, sel_src)
+                    if instrument:
+                        for gi, (a, _) in enumerate(groups):
+                            hs.copy_miss_counts(a, miss_hist[t, gi],
+                                                stream=torch.cuda.current_stream())
+        finally:
+            for n in names:
+                setattr(hs, n, orig[n])
+        return g, evs, wev, rpev
+
+    def capture_pass(events):
+        """One graph holding the K timed steps, each after the L2 flush; with
+        `events`, a pair of CUDA events inside the graph around each step.  The
+        pass is one graph launch, so no timed step carries a graph launch of
+        its own (as in a serving step, whose graph holds every layer)."""
+        evs = [(timing_event()[0], timing_event()[0]) for _ in range(K)] if events else None
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                s = torch.cuda.current_stream()
+                for i in range(K):
+                    flush.fill_(i & 0xFF)
+                    if events:
+                        evs[i][0].record(s)
+                    issue(W + i)
+                    if events:
+                        evs[i][1].record(s)
+        return g, evs
+
+    def capture_flush_only():
+        """The pass graph without the steps: K L2 flushes."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                for i in range(K):
+                    flush.fill_(i & 0xFF)
+        return g
+
+    ext_ok = timing_event()[1]
+    plain = [capture(t, False)[0] for t in range(T)]
+    plain_alt = [capture(t, False, sel_alt)[0] for t in range(T)] if sel_alt is not None else None
+    instr = [capture(t, ext_ok) for t in range(T)] if ext_ok else None
+    passg = capture_pass(True) if ext_ok else None
+    pass_net = capture_pass(False)
+    flush_g = capture_flush_only()
+    torch.cuda.synchronize()
+    cur = torch.cuda.current_stream()
+
+    def wake():
+        """About 20 ms of HBM writes: a GPU that sat idle (while the host
+        checked results or sampled clocks) runs its first microseconds of
+        work slower, which a serving GPU, busy step after step, does not."""
+        for i in range(400):
+            flush.fill_(i & 0xFF)
+
+    def from_admission(warm=True):
         hs.reset()
         mem.hot.zero_()
+        admit_all()
         torch.cuda.synchronize()
-        e2e_ms = []
+        if warm:
+            wake()
+            for t in range(W):
+                plain[t].replay()
+            torch.cuda.synchronize()
+
+    def burn(graphs):
+        """Untimed passes over every step, each from the admission state.  The
+        GPU's first accesses to host pages of a new pool pay one-time
+        address-translation work (tens of us to ms per launch, measured to last
+        about two passes over a trace); a serving system pays that once at
+        start-up, so it stays out of the timed steps."""
+        for _ in range(0 if o.no_burn_in else o.burn_in):
+            for t in range(T):
+                graphs[t].replay()
+            torch.cuda.synchronize()
+            from_admission(warm=False)
+
+    def per_step_graphs():
+        """The K timed steps as K graph launches, events outside the graphs
+        (each step pays its own graph launch); returns per-step ms."""
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
+        for i in range(K):
+            flush.fill_(i & 0xFF)     # also keeps the GPU busy while the host enqueues
+            ev[i][0].record(cur)
+            plain[W + i].replay()
+            ev[i][1].record(cur)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in ev]
+
+    def timed_pass():
+        """Pass 1: per-step ms (events inside the pass graph around each step)."""
+        if passg is not None:
+            passg[0].replay()
+            torch.cuda.synchronize()
+            return [a.elapsed_time(b) for a, b in passg[1]]
+        return per_step_graphs()     # no timing events inside graphs in this torch
+
+    def net_pass():
+        """The K steps without any event between them, minus the same graph
+        with the flushes alone: ms per step of the steps' own GPU time."""
+        res = []
+        for _ in range(3):
+            from_admission()
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            e[0].record(cur)
+            pass_net[0].replay()
+            e[1].record(cur)
+            e[2].record(cur)
+            flush_g.replay()
+            e[3].record(cur)
+            torch.cuda.synchronize()
+            res.append((e[0].elapsed_time(e[1]) - e[2].elapsed_time(e[3])) / K)
+        return sorted(res)[1], res
+
+    # ---- burn-in over another trace, then the timed steps (headline only):
+    #      the timed accesses are then not the ones the burn-in warmed ----
+    alt = None
+    if plain_alt is not None:
+        burn(plain_alt)
+        from_admission()
+        alt_ms = timed_pass()
+        alt = {"ms_per_step": round(sum(alt_ms) / K, 4),
+               "selections_per_s": round(G * w.R * w.k * K / (sum(alt_ms) / 1e3), 1),
+               "burn_in": f"{o.burn_in} passes over a trace of another selection seed on "
+                          "the same pool, then the W warm-up and K timed steps of the "
+                          "timed trace"}
+        from_admission(warm=False)
+
+    # ---- burn-in over the timed trace, then pass 1 (the headline): W warm-up
+    #      steps, then exactly K timed steps, the L2 flushed before each, all
+    #      K in one graph launch with an event pair inside the graph around
+    #      every step ----
+    if clocks is not None:   # sampling from before the burn-in until after the timed pass
+        clocks.__enter__()
+        t_wait = time.time()
+        while not clocks.samples and time.time() - t_wait < 5:
+            time.sleep(0.05)
+    burn(plain)
+    splits_burn = {k_: v - splits0.get(k_, 0) for k_, v in thp_splits().items()}
+    splits0 = thp_splits()
+    from_admission()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    step_ms = timed_pass()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if clocks is not None:
+        time.sleep(0.25)           # one more clock sample after the timed region
+        clocks.__exit__()
+    flags, _ = hs.status()
+
+    # ---- the timed run's final state against the oracle ----
+    verify = None
+    if o.verify and not o.resident and w.sel_block_tokens == 1 and o.verify_rows == 1:
+        verify = verify_against_oracle(w, hs, mem, groups, traces, T)
+
+    replay_launches = sum((-(-len(f) // 8) if o.replay == "group" else
+                           0 if o.replay == "inline" else len(f)) for _, f in groups if f)
+    launches = K * (G + replay_launches + (1 if (wb is not None and o.unfused) else 0))
+
+    rep_ms = sg_ms = None
+    # the whole trace more times from the admission state, timed like pass 1
+    rep_ms = []
+    for _ in range(5 if headline else 3):
+        from_admission()
+        rep_ms.append(sum(timed_pass()) / K)
+    if headline:
+        # one graph launch per step (the difference is the graph launch)
+        from_admission()
+        sg_ms = per_step_graphs()
+    net_ms, net_all = net_pass()
+
+    # ---- pass 2 (per-kernel durations): the same steps from the admission
+    #      state, with events inside the graphs around every launch ----
+    from_admission(warm=False)
+    res_ms = wb_ms = rp_ms = cold_ms = None
+    if instr is not None:
         for t in range(T):
-            if t >= args.warmup:
-                flush.fill_(t & 0xFF)
-                s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                s0.record(cur)
-            e_graphs[t].replay()
-            if t >= args.warmup:
-                s1.record(cur)
-                torch.cuda.synchronize()
-                e2e_ms.append(s0.elapsed_time(s1))
+            flush.fill_(t & 0xFF)
+            instr[t][0].replay()
+            torch.cuda.synchronize()
+        res_ms = [[a.elapsed_time(b) for a, b in instr[W + i][1]] for i in range(K)]
+        cold_ms = [a.elapsed_time(b) for a, b in instr[0][1]]
+        wb_ms = [a.elapsed_time(b) for i in range(K) for a, b in instr[W + i][2]]
+        rp_ms = [a.elapsed_time(b) for i in range(K) for a, b in instr[W + i][3]]
+    else:   # no in-graph timing events in this torch: count misses eagerly
+        for t in range(T):
+            plain[t].replay()
+            for gi, (a, _) in enumerate(groups):
+                hs.copy_miss_counts(a, miss_hist[t, gi], stream=cur)
         torch.cuda.synchronize()
-        e2e = {"value": round(sel_per_step * len(e2e_ms) * world / (sum(e2e_ms) / 1e3), 1),
-               "unit": "selections/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-               "mode": "per-step CUDA graph built through the C ABI; the step's inputs packed "
-                       "in one pinned buffer copied up, and its slot vectors copied back, inside "
-                       "the timed region, " + ("by SM threads (hisparse_copy)"
-                                              if args.e2e_copy == "sm" else
-                                              "by the copy engines (cudaMemcpyAsync)")}
-        flags |= hs.status()[0]
+    flags |= hs.status()[0]
+    miss = miss_hist[W:].cpu().numpy().astype(np.int64)       # [K][G][R]
 
-    peaks, peak_src = measured_peaks()
-    kernel_src = os.path.join(ROOT, "host_offload_serving_gb300", "csrc", "hisparse.cu")
-    kname = "resolve_pt_kernel" if args.lookup == 0 else "resolve_kernel"
-    prof = profile_traffic(kernel_src, kname)
-    if args.mirror:   # records move HBM -> HBM: read and write once each
-        bound, ach, peak = "hbm", 2 * fetch_gbs, peaks["hbm_gbs"]
+    total_ms = sum(step_ms)
+    sel_per_step = G * w.R * w.k
+    total_ms_max = max_over_ranks(total_ms, dist, dev)
+    value = job_throughput(sel_per_step * K, total_ms_max / 1e3, world)
+
+    if res_ms is not None:
+        res_flat = [x for r in res_ms for x in r]
     else:
-        bound, ach, peak = "host_link", fetch_gbs, h2d_gbs
-    roof = {"bound": bound, "achieved": round(ach, 2), "peak": round(peak, 2),
-            "unit": "GB/s", "frac": round(ach / peak, 4),
-            "traffic": prof["dram_bytes_per_launch"] if prof else None,
-            "traffic_sysmem": prof["sysmem_bytes_per_launch"] if prof else None,
-            "traffic_source": prof["source"] if prof else None,
-            "traffic_launch_algorithmic_bytes": prof["algorithmic_bytes"] if prof else None,
-            "kernel": kname,
-            "peak_source": (f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if args.mirror else
-                            "pinned cudaMemcpyAsync H2D, 1 GiB x 20, best of 3 rounds, same run"),
-            "algorithmic_bytes_per_launch": miss_bytes / (args.steps * G),
-            "avg_launch_us": round(launch_ms * 1e3, 2),
-            "avg_launch_us_event_window": round(resolve_avg_ms * 1e3, 2), "timing": timing_note,
-            "launch_us_p50_p90_p99_max": [round(pct(0.5), 2), round(pct(0.9), 2),
-                                          round(pct(0.99), 2), round(srt[-1] * 1e3, 2)],
-            "writeback_us_avg": round(1e3 * sum(wb_ms) / len(wb_ms), 2) if wb_ms else None}
-    # ---- admission: every request of every layer reset with its first
-    #      min(B, P) positions preloaded (the short-request path of direct
-    #      admission), and reset alone (the long-request path) ----
-    admission = None
-    if not args.no_allhit:
-        reqs_d = torch.arange(w.R, dtype=torch.int32, device=dev)
-        npre = min(w.B, w.P)
-        pre_d = torch.full((w.R,), npre, dtype=torch.int32, device=dev)
-        ms_pre, ms_rst = [], []
-        for i in range(5):
-            for pre, acc in ((pre_d, ms_pre), (None, ms_rst)):
-                flush.fill_(i)
-                a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a0.record(cur)
-                hs.admit(-1, reqs_d, pre, stream=cur)
-                a1.record(cur)
-                torch.cuda.synchronize()
-                acc.append(a0.elapsed_time(a1))
-        ab = w.R * w.L * npre * w.rec
-        t_pre = sorted(ms_pre)[len(ms_pre) // 2]
-        admission = {"preload_positions": npre, "bytes": ab,
-                     "us_preload_all": round(t_pre * 1e3, 1),
-                     "preload_gbs": round(ab / (t_pre / 1e3) / 1e9, 2),
-                     "preload_frac_of_link": round(ab / (t_pre / 1e3) / 1e9 / h2d_gbs, 4),
-                     "us_reset_all": round(sorted(ms_rst)[len(ms_rst) // 2] * 1e3, 1),
-                     "timing": "hisparse_admit of every request on every layer, median of 5, "
-                               "L2 flushed before each"}
-        flags |= hs.status()[0]
+        res_flat = [x / G for x in step_ms]
+    resolve_avg_ms = sum(res_flat) / len(res_flat)
+    srt = sorted(res_flat)
+    pct = lambda q: srt[min(len(srt) - 1, int(q * (len(srt) - 1) + 0.5))] * 1e3  # noqa: E731
+    # When a step holds nothing but the RESOLVE launches (write-through fused,
+    # no replay launches), a launch's duration is the step time over the
+    # launches per step: from pass 1 (events around each step) and from the
+    # event-free pass (the steps' own GPU time).
+    inline = o.replay == "inline"
+    only_resolve = (all(not f for _, f in groups) or (inline and wb is None)) and \
+        not (o.unfused and wb is not None)
+    if only_resolve:
+        launch_ms = (total_ms / K) / G
+        launch_net_ms = net_ms / G
+        timing_note = ("launch = step time / RESOLVE launches per step (the step holds only "
+                       "RESOLVE launches). avg_launch_us: the event-free pass (the K steps in "
+                       "one graph with no event between them, minus the same graph with the "
+                       "L2 flushes alone; median of 3). avg_launch_us_step_events: pass 1, "
+                       "CUDA events inside the pass graph around each step (each step then "
+                       "also carries its two events' idle time). Percentiles: per-launch event "
+                       "windows in a second pass over the same steps")
+    else:
+        launch_ms = resolve_avg_ms
+        launch_net_ms = None
+        timing_note = ("launch = per-launch event windows in a second pass over the same steps "
+                       "(the step also holds replay or write-back launches)")
+    miss_bytes = int(miss.sum()) * w.rec
+    if inline:   # a RESOLVE launch also moves every miss's rows of its shared-index layers
+        miss_bytes = sum(int(miss[:, gi].sum()) * (1 + len(f))
+                         for gi, (_, f) in enumerate(groups)) * w.rec
+    n_launch = K * G
+    fetch_gbs = miss_bytes / (launch_ms * n_launch / 1e3) / 1e9
+    fetch_net_gbs = (miss_bytes / (launch_net_ms * n_launch / 1e3) / 1e9
+                     if launch_net_ms else None)
+    miss_rate = float(miss.sum()) / (K * G * w.R * w.k)
 
-    # step 0 from the admission state: every selection but the newest misses,
-    # so each launch moves R x k records -- the fetch path at full size
     cold = None
     if cold_ms:
         cb = int(miss_hist[0].sum().item()) * w.rec
+        if inline:
+            cb = sum(int(miss_hist[0, gi].sum().item()) * (1 + len(f))
+                     for gi, (_, f) in enumerate(groups)) * w.rec
         c_s = sum(cold_ms) / 1e3
         cold = {"us_per_launch": round(1e3 * sum(cold_ms) / len(cold_ms), 2),
                 "bytes_per_launch": cb // G, "fetch_gbs": round(cb / c_s / 1e9, 2),
@@ -919,87 +872,431 @@ def run_ours(args):
                   "fetch_gbs": round(rp_bytes / (sum(rp_ms) / 1e3) / 1e9, 2),
                   "frac_of_link": round(rp_bytes / (sum(rp_ms) / 1e3) / 1e9 / h2d_gbs, 4),
                   "followers_per_step": nf,
-                  "layers_per_launch": round(nf * args.steps / len(rp_ms), 2)}
-    if allhit:
-        allhit["hbm_peak_gbs"] = peaks.get("hbm_gbs")
-        allhit["hbm_frac"] = round(allhit["hbm_gbs"] / peaks.get("hbm_gbs"), 5)
-        allhit["hbm_peak_source"] = f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+                  "layers_per_launch": round(nf * K / len(rp_ms), 2),
+                  "order": "each CTA batch of plan records read in source-address order"}
 
-    cpu = cpu_mt = None
-    if rank == 0 and not args.no_cpu and not args.resident:
-        views = {l: mem.host_view(l) for l in range(w.L)}
-        ttr = token_traces(w, traces)
-        uni = args.verify_rows > 1
-        cpu = cpu_oracle_rate(w, ttr, host_views=views, budget_s=20.0, union=uni)
-        cpu.pop("seconds", None)
-        cpu.pop("steps", None)
-        cpu_mt = cpu_oracle_rate_threads(w, ttr, views, os.cpu_count() or 1, union=uni)
-        cpu_mt.pop("seconds", None)
-
-    hp_frac_end = mem.pool.hugepage_fraction()
-    s1 = thp_splits()
-    splits_run = {k: s1[k] - splits0.get(k, 0) for k in s1}
-    hs.close()
-    mem.close()
-    if rank == 0:
-        line = {
-            "metric": METRIC, "value": round(value, 1), "unit": "selections/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(total_ms_max / args.steps, 4), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
-            "config": {"workload": w.name, "requests": w.R, "layers": w.L, "anchors": G,
-                       "top_k": w.k, "B": w.B, "L_ctx": w.L_ctx, "record_bytes": w.rec,
-                       "write_through": w.write_through, "parallelism": f"replicas{world}",
-                       "l2": "flushed (256 MB write) before every timed step",
-                       "ctas_per_request": info["ctas_per_request"],
-                       "lookup": ["page_table", "hash"][info["lookup"]],
-                       "write_through_launch": "separate" if args.unfused else "fused into RESOLVE",
-                       "host_pool": args.pool,
-                       "replay_launch": {"group": "one per anchor for all its shared-index layers",
-                                         "layer": "one per shared-index layer",
-                                         "inline": "none: shared-index layers filled inside "
-                                                   "the anchor's RESOLVE"}[args.replay],
-                       "host_layout": ("rows of each shared-index group interleaved"
-                                       if args.interleave else "one block of rows per layer"),
-                       "fetch_source": "HBM mirror of the host pool" if args.mirror else "host pool",
-                       "verify_rows": args.verify_rows,
-                       "resident_tier": (dict(zip(("full_requests", "window", "tokens_per_block"),
-                                                  (int(x) for x in args.resident.split(","))))
-                                         if args.resident else None),
-                       "host_pool_hugepage_fraction": round(hp_frac, 3),
-                       "host_pool_hugepage_fraction_end": round(hp_frac_end, 3),
-                       "host_thp_splits_during_burn_in": splits_burn,
-                       "host_thp_splits_during_run": splits_run,
-                       "burn_in": None if args.no_burn_in else
-                       f"{args.burn_in} untimed passes over all steps, each from the admission state"},
-            "roofline": roof,
-            "miss_fetch_gbs": round(fetch_gbs, 2), "h2d_link_gbs": round(h2d_gbs, 2),
-            "miss_rate": round(miss_rate, 4),
-            "us_per_layer_step": round(launch_ms * 1e3, 2),
-            "all_hit_no_io": allhit,
-            "cold_step0": cold,
+    # algorithmic HBM bytes of one RESOLVE launch (the metadata side): per unit
+    # 4k selections + 4k slot vector + 4B slot map + 2B + 2B LRU order in and
+    # out + 12 per miss (slot map and two page-table writes) + the missed
+    # records written into the hot buffer; this design also gathers one 4-byte
+    # page-table entry per selection
+    Mbar = int(miss.sum()) / n_launch
+    hbm_alg = (w.R * (4 * w.k + 4 * w.k + 4 * w.B + 2 * w.B + 2 * w.B) + Mbar * (12 + w.rec)
+               + (2 * w.R * w.rec if w.write_through else 0))
+    hbm_peak = measured_peaks()[0]["hbm_gbs"]
+    hbm_gbs = hbm_alg / ((launch_net_ms or launch_ms) / 1e3) / 1e9
+    fig = {
+        "workload": w.name, "steps": K, "warmup": W,
+        "selections_per_s": round(value, 1), "ms_per_step": round(total_ms_max / K, 4),
+        "ms_per_step_net": round(net_ms, 4),
+        "ms_per_step_repeats": [round(x, 4) for x in rep_ms],
+        "ms_per_step_net_runs": [round(x, 4) for x in net_all],
+        "us_per_layer_step": round(launch_ms * 1e3, 2),
+        "us_per_layer_step_net": round(launch_net_ms * 1e3, 2) if launch_net_ms else None,
+        "launch_us_p50_p90_p99_max": [round(pct(0.5), 2), round(pct(0.9), 2),
+                                      round(pct(0.99), 2), round(srt[-1] * 1e3, 2)],
+        "avg_launch_us_event_window": round(resolve_avg_ms * 1e3, 2),
+        "miss_rate": round(miss_rate, 4),
+        "miss_bytes_per_launch": miss_bytes / n_launch,
+        "fetch_gbs": round(fetch_gbs, 2), "fetch_frac_of_link": round(fetch_gbs / h2d_gbs, 4),
+        "fetch_gbs_net": round(fetch_net_gbs, 2) if fetch_net_gbs else None,
+        "fetch_frac_of_link_net": round(fetch_net_gbs / h2d_gbs, 4) if fetch_net_gbs else None,
+        "hbm_algorithmic_bytes_per_launch": round(hbm_alg),
+        "hbm_gbs": round(hbm_gbs, 2), "hbm_frac": round(hbm_gbs / hbm_peak, 5),
+        "cold_step0": cold, "replay": replay, "verify": verify, "status_flags": flags,
+        "setup_s": round(setup_s, 1), "host_pool_gb": round(w.host_bytes() / 1e9, 1),
+        "timing": timing_note,
+        "_launch_ms": launch_ms, "_launch_net_ms": launch_net_ms, "_miss_bytes": miss_bytes,
+        "_launches": launches, "_total_ms_max": total_ms_max,
+    }
+    if headline:
+        fig.update({
+            "info": info, "wb_ms": wb_ms, "burn_in_other_trace": alt,
             "repeats": {"ms_per_step": [round(x, 4) for x in rep_ms],
                         "median_ms_per_step": round(sorted(rep_ms)[len(rep_ms) // 2], 4),
                         "timing": "the whole trace 5 more times from the admission state, "
-                                  "timed like pass 1"},
+                                  "timed like pass 1 (sub-workloads: 3 times)"},
             "step_graphs": {"ms_per_step": round(sum(sg_ms) / len(sg_ms), 4),
-                            "selections_per_s": round(sel_per_step * len(sg_ms) / (sum(sg_ms) / 1e3), 1),
-                            "timing": "the same steps from the admission state, one graph launch "
-                                      "per step, events outside the graphs: adds each step's "
-                                      "graph launch to its time"},
-            "timing": ("pass graph: the K timed steps in one graph launch, the L2 flush before "
-                       "each step, CUDA events recorded inside the graph around each step"
-                       if passg is not None else "one graph launch per step, events outside"),
-            "admission": admission,
-            "replay": replay,
-            "e2e": e2e,
-            "cpu_baseline": cpu,
-            "cpu_baseline_threads": cpu_mt,
-            "gpu_launches": launches,
+                            "selections_per_s": round(sel_per_step * len(sg_ms) /
+                                                      (sum(sg_ms) / 1e3), 1),
+                            "timing": "the same steps from the admission state, one graph "
+                                      "launch per step, events outside the graphs: adds each "
+                                      "step's graph launch to its time"},
+            "timing_pass": ("pass graph: the K timed steps in one graph launch, the L2 flush "
+                            "before each step, CUDA events recorded inside the graph around "
+                            "each step" if passg is not None else
+                            "one graph launch per step, events outside"),
+            "host_pool_hugepage_fraction": round(hp_frac, 3),
+            "host_thp_splits_during_burn_in": splits_burn,
+        })
+        fig["all_hit_no_io"] = all_hit(o, w, hs, groups, sel, newest, out, flush, cap, cur, G)
+        fig["e2e"] = None if o.no_e2e else end_to_end(
+            o, w, hs, mem, runner, sel_np, newest_np, wb, out, flush, cap, cur, T, world,
+            sm_copy, res_all, res_tok, seq_dev, admit_all)
+        fig["admission"] = admission(w, hs, flush, cur, dev, h2d_gbs)
+        flags |= hs.status()[0]
+        fig["status_flags"] = flags
+        fig["host_pool_hugepage_fraction_end"] = round(mem.pool.hugepage_fraction(), 3)
+        s1 = thp_splits()
+        fig["host_thp_splits_during_run"] = {k_: s1[k_] - splits0.get(k_, 0) for k_ in s1}
+
+    # ---- the oracle on the host cores, on a bounded sample ----
+    if rank == 0 and not o.no_cpu and not o.resident:
+        views = {l: mem.host_view(l) for l in range(w.L)}
+        ttr = token_traces(w, traces)
+        uni = o.verify_rows > 1
+        cpu = cpu_oracle_rate(w, ttr, host_views=views, budget_s=20.0 if headline else 5.0,
+                              union=uni)
+        cpu.pop("seconds", None)
+        cpu.pop("steps", None)
+        fig["cpu_baseline"] = cpu
+        if headline:
+            cpu_mt = cpu_oracle_rate_threads(w, ttr, views, os.cpu_count() or 1, union=uni)
+            cpu_mt.pop("seconds", None)
+            fig["cpu_baseline_threads"] = cpu_mt
+    hs.close()
+    mem.close()
+    del plain, plain_alt, instr, passg, pass_net, flush_g
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return fig
+
+
+def all_hit(o, w, hs, groups, sel, newest, out, flush, cap, cur, G):
+    """All-hit / no-IO: the last step's selections again, with SKIP_IO.  Every
+    selection is now resident, so this is the metadata path alone (lookup,
+    scans, publish) against HBM."""
+    import numpy as np
+    import torch
+    from host_offload_serving_gb300 import hisparse as H
+    if o.no_allhit:
+        return None
+    t_last = o.warmup + o.steps - 1
+    gh = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(gh, stream=cap):
+            for gi, (a, _) in enumerate(groups):
+                hs.resolve_ex(a, sel[t_last, gi], out[gi], None,
+                              newest[t_last] if newest is not None else None,
+                              sel_block_tokens=w.sel_block_tokens,
+                              flags=H.SKIP_IO | (H.UNION if o.verify_rows > 1 else 0),
+                              stream=torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    hit_ms = []
+    for i in range(10):
+        flush.fill_(i)
+        h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        h0.record(cur)
+        gh.replay()
+        h1.record(cur)
+        torch.cuda.synchronize()
+        hit_ms.append(h0.elapsed_time(h1) / G)
+    mc = np.stack([hs.export_state(a)[3] for a, _ in groups])
+    hit_avg = sum(hit_ms) / len(hit_ms)
+    alg = w.R * (4 * w.k + 4 * w.B + 2 * w.B + 2 * w.B + 4 * w.k)   # bytes per launch
+    peaks, peak_src = measured_peaks()
+    gbs = alg / (hit_avg / 1e3) / 1e9
+    return {"us_per_layer_step": round(hit_avg * 1e3, 2), "misses": int(mc.sum()),
+            "selections_per_s": round(w.R * w.k / (hit_avg / 1e3), 1),
+            "algorithmic_bytes_per_launch": alg, "hbm_gbs": round(gbs, 3),
+            "hbm_peak_gbs": peaks.get("hbm_gbs"),
+            "hbm_frac": round(gbs / peaks.get("hbm_gbs"), 5),
+            "hbm_peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
+            "timing": "graph of one SKIP_IO resolve per anchor, time / anchors"}
+
+
+def end_to_end(o, w, hs, mem, runner, sel_np, newest_np, wb, out, flush, cap, cur, T, world,
+               sm_copy, res_all, res_tok, seq_dev, admit_all):
+    """End to end through the C ABI with host buffers: every step copies its
+    selections (and write-back positions, new-token KV) from pinned host
+    memory and reads the slot vectors back, inside the timed region.  Steps
+    are captured as graphs, as a serving loop would."""
+    import numpy as np
+    import torch
+    from workload import records as REC
+    G = sel_np.shape[1]
+    # A step's inputs (selections; with write-through also the newest
+    # positions, the write-back positions and the new tokens' KV) travel packed
+    # in one pinned buffer: one host-to-device copy per step, then the RESOLVE
+    # launches, then one device-to-host copy of the slot vectors.
+    parts = [("sel", tuple(sel_np.shape[1:]), 4)]
+    if w.write_through:
+        parts += [("newest", (w.R,), 4), ("wb", (w.L, w.R), 4), ("new", (w.L, w.R, w.rec), 1)]
+    offs, off = {}, 0
+    for name, shape, isz in parts:
+        offs[name] = off
+        off += -(-int(np.prod(shape)) * isz // 16) * 16
+    h_pack = torch.zeros((T, off), dtype=torch.uint8).pin_memory()
+    d_pack = torch.empty(off, dtype=torch.uint8, device=out.device)
+
+    def view(buf, name):
+        shape, isz = next((sh, z) for n, sh, z in parts if n == name)
+        nb = int(np.prod(shape)) * isz
+        return buf[offs[name]:offs[name] + nb].view(torch.int32 if isz == 4 else torch.uint8).view(shape)
+
+    h_new = REC.new_token_records(w) if w.write_through else None
+    wb_np = wb.cpu().numpy() if w.write_through else None
+    for t in range(T):
+        view(h_pack[t], "sel").copy_(torch.from_numpy(sel_np[t]))
+        if w.write_through:
+            view(h_pack[t], "newest").copy_(torch.from_numpy(newest_np[t]))
+            view(h_pack[t], "wb").copy_(torch.from_numpy(wb_np[t]))
+            view(h_pack[t], "new").copy_(torch.from_numpy(h_new[t]))
+    h_out = torch.empty((T, G, w.R, w.k), dtype=torch.int32).pin_memory()
+    wt = w.write_through
+    e_graphs = []
+    for t in range(T):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                if o.e2e_copy == "sm":
+                    sm_copy(d_pack, h_pack[t])
+                else:
+                    d_pack.copy_(h_pack[t], non_blocking=True)
+                if res_all is not None:
+                    runner.resident = (res_all[t], res_tok)
+                runner.issue(view(d_pack, "sel"), out,
+                             newest=view(d_pack, "newest") if wt else None,
+                             wb_pos=view(d_pack, "wb") if (wt and t > 0) else None,
+                             new_rows=view(d_pack, "new") if wt else None,
+                             seq_lens=seq_dev[t] if seq_dev is not None else None)
+                if o.e2e_copy == "sm":
+                    sm_copy(h_out[t], out)
+                else:
+                    h_out[t].copy_(out, non_blocking=True)
+        e_graphs.append(g)
+
+    def reset():
+        hs.reset()
+        mem.hot.zero_()
+        admit_all()
+        torch.cuda.synchronize()
+    for _ in range(0 if o.no_burn_in else o.burn_in):   # as for pass 1
+        reset()
+        for t in range(T):
+            e_graphs[t].replay()
+        torch.cuda.synchronize()
+    reset()
+    e2e_ms = []
+    for t in range(T):
+        if t >= o.warmup:
+            flush.fill_(t & 0xFF)
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0.record(cur)
+        e_graphs[t].replay()
+        if t >= o.warmup:
+            s1.record(cur)
+            torch.cuda.synchronize()
+            e2e_ms.append(s0.elapsed_time(s1))
+    torch.cuda.synchronize()
+    sel_per_step = G * w.R * w.k
+    return {"value": round(sel_per_step * len(e2e_ms) * world / (sum(e2e_ms) / 1e3), 1),
+            "unit": "selections/s", "h2d_bytes_per_step": off,
+            "d2h_bytes_per_step": h_out[0].numel() * 4,
+            "mode": "per-step CUDA graph built through the C ABI; the step's inputs packed in "
+                    "one pinned buffer copied up, and its slot vectors copied back, inside the "
+                    "timed region, " + ("by SM threads (hisparse_copy)" if o.e2e_copy == "sm"
+                                        else "by the copy engines (cudaMemcpyAsync)")}
+
+
+def admission(w, hs, flush, cur, dev, h2d_gbs):
+    """Every request of every layer reset with its first min(B, P) positions
+    preloaded (the short-request path of direct admission), and reset alone
+    (the long-request path)."""
+    import torch
+    reqs_d = torch.arange(w.R, dtype=torch.int32, device=dev)
+    npre = min(w.B, w.P)
+    pre_d = torch.full((w.R,), npre, dtype=torch.int32, device=dev)
+    ms_pre, ms_rst = [], []
+    for i in range(5):
+        for pre, acc in ((pre_d, ms_pre), (None, ms_rst)):
+            flush.fill_(i)
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(cur)
+            hs.admit(-1, reqs_d, pre, stream=cur)
+            a1.record(cur)
+            torch.cuda.synchronize()
+            acc.append(a0.elapsed_time(a1))
+    ab = w.R * w.L * npre * w.rec
+    t_pre = sorted(ms_pre)[len(ms_pre) // 2]
+    return {"preload_positions": npre, "bytes": ab,
+            "us_preload_all": round(t_pre * 1e3, 1),
+            "preload_gbs": round(ab / (t_pre / 1e3) / 1e9, 2),
+            "preload_frac_of_link": round(ab / (t_pre / 1e3) / 1e9 / h2d_gbs, 4),
+            "us_reset_all": round(sorted(ms_rst)[len(ms_rst) // 2] * 1e3, 1),
+            "timing": "hisparse_admit of every request on every layer, median of 5, "
+                      "L2 flushed before each"}
+
+
+def sub_workload(args, name):
+    """(workload, options) of one entry of the line's `workloads` object, or
+    (None, reason) when it cannot run here."""
+    from workload import get, sweep_workload
+    base = dict(no_e2e=True, no_allhit=True, resident="", verify_rows=1, unfused=False,
+                mirror=False, L_ctx=0)
+    if name == "tiny":
+        w = get("tiny")
+        return w, opts_for(args, replay="group", interleave=False, **base)
+    if name == "quest":
+        return get("quest"), opts_for(args, replay="group", interleave=False, **base)
+    if name == "short":
+        return get("short"), opts_for(args, replay="group", interleave=False, **base)
+    if name in ("shared_inline", "shared_anchor"):
+        return get("shared"), opts_for(args, replay="inline" if name == "shared_inline"
+                                       else "group", interleave=True, **base)
+    if name in ("sweep", "sweep_allhit"):
+        B, f = SWEEP_POINT
+        L, why = pick_sweep_context(B, f)
+        if L is None:
+            return None, {"reason": "no capacity-sweep context leaves the host-memory margin",
+                          **why}
+        w = sweep_workload(B, f, L_ctx=L, all_hit=name == "sweep_allhit")
+        if name == "sweep_allhit":   # the HBM mirror of the pool must fit beside the rest
+            import torch
+            free = torch.cuda.mem_get_info()[0]
+            if free < w.host_bytes() + w.hot_bytes() + (16 << 30):
+                return None, {"reason": "the HBM mirror does not fit", "hbm_free_gb":
+                              round(free / 1e9, 1), "mirror_gb": round(w.host_bytes() / 1e9, 1)}
+        kw = dict(base, mirror=name == "sweep_allhit")
+        o = opts_for(args, replay="group", interleave=False, **kw)
+        o._context_choice = why
+        return w, o
+    raise KeyError(name)
+
+
+def sub_steps(args, w):
+    """(warm-up, timed) steps of a workload entry: the bench's, within the
+    workload's own step count."""
+    W = min(args.warmup, max(3, w.steps // 4))
+    return W, max(1, min(args.steps, w.steps - W))
+
+
+# --------------------------------------------------------------------------- #
+def run_ours(args):
+    import torch
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from host_offload_serving_gb300.replicas import replica_seed
+    from workload import get
+
+    dev = torch.device("cuda", local)
+    h2d_gbs = h2d_probe(dev)
+    w = get(args.workload)
+    if args.L_ctx:
+        w = w.scaled(L_ctx=args.L_ctx)
+    if w.write_through:
+        w = w.scaled(steps=max(w.steps, args.warmup + args.steps))
+    w = w.scaled(seed=replica_seed(w.seed, rank))     # each replica its own requests
+    clocks = Clocks(local)
+    fig = measure(args, w, dev, h2d_gbs, dist=dist, world=world, headline=True, rank=rank,
+                  clocks=clocks)
+
+    # ---- the other workloads, each on its own pool (one GPU only) ----
+    subs = {}
+    names = [] if (args.no_workloads or world > 1) else \
+        [n for n in args.workloads.split(",") if n]
+    for name in names:
+        wo = sub_workload(args, name)
+        if wo[0] is None:
+            subs[name] = {"skipped": wo[1]}
+            continue
+        ws, os_ = wo
+        Wd, Kd = sub_steps(args, ws)
+        os_.warmup, os_.steps = Wd, Kd
+        try:
+            f = measure(os_, ws, dev, h2d_gbs, rank=rank)
+        except Exception as e:   # recorded on the line, the headline stands
+            subs[name] = {"error": f"{type(e).__name__}: {e}"}
+            torch.cuda.synchronize()
+            torch.cuda.empty_cache()
+            continue
+        for k_ in [k_ for k_ in f if k_.startswith("_")]:
+            f.pop(k_)
+        f["config"] = workload_config(ws, os_, world)
+        if getattr(os_, "_context_choice", None):
+            f["context_choice"] = os_._context_choice
+        subs[name] = f
+
+    peaks, peak_src = measured_peaks()
+    kernel_src = os.path.join(ROOT, "host_offload_serving_gb300", "csrc", "hisparse.cu")
+    kname = "resolve_pt_kernel" if args.lookup == 0 else "resolve_kernel"
+    prof = profile_traffic(kernel_src, kname)
+    K = args.steps
+    G = len(w.anchors())
+    launch_ms = fig["_launch_net_ms"] or fig["_launch_ms"]
+    ach_link = fig["_miss_bytes"] / (launch_ms * K * G / 1e3) / 1e9
+    if args.mirror:   # records move HBM -> HBM: read and write once each
+        bound, ach, peak = "hbm", 2 * ach_link, peaks["hbm_gbs"]
+    else:
+        bound, ach, peak = "host_link", ach_link, h2d_gbs
+    roof = {"bound": bound, "achieved": round(ach, 2), "peak": round(peak, 2),
+            "unit": "GB/s", "frac": round(ach / peak, 4),
+            "target_frac": TARGET_LINK_FRAC if bound == "host_link" else None,
+            "meets_target": (ach / peak >= TARGET_LINK_FRAC) if bound == "host_link" else None,
+            "frac_step_events": round((2 if args.mirror else 1) * fig["_miss_bytes"] /
+                                      (fig["_launch_ms"] * K * G / 1e3) / 1e9 / peak, 4),
+            "traffic": prof["dram_bytes_per_launch"] if prof else None,
+            "traffic_sysmem": prof["sysmem_bytes_per_launch"] if prof else None,
+            "traffic_source": prof["source"] if prof else None,
+            "traffic_vs": ("dram__bytes_read + dram__bytes_write of one captured launch, against "
+                           "hbm_algorithmic_bytes_per_launch (the metadata side and the hot-row "
+                           "writes); the host-link reads are traffic_sysmem, against "
+                           "algorithmic_bytes_per_launch"),
+            "hbm_algorithmic_bytes_per_launch": fig["hbm_algorithmic_bytes_per_launch"],
+            "kernel": kname,
+            "peak_source": (f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if args.mirror else
+                            "pinned cudaMemcpyAsync H2D, 1 GiB x 20, best of 3 rounds, same run"),
+            "algorithmic_bytes_per_launch": fig["miss_bytes_per_launch"],
+            "avg_launch_us": round(launch_ms * 1e3, 2),
+            "avg_launch_us_step_events": round(fig["_launch_ms"] * 1e3, 2),
+            "avg_launch_us_event_window": fig["avg_launch_us_event_window"],
+            "timing": fig["timing"],
+            "launch_us_p50_p90_p99_max": fig["launch_us_p50_p90_p99_max"],
+            "writeback_us_avg": (round(1e3 * sum(fig["wb_ms"]) / len(fig["wb_ms"]), 2)
+                                 if fig.get("wb_ms") else None)}
+    if rank == 0:
+        info = fig["info"]
+        cfg = workload_config(w, args, world)
+        line = {
+            "metric": METRIC, "value": fig["selections_per_s"], "unit": "selections/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": fig["ms_per_step"], "ms_per_step_net": fig["ms_per_step_net"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
+            "data": "synthetic", "config": cfg,
+            "run": {"ctas_per_request": info["ctas_per_request"],
+                    "smem_bytes_per_cta": info["smem_bytes"],
+                    "metadata_bytes": info["metadata_bytes"],
+                    "host_pool_hugepage_fraction": fig["host_pool_hugepage_fraction"],
+                    "host_pool_hugepage_fraction_end": fig["host_pool_hugepage_fraction_end"],
+                    "host_thp_splits_during_burn_in": fig["host_thp_splits_during_burn_in"],
+                    "host_thp_splits_during_run": fig["host_thp_splits_during_run"],
+                    "setup_s": fig["setup_s"]},
+            "roofline": roof,
+            "miss_fetch_gbs": fig["fetch_gbs"], "miss_fetch_gbs_net": fig["fetch_gbs_net"],
+            "h2d_link_gbs": round(h2d_gbs, 2), "miss_rate": fig["miss_rate"],
+            "us_per_layer_step": fig["us_per_layer_step"],
+            "us_per_layer_step_net": fig["us_per_layer_step_net"],
+            "all_hit_no_io": fig["all_hit_no_io"],
+            "cold_step0": fig["cold_step0"],
+            "burn_in_other_trace": fig["burn_in_other_trace"],
+            "repeats": fig["repeats"],
+            "step_graphs": fig["step_graphs"],
+            "timing": fig["timing_pass"],
+            "admission": fig["admission"],
+            "replay": fig["replay"],
+            "e2e": fig["e2e"],
+            "cpu_baseline": fig.get("cpu_baseline"),
+            "cpu_baseline_threads": fig.get("cpu_baseline_threads"),
+            "gpu_launches": fig["_launches"],
             "clocks": clocks.summary(),
-            "status_flags": flags,
-            "setup_s": round(setup_s, 1),
-            "verify": verify,
+            "status_flags": fig["status_flags"],
+            "verify": fig["verify"],
+            "workloads": subs if names else None,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -1008,23 +1305,59 @@ def run_ours(args):
 
 
 def verify_against_oracle(w, hs, mem, groups, traces, steps):
-    """Replay the same steps on the oracle and compare the final state (sampled bytes)."""
+    """Replay the same steps on the oracle and compare the final state: slot
+    maps, LRU orders, page tables and miss counts of every anchor, and the
+    bytes of a sample of occupied hot rows (of every layer) against records
+    generated afresh for their positions."""
     import numpy as np
     from oracle.coracle import OracleLayer
     from workload import records as REC
-    anchors = [a for a, _ in groups]
     res = {}
-    for a in anchors:
+    rng = np.random.default_rng(1)
+    hot = mem.hot
+    new_rows = REC.new_token_records(w) if w.write_through else None
+    ok_all = True
+    for a, fl in groups:
         o = OracleLayer(w.R, w.k, w.B, w.P, w.rec, host=mem.host_view(a), host_split=w.L_ctx,
                         keep_bytes=False)
         o.reset()
+        if w.admit_preload:
+            for r in range(w.R):
+                o.admit(r, w.L_ctx, io=False)
         for t in range(steps):
             nw = traces[a][1][t] if w.write_through else None
-            o.resolve(traces[a][0][t], nw)
+            if w.admit_preload:
+                prev = traces[a][1][t - 1] if t > 0 else np.full(w.R, -1, np.int32)
+                o.resolve_with_seq_lens(traces[a][0][t], nw, prev,
+                                        np.full(w.R, w.L_ctx + t + 1, np.int32), io=False)
+            else:
+                o.resolve(traces[a][0][t], nw)
         sp, lru, pt, mc = hs.export_state(a)
         ok = (np.array_equal(sp, o.slot_pos) and np.array_equal(lru, o.lru)
               and np.array_equal(pt, o.page_table) and np.array_equal(mc, o.miss_count))
-        res[str(a)] = bool(ok)
+        # sampled bytes: hot row s of every layer of the group holds the
+        # record of the position in slot s
+        nbad = nchk = 0
+        picks = []
+        for r in range(w.R):
+            occ = np.flatnonzero(sp[r] >= 0)
+            if len(occ):
+                picks += [(r, int(s)) for s in rng.choice(occ, size=min(32, len(occ)),
+                                                         replace=False)]
+        if picks:
+            ri = [r for r, _ in picks]
+            si = [s for _, s in picks]
+            for l in [a] + list(fl):
+                got = hot[l][ri, si].cpu().numpy()              # one gather per layer
+                for j, (r, s) in enumerate(picks):
+                    p = int(sp[r, s])
+                    exp = (REC.records(w, l, r, [p])[0] if p < w.L_ctx
+                           else new_rows[p - w.L_ctx, l, r])
+                    nchk += 1
+                    nbad += int(not np.array_equal(got[j], exp))
+        res[str(a)] = {"state": bool(ok), "rows_checked": nchk, "rows_differ": nbad}
+        ok_all = ok_all and ok and nbad == 0
+    res["ok"] = bool(ok_all)
     return res
 
 

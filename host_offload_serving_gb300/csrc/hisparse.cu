@@ -673,6 +673,10 @@ struct PtArgs {
   // Union mode (speculative verify rows resolved as one list): a repeated
   // position is resolved at its first reference and shares its row.
   int32_t union_mode;
+  // Short requests (hisparse_resolve_options.d_seq_lens): a request whose
+  // seq_len is at most B grows by its previous token and is looked up by
+  // position; NULL = every request takes the general path.
+  const int32_t *seq_lens;
   // Shared-index layers filled in the same launch (HISPARSE_WITH_SHARED):
   // every missed record's row of each, at the anchor's victim slot.
   int32_t nfl;
@@ -1400,6 +1404,142 @@ __device__ void pt_leader_write_through(const PtArgs &a, int r, int32_t prev, un
   }
 }
 
+// Short request ([DD] §5.4: with seq_len <= B every token of the request sits
+// in the buffer in order and RESOLVE returns slots by position, with no host
+// IO; the buffer grows on demand; §5.5: the kernel's fast path returns before
+// any LRU work).  Run by the leader CTA alone, the cluster's other CTAs having
+// left:
+//   1. the fused write-through (row B kept, new token in, kept row to the
+//      host pool and its mirror);
+//   2. growth: the previous token resolved as a one-entry selection -- a hit
+//      moves its slot to the recent end of the LRU order; a miss takes the
+//      least recent slot, filled from the kept row (and, inline, the shared
+//      layers' rows), mapped, planned, and moved to the recent end;
+//   3. the lookup: padding -1, a resident row first, the newest token B, a
+//      position in [0, seq_len) its own slot, anything else fails the lookup.
+template <bool kRecordPlan>
+__device__ void pt_short_path(const PtArgs &a, int r, int32_t prev, int32_t newest,
+                              int32_t seq_len, unsigned char *smem, const PtLayout &L) {
+  const int tid = threadIdx.x;
+  const int B = a.B, k = a.k;
+  const int64_t P = a.P;
+  int16_t *l_lru = reinterpret_cast<int16_t *>(smem + L.l_lru);
+  int32_t *l_out = reinterpret_cast<int32_t *>(smem + L.l_ev);   // k entries
+  uint32_t *l_misc = reinterpret_cast<uint32_t *>(smem + L.l_misc);
+  int32_t *g_pt = a.page_table + static_cast<int64_t>(r) * P;
+  int32_t *g_sp = a.slot_pos + static_cast<int64_t>(r) * B;
+  int16_t *g_lru = a.lru + static_cast<int64_t>(r) * B;
+  const uint4 *keep = reinterpret_cast<const uint4 *>(smem + L.l_prevrow);
+
+  // (1) write-through
+  pt_leader_write_through(a, r, prev, smem, L);
+  if (tid == 0) {
+    l_misc[kLErr] = (newest < -1 || newest >= P) ? HISPARSE_ERR_RANGE : 0u;
+    l_misc[kLM] = 0;
+    l_misc[kLHits] = 0;
+  }
+  __syncthreads();
+  const bool grow = a.prev_pos && prev >= 0 && prev < P;
+  if (grow) {
+    uint4 *hrow = reinterpret_cast<uint4 *>(a.host_w + static_cast<int64_t>(r) * a.host_req_stride +
+                                            static_cast<int64_t>(prev) * a.host_row_stride);
+    for (int c = tid; c < a.rec16; c += kThreads) st_v4(hrow + c, keep[c]);
+    if (a.mirror_w) {
+      uint4 *mrow = reinterpret_cast<uint4 *>(a.mirror_w + static_cast<int64_t>(r) * a.host_req_stride +
+                                              static_cast<int64_t>(prev) * a.host_row_stride);
+      for (int c = tid; c < a.rec16; c += kThreads) st_v4(mrow + c, keep[c]);
+    }
+    // (2) growth by the previous token
+    for (int j = tid; j < B; j += kThreads) l_lru[j] = g_lru[j];
+    if (tid == 0) l_misc[kLM] = static_cast<uint32_t>(g_pt[prev]);
+    __syncthreads();
+    const int32_t hslot = static_cast<int32_t>(l_misc[kLM]);
+    const bool bad = hslot >= B || hslot < -1;   // a corrupt page-table entry
+    if (hslot >= 0 && !bad)
+      for (int j = tid; j < B; j += kThreads)
+        if (l_lru[j] == hslot) l_misc[kLHits] = static_cast<uint32_t>(j);
+    __syncthreads();
+    if (bad) {
+      if (tid == 0) l_misc[kLErr] |= HISPARSE_ERR_RANGE;
+    } else {
+      const int jm = hslot >= 0 ? static_cast<int>(l_misc[kLHits]) : 0;
+      const int16_t moved = hslot >= 0 ? static_cast<int16_t>(hslot) : l_lru[0];
+      for (int j = tid; j < B; j += kThreads) g_lru[j] = j < B - 1 ? l_lru[j + (j >= jm)] : moved;
+      if (hslot < 0) {   // a miss into the least recent slot
+        const int v = moved;
+        if (tid == 0) {
+          const int32_t old = g_sp[v];
+          if (old >= 0) g_pt[old] = -1;
+          g_sp[v] = prev;
+          g_pt[prev] = v;
+          if (kRecordPlan) {
+            a.plan_pos[static_cast<int64_t>(r) * k] = prev;
+            a.plan_slot[static_cast<int64_t>(r) * k] = v;
+          }
+        }
+        if (a.io) {
+          uint4 *row = reinterpret_cast<uint4 *>(a.hot + static_cast<int64_t>(r) * a.hot_req_stride +
+                                                 static_cast<int64_t>(v) * a.hot_row_stride);
+          for (int c = tid; c < a.rec16; c += kThreads) st_v4(row + c, keep[c]);
+          for (int f = 0; f < a.nfl; ++f) {   // the shared-index layers' rows, inline
+            const ReplayTarget &T = a.fl[f];
+            const uint4 *src = reinterpret_cast<const uint4 *>(
+                T.src + static_cast<int64_t>(r) * T.src_req_stride +
+                static_cast<int64_t>(prev) * T.src_row_stride);
+            uint4 *dst = reinterpret_cast<uint4 *>(T.hot + static_cast<int64_t>(r) * T.hot_req_stride +
+                                                   static_cast<int64_t>(v) * T.hot_row_stride);
+            for (int c = tid; c < a.rec16; c += kThreads) st_v4(dst + c, ld_nc_v4(src + c));
+          }
+        }
+      }
+      if (tid == 0) {
+        a.miss_count[r] = hslot < 0 ? 1 : 0;
+        a.plan_count[r] = (kRecordPlan && hslot < 0) ? 1 : 0;
+      }
+    }
+  } else if (tid == 0) {
+    a.miss_count[r] = 0;
+    a.plan_count[r] = 0;
+  }
+  // (3) the lookup by position
+  const int32_t *g_res = a.res_blocks ? a.res_blocks + static_cast<int64_t>(r) * a.res_nblk : nullptr;
+  uint32_t err = 0;
+  for (int i = tid; i < k; i += kThreads) {
+    const int32_t p = sel_position<true>(a, r, i);
+    int32_t v = -1;
+    if (p != -1) {
+      if (p < -1 || p >= P) {
+        err |= HISPARSE_ERR_RANGE;
+      } else {
+        const int32_t e = (g_res && p / a.res_tok < a.res_nblk) ? g_res[p / a.res_tok] : -1;
+        if (e < -1) {
+          err |= HISPARSE_ERR_RANGE;
+        } else if (e >= 0) {
+          const int64_t row = static_cast<int64_t>(e) * a.res_tok + p % a.res_tok;
+          if (static_cast<int64_t>(B) + 1 + row > INT32_MAX) err |= HISPARSE_ERR_RANGE;
+          else v = static_cast<int32_t>(B + 1 + row);
+        } else if (p == newest) {
+          v = B;
+        } else if (p >= seq_len) {
+          err |= HISPARSE_ERR_RANGE;
+        } else {
+          v = p;   // the slot numbered like the position
+        }
+      }
+    }
+    l_out[i] = v;
+  }
+  if (err) atomicOr(&l_misc[kLErr], err);
+  __syncthreads();
+  const uint32_t uerr = l_misc[kLErr];
+  int32_t *g_out = a.out + static_cast<int64_t>(r) * k;
+  for (int i = tid; i < k; i += kThreads) g_out[i] = uerr ? -1 : l_out[i];
+  if (tid == 0) {
+    a.unit_err[r] = static_cast<int32_t>(uerr);
+    if (uerr) atomicOr(a.status, uerr);
+  }
+}
+
 template <bool kRecordPlan, bool kExt>
 __global__ void __launch_bounds__(kThreads, 1) resolve_pt_kernel(const PtArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
@@ -1439,8 +1579,13 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_pt_kernel(const PtArgs a)
   }
   const int32_t newest = a.newest ? a.newest[r] : -1;
   const int32_t prev = a.prev_pos ? a.prev_pos[r] : -1;
+  const int32_t seq_len = (kExt && a.seq_lens) ? a.seq_lens[r] : INT32_MAX;
   const int nreq = a.num_reqs ? min(*a.num_reqs, a.R) : a.R;
   if (r >= nreq) return;  // graph padding: every CTA of the cluster leaves
+  if (kExt && seq_len <= a.B) {  // a short request: the leader alone, no cluster barrier
+    if (leader) pt_short_path<kRecordPlan>(a, r, prev, newest, seq_len, smem, L);
+    return;
+  }
   // the previous token's record, when filled from row B, is not read from the host
   const int32_t skip_pos = (a.prev_from_row && prev >= 0) ? prev : -2;
 
@@ -1548,32 +1693,27 @@ __global__ void __launch_bounds__(128) writeback_kernel(const WritebackArgs a) {
 // Plan replay for a shared-index layer ([DD] §3.6, §5.6).  The plan's records
 // (every request's, back to back) are split evenly over a small grid; a CTA
 // resolves a batch of its records to source and destination rows once, into
-// shared memory, orders the batch by source address (so that records of
-// nearby host pages are read together, as RESOLVE orders each slice's
-// fetches), then streams the batch's 16-byte chunks with kReplayDepth host
-// loads in flight per thread.  Nothing on the load path waits on a global
-// read of the plan.
+// shared memory, then streams the batch's 16-byte chunks with kReplayDepth
+// host loads in flight per thread.  Nothing on the load path waits on a global
+// read of the plan.  (Reading each batch in source-address order was measured
+// to change nothing: a plan record's rows are on distinct 64 KB host pages in
+// any order.)
 // ---------------------------------------------------------------------------
 constexpr int kReplayThreads = 512;
-constexpr int kReplayBatch = 512;  // plan records resolved to rows per round (== threads)
+constexpr int kReplayBatch = 512;  // plan records resolved to rows per round
 constexpr int kReplayDepth = 8;    // 16-byte host loads in flight per thread
-static_assert(kReplayBatch == kReplayThreads, "one batch entry per thread in the ordering");
 
 __host__ __device__ inline int replay_pref_bytes(int R) { return ((R + 1) * 4 + 15) & ~15; }
 __host__ __device__ inline size_t replay_smem_bytes(int R) {
-  // prefix [R + 1], then source and destination rows of a batch in resolve
-  // order, then the same two in source-address order
-  return static_cast<size_t>(replay_pref_bytes(R)) + 4 * sizeof(char *) * kReplayBatch;
+  // prefix [R + 1], then source and destination rows of a batch
+  return static_cast<size_t>(replay_pref_bytes(R)) + 2 * sizeof(char *) * kReplayBatch;
 }
 
 __global__ void __launch_bounds__(kReplayThreads) replay_kernel(const ReplayArgs a) {
   extern __shared__ __align__(16) unsigned char rsm[];
   int32_t *s_pref = reinterpret_cast<int32_t *>(rsm);  // [R + 1] exclusive prefix of plan counts
-  unsigned char *rows = rsm + replay_pref_bytes(a.R);  // four arrays of kReplayBatch pointers
-  const char **s_src0 = reinterpret_cast<const char **>(rows);
-  char **s_dst0 = reinterpret_cast<char **>(rows + sizeof(char *) * kReplayBatch);
-  const char **s_src = reinterpret_cast<const char **>(rows + 2 * sizeof(char *) * kReplayBatch);
-  char **s_dst = reinterpret_cast<char **>(rows + 3 * sizeof(char *) * kReplayBatch);
+  const char **s_src = reinterpret_cast<const char **>(rsm + replay_pref_bytes(a.R));  // [kReplayBatch]
+  char **s_dst = reinterpret_cast<char **>(rsm + replay_pref_bytes(a.R) + sizeof(char *) * kReplayBatch);
   const int tid = threadIdx.x;
   const int nreq = a.num_reqs ? min(*a.num_reqs, a.R) : a.R;
   if (tid < 32) {
@@ -1611,23 +1751,10 @@ __global__ void __launch_bounds__(kReplayThreads) replay_kernel(const ReplayArgs
       }
       const int64_t pk = static_cast<int64_t>(lo) * a.k + (m - s_pref[lo]);
       const ReplayTarget &T = a.f[f];
-      s_src0[i] = T.src + static_cast<int64_t>(lo) * T.src_req_stride +
-                  static_cast<int64_t>(a.plan_pos[pk]) * T.src_row_stride;
-      s_dst0[i] = T.hot + static_cast<int64_t>(lo) * T.hot_req_stride +
-                  static_cast<int64_t>(a.plan_slot[pk]) * T.hot_row_stride;
-    }
-    __syncthreads();
-    // entry i's rank among the batch by source address (ties by index: a
-    // permutation even if two entries read the same row)
-    if (tid < nb) {
-      const uintptr_t key = reinterpret_cast<uintptr_t>(s_src0[tid]);
-      int rnk = 0;
-      for (int x = 0; x < nb; ++x) {
-        const uintptr_t kx = reinterpret_cast<uintptr_t>(s_src0[x]);
-        rnk += kx < key || (kx == key && x < tid);
-      }
-      s_src[rnk] = s_src0[tid];
-      s_dst[rnk] = s_dst0[tid];
+      s_src[i] = T.src + static_cast<int64_t>(lo) * T.src_req_stride +
+                 static_cast<int64_t>(a.plan_pos[pk]) * T.src_row_stride;
+      s_dst[i] = T.hot + static_cast<int64_t>(lo) * T.hot_req_stride +
+                 static_cast<int64_t>(a.plan_slot[pk]) * T.hot_row_stride;
     }
     __syncthreads();
     const uint32_t n = static_cast<uint32_t>(nb) * rec16;
@@ -1781,6 +1908,7 @@ struct hisparse_handle {
   int64_t P;
   int32_t cs, cap_log2, replay_ctas, sm_count, device, lookup, ks;
   uint32_t smem;
+  float l2_hit_ratio = 0.f;   // > 0: RESOLVE launches keep the page table persisting in L2
   std::vector<int32_t> anchor_of;
   std::vector<LayerDev> layers;
   std::vector<int32_t> bucket_shift, nbuckets;  // per layer: fetch-order buckets
@@ -2288,7 +2416,9 @@ int hisparse_resolve_ex(hisparse_handle *h, int32_t layer, const int32_t *d_sel,
   const int32_t *d_res_blocks = opt->d_res_blocks;
   const int32_t res_max_blocks = opt->res_max_blocks, res_block_tokens = opt->res_block_tokens;
   const int32_t sel_bt = opt->sel_block_tokens < 1 ? 1 : opt->sel_block_tokens;
+  const int32_t *d_seq_lens = opt->d_seq_lens;
   if (layer_ok(h, layer)) return HISPARSE_EINVAL;
+  if (d_seq_lens && h->lookup == HISPARSE_LOOKUP_HASH) return HISPARSE_EINVAL;
   if (d_res_blocks && (res_max_blocks < 1 || res_block_tokens < 1 ||
                        h->lookup == HISPARSE_LOOKUP_HASH))
     return HISPARSE_EINVAL;
@@ -2324,13 +2454,21 @@ int hisparse_resolve_ex(hisparse_handle *h, int32_t layer, const int32_t *d_sel,
   lc.blockDim = dim3(kThreads);
   lc.dynamicSmemBytes = h->smem;
   lc.stream = static_cast<cudaStream_t>(stream);
-  cudaLaunchAttribute at[2];
+  cudaLaunchAttribute at[3];
   at[0].id = cudaLaunchAttributeClusterDimension;
   at[0].val.clusterDim.x = h->cs;
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
   at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[1].val.programmaticStreamSerializationAllowed = 1;
+  // hisparse_set_l2_persisting: the layer's page table, read by one gather
+  // per selection, is marked persisting so it survives in L2 between steps
+  at[2].id = cudaLaunchAttributeAccessPolicyWindow;
+  at[2].val.accessPolicyWindow.base_ptr = m.page_table;
+  at[2].val.accessPolicyWindow.num_bytes = static_cast<size_t>(h->R) * h->P * sizeof(int32_t);
+  at[2].val.accessPolicyWindow.hitRatio = h->l2_hit_ratio;
+  at[2].val.accessPolicyWindow.hitProp = cudaAccessPropertyPersisting;
+  at[2].val.accessPolicyWindow.missProp = cudaAccessPropertyStreaming;
   lc.attrs = at;
   lc.numAttrs = 1;
   cudaError_t e;
@@ -2376,6 +2514,7 @@ int hisparse_resolve_ex(hisparse_handle *h, int32_t layer, const int32_t *d_sel,
     a.res_tok = d_res_blocks ? res_block_tokens : 1;
     a.sel_bt = sel_bt;
     a.union_mode = (flags & HISPARSE_UNION) ? 1 : 0;
+    a.seq_lens = d_seq_lens;
     a.P = h->P;
     a.sel = d_sel; a.num_reqs = d_num_reqs; a.newest = d_newest; a.out = d_out;
     a.slot_pos = m.slot_pos; a.lru = m.lru; a.page_table = m.page_table;
@@ -2394,8 +2533,9 @@ int hisparse_resolve_ex(hisparse_handle *h, int32_t layer, const int32_t *d_sel,
       a.fl[i].hot_req_stride = Lf.hot_req_stride;
       a.fl[i].hot_row_stride = Lf.hot_row_stride;
     }
-    lc.numAttrs = 2;  // cluster shape + programmatic dependent launch
-    if (d_res_blocks || sel_bt > 1 || a.union_mode)  // the extended instantiation
+    lc.numAttrs = h->l2_hit_ratio > 0.f ? 3 : 2;  // cluster shape + programmatic dependent
+                                                  // launch (+ the L2 window)
+    if (d_res_blocks || sel_bt > 1 || a.union_mode || d_seq_lens)  // the extended instantiation
       e = plan ? cudaLaunchKernelEx(&lc, resolve_pt_kernel<true, true>, a)
                : cudaLaunchKernelEx(&lc, resolve_pt_kernel<false, true>, a);
     else
@@ -2571,6 +2711,29 @@ int hisparse_export_plan(hisparse_handle *h, int32_t layer, int32_t *count, int3
   HS_CUDA(cudaMemcpy(count, m.plan_count, 4 * h->R, cudaMemcpyDeviceToHost));
   HS_CUDA(cudaMemcpy(pos, m.plan_pos, 4 * Rk, cudaMemcpyDeviceToHost));
   HS_CUDA(cudaMemcpy(slot, m.plan_slot, 4 * Rk, cudaMemcpyDeviceToHost));
+  return HISPARSE_OK;
+}
+
+int hisparse_set_l2_persisting(hisparse_handle *h, int64_t bytes) {
+  if (!h || bytes < 0) return HISPARSE_EINVAL;
+  if (bytes == 0) {
+    h->l2_hit_ratio = 0.f;
+    HS_CUDA(cudaCtxResetPersistingL2Cache());
+    return HISPARSE_OK;
+  }
+  int max_persist = 0, max_window = 0;
+  HS_CUDA(cudaDeviceGetAttribute(&max_persist, cudaDevAttrMaxPersistingL2CacheSize, h->device));
+  HS_CUDA(cudaDeviceGetAttribute(&max_window, cudaDevAttrMaxAccessPolicyWindowSize, h->device));
+  const int64_t table = static_cast<int64_t>(h->R) * h->P * static_cast<int64_t>(sizeof(int32_t));
+  if (max_persist <= 0 || table > max_window) return HISPARSE_EBOUND;
+  int64_t tables = 0;
+  for (int l = 0; l < h->L; ++l)
+    if (h->anchor_of[l] == -1) tables += table;
+  const int64_t aside = std::min<int64_t>(bytes, max_persist);
+  HS_CUDA(cudaDeviceSetLimit(cudaLimitPersistingL2CacheSize, static_cast<size_t>(aside)));
+  // the share of each window's lines marked persisting, so that all layers'
+  // persisting lines fit the set-aside together
+  h->l2_hit_ratio = static_cast<float>(std::min<double>(1.0, double(aside) / double(tables)));
   return HISPARSE_OK;
 }
 

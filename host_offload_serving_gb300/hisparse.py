@@ -58,6 +58,7 @@ SIGNATURES = [
     ("hisparse_import_state", _i32, [_vp, _i32, _vp, _vp, _vp, _vp]),
     ("hisparse_export_plan", _i32, [_vp, _i32, _vp, _vp, _vp]),
     ("hisparse_reset", _i32, [_vp, _i32, _vp]),
+    ("hisparse_set_l2_persisting", _i32, [_vp, _i64]),
     ("hisparse_get_info", _i32, [_vp, ctypes.POINTER(Info)]),
     ("hisparse_host_alloc", _i32, [ctypes.c_size_t, ctypes.POINTER(_vp)]),
     ("hisparse_host_free", _i32, [_vp]),
@@ -130,7 +131,8 @@ class ResolveOptions(ctypes.Structure):
     """hisparse_resolve_options."""
     _fields_ = [("d_prev_pos", ctypes.c_void_p), ("d_new_rows", ctypes.c_void_p),
                 ("d_res_blocks", ctypes.c_void_p), ("res_max_blocks", ctypes.c_int32),
-                ("res_block_tokens", ctypes.c_int32), ("sel_block_tokens", ctypes.c_int32)]
+                ("res_block_tokens", ctypes.c_int32), ("sel_block_tokens", ctypes.c_int32),
+                ("d_seq_lens", ctypes.c_void_p)]
 
 
 def hisparse_resolve_ex(h, layer, d_sel, d_num_reqs, d_newest, opt, d_out, flags, stream):
@@ -183,6 +185,10 @@ def hisparse_export_plan(h, layer, count, pos, slot):
 
 def hisparse_reset(h, layer, stream):
     return load().hisparse_reset(h, layer, stream)
+
+
+def hisparse_set_l2_persisting(h, nbytes):
+    return load().hisparse_set_l2_persisting(h, nbytes)
 
 
 def hisparse_get_info(h):

@@ -122,12 +122,13 @@ class HiSparse:
 
     def resolve_ex(self, layer, sel, out, num_reqs=None, newest=None, prev_pos=None,
                    new_rows=None, res_blocks=None, res_block_tokens=0, sel_block_tokens=1,
-                   flags=0, stream=None):
+                   flags=0, stream=None, seq_lens=None):
         """The general RESOLVE (``hisparse_resolve_ex``): fused write-through,
-        resident tier and block-id selections, each optional."""
+        resident tier, block-id selections and short requests (``seq_lens``,
+        device int32 [R]), each optional."""
         o = H.ResolveOptions(_ptr(prev_pos), _ptr(new_rows), _ptr(res_blocks),
                              int(res_blocks.shape[1]) if res_blocks is not None else 0,
-                             int(res_block_tokens), int(sel_block_tokens))
+                             int(res_block_tokens), int(sel_block_tokens), _ptr(seq_lens))
         H.check(H.hisparse_resolve_ex(self.h, layer, _ptr(sel), _ptr(num_reqs), _ptr(newest), o,
                                       _ptr(out), flags, _stream(stream)), "hisparse_resolve_ex")
 
@@ -185,6 +186,11 @@ class HiSparse:
         H.check(H.hisparse_export_plan(self.h, layer, c.ctypes.data, p.ctypes.data, s.ctypes.data),
                 "hisparse_export_plan")
         return c, p, s
+
+    def set_l2_persisting(self, nbytes):
+        """Keep the RESOLVE layers' page tables in L2 (``hisparse_set_l2_persisting``;
+        0 turns it off)."""
+        H.check(H.hisparse_set_l2_persisting(self.h, int(nbytes)), "hisparse_set_l2_persisting")
 
     def info(self):
         rc, info = H.hisparse_get_info(self.h)
@@ -314,8 +320,11 @@ class DecodeStep:
     def _no_pos(self):
         return self._nopos
 
-    def issue(self, sel, out, newest=None, wb_pos=None, new_rows=None):
-        """Enqueue one step on the instance's streams (returns immediately)."""
+    def issue(self, sel, out, newest=None, wb_pos=None, new_rows=None, seq_lens=None):
+        """Enqueue one step on the instance's streams (returns immediately).
+        ``seq_lens`` (device int32 [R], optional): each request's positions so
+        far; requests whose length fits the buffer take the short path
+        (``hisparse_resolve_options.d_seq_lens``)."""
         hs = self.hs
         cur = torch.cuda.current_stream()
         self.ev_step_start.record(cur)
@@ -340,7 +349,7 @@ class DecodeStep:
                                      new_rows=new_rows[fl] if new_rows is not None else None)
             else:
                 f = self.flags | (H.RECORD_PLAN if followers else 0)
-            if self.resident is not None or self.sel_block_tokens > 1:
+            if self.resident is not None or self.sel_block_tokens > 1 or seq_lens is not None:
                 fused = through and self.fused
                 res = self.resident
                 hs.resolve_ex(anchor, sel[gi], out[gi], self.num_reqs, newest,
@@ -348,7 +357,7 @@ class DecodeStep:
                               new_rows[anchor] if (fused and new_rows is not None) else None,
                               res[0] if res is not None else None,
                               res[1] if res is not None else 0, self.sel_block_tokens, f,
-                              stream=self.compute)
+                              stream=self.compute, seq_lens=seq_lens)
             elif through and self.fused:
                 hs.resolve_step(anchor, sel[gi], out[gi], self.num_reqs, newest, pos[anchor],
                                 new_rows[anchor] if new_rows is not None else None, f,

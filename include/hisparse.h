@@ -231,6 +231,29 @@ typedef struct {
    * HISPARSE_ERR_RANGE.  top_k must be a multiple; page-table lookup only.
    * 0 or 1: d_sel holds positions. */
   int32_t sel_block_tokens;
+  /* Short requests ([DD] §5.4 short-sequence fast path and on-demand buffer
+   * growth; §5.5 the swap-in kernel's early return): device int32 [R], the
+   * number of positions of each request so far, the newest included; NULL:
+   * every request takes the general path.  A request with d_seq_lens[r] <= B
+   * skips the LRU lookup.  First its buffer grows by its previous token: when
+   * d_prev_pos[r] >= 0 (the fused write-through), that token is resolved as a
+   * one-entry selection -- a miss takes the least recent slot, filled from
+   * the row it was just written back from (and, with HISPARSE_WITH_SHARED,
+   * the shared-index layers' rows), is mapped and recorded in the plan; a hit
+   * moves its slot to the recent end; without a previous token the miss
+   * count and plan count are 0.  Then each selection outputs -1 for padding,
+   * its resident row when d_res_blocks has one, B for d_newest[r], else the
+   * slot numbered like the position; a position outside [0, seq_len) or
+   * [0, P) fails the request's output (all -1, HISPARSE_ERR_RANGE; the
+   * growth stays); repeats are not errors.  This is exact when slot s holds
+   * position s for every position before the newest: a request admitted
+   * with hisparse_admit preloading its host_len positions and decoded with
+   * the fused write-through since.  The pages' early return then equals the
+   * general resolve's output (all hits) without its LRU work.  Longer
+   * requests in the same launch take the general path; a request that
+   * outgrows B takes it from its next step on, its un-grown slot being the
+   * least recent.  Page-table lookup only. */
+  const int32_t *d_seq_lens;
 } hisparse_resolve_options;
 
 /* The general RESOLVE: hisparse_resolve with the options above (opt may be
@@ -285,9 +308,12 @@ int hisparse_admit(hisparse_handle *h, int32_t layer, const int32_t *d_reqs, int
 
 /* Write-through of the newest row ([DD] §3.4 step 4, §5.4 eager backup):
  * for r < *d_num_reqs with d_pos[r] >= 0, copy hot row B of (layer, r) to
- * host row d_pos[r] of (layer, r); then, if d_new_rows is not NULL, place the
- * new token's KV (d_new_rows, device, [R][record_bytes] per layer, 16-byte
- * aligned) in row B -- the old row is always read before it is replaced.
+ * host row d_pos[r] of (layer, r) (and of its HBM mirror, if it has one);
+ * then, if d_new_rows is not NULL, place the new token's KV (d_new_rows,
+ * device, [R][record_bytes] per layer, 16-byte aligned) in row B -- the old
+ * row is always read before it is replaced.  d_new_rows is this library's
+ * addition to the pages' write-back: the caller's new-token KV enters row B
+ * in the same launch ([DD] §5.4 writes it to the newest slot separately).
  * layer == -1 does every layer in one launch (d_pos is then [L][R] and
  * d_new_rows [L][R][record_bytes]).  Positions >= P set HISPARSE_ERR_RANGE in
  * the status word and are not written back.  Make every resolve that may
@@ -313,7 +339,8 @@ int hisparse_writeback(hisparse_handle *h, int32_t layer, const int32_t *d_pos,
 int hisparse_prefetch_plan(hisparse_handle *h, int32_t anchor_layer, int32_t follower_layer,
                            const int32_t *d_num_reqs, void *stream);
 
-/* Copy `bytes` (a multiple of 16) from src to dst with SM threads, on
+/* (Library call, not a step of the pages' method.)
+ * Copy `bytes` (a multiple of 16) from src to dst with SM threads, on
  * `stream`, after the stream's previous work (graph-capturable, no
  * synchronisation).  Either side may be device memory or pinned host memory
  * mapped for the device (hisparse_host_alloc, cudaHostAlloc); both 16-byte
@@ -323,25 +350,31 @@ int hisparse_prefetch_plan(hisparse_handle *h, int32_t anchor_layer, int32_t fol
  * hundred KB.  Errors: EINVAL (NULL, misaligned, bad size), ECUDA. */
 int hisparse_copy(void *dst, const void *src, int64_t bytes, void *stream);
 
-/* Copy the per-request miss counts of one anchor layer's last resolve
+/* (Library call, not a step of the pages' method.)
+ * Copy the per-request miss counts of one anchor layer's last resolve
  * (int32 [R]) to device memory d_dst, asynchronously on `stream` (no
  * synchronisation; graph-capturable).  Errors: EINVAL, EROLE, ECUDA. */
 int hisparse_copy_miss_counts(hisparse_handle *h, int32_t layer, int32_t *d_dst, void *stream);
 
-/* Read and clear the sticky status word (bit-OR of HISPARSE_ERR_*), and copy
+/* (Library call, not a step of the pages' method: how device-detected input
+ * errors reach the host.)
+ * Read and clear the sticky status word (bit-OR of HISPARSE_ERR_*), and copy
  * the per-unit codes of the last resolve ([L][R] int32, zero for followers)
  * if unit_err_out is not NULL.  Synchronises the device: not for use inside
  * a graph capture or a timed region. */
 int hisparse_get_status(hisparse_handle *h, uint32_t *flags_out, int32_t *unit_err_out);
 
-/* Copy one anchor layer's state to host arrays (any may be NULL):
+/* (Library call, not a step of the pages' method: checkpoint and test access
+ * to the metadata of [DD] §5.2.)
+ * Copy one anchor layer's state to host arrays (any may be NULL):
  * slot_pos [R][B] int32 (-1 empty), lru [R][B] int16 (least recent first),
  * page_table [R][P] int32 (slot, or -1 = host only), miss_counts [R] int32
  * (misses of the last resolve).  Synchronises.  Errors: EINVAL, EROLE, ECUDA. */
 int hisparse_export_state(hisparse_handle *h, int32_t layer, int32_t *slot_pos, int16_t *lru,
                           int32_t *page_table, int32_t *miss_counts);
 
-/* Replace one anchor layer's state (checkpoint / test set-up): the arrays of
+/* (Library call, not a step of the pages' method.)
+ * Replace one anchor layer's state (checkpoint / test set-up): the arrays of
  * hisparse_export_state.  slot_pos, lru and page_table are required;
  * miss_counts may be NULL (the layer's miss counts are then left as they
  * are).  The arrays are validated first: every slot_pos in [-1, P) with no
@@ -353,7 +386,9 @@ int hisparse_import_state(hisparse_handle *h, int32_t layer, const int32_t *slot
                           const int16_t *lru, const int32_t *page_table,
                           const int32_t *miss_counts);
 
-/* Copy one anchor layer's last miss plan to host arrays: count [R],
+/* (Library call, not a step of the pages' method: host access to the plan of
+ * [DD] §5.5.)
+ * Copy one anchor layer's last miss plan to host arrays: count [R],
  * pos [R][k] int32, slot [R][k] int32 (only the first count[r] entries of a
  * row are meaningful).  Entries are the (position, slot) pairs fetched by the
  * last resolve: in list order with HISPARSE_LOOKUP_PAGE_TABLE, in ascending
@@ -364,13 +399,35 @@ int hisparse_export_plan(hisparse_handle *h, int32_t layer, int32_t *count, int3
 
 /* Reset one anchor layer (or all layers with layer == -1) to the admission
  * state: slots empty, LRU 0..B-1, page table all host-only ([DD] §5.4
- * request release).  Asynchronous on `stream`.  Errors: EINVAL, EROLE, ECUDA. */
+ * request release).  Asynchronous on `stream` (the stream argument is this
+ * library's: a reset is ordered with the launches around it, and can be
+ * captured in a graph).  Errors: EINVAL, EROLE, ECUDA. */
 int hisparse_reset(hisparse_handle *h, int32_t layer, void *stream);
 
-/* Fill `out` with facts about the instance. */
+/* Keep the page tables of the layers that run RESOLVE in L2 between decode
+ * steps (build-own call; the pages keep their slot lookup in shared memory
+ * and have no counterpart).  RESOLVE with HISPARSE_LOOKUP_PAGE_TABLE gathers
+ * one page-table entry per selection right after reading the selections;
+ * when the rest of a decode step has evicted that table from L2 the gather
+ * costs a DRAM round trip on the critical path.  With bytes > 0 this sets the
+ * calling process's persisting-L2 set-aside (cudaLimitPersistingL2CacheSize,
+ * a limit of this CUDA context that ends with it) to min(bytes, the device
+ * maximum), and every later page-table RESOLVE launch carries an
+ * access-policy window over its layer's page table whose hit ratio lets the
+ * tables of all RESOLVE layers share the set-aside.  bytes == 0 turns it off
+ * and returns persisting lines to normal (cudaCtxResetPersistingL2Cache).
+ * Results are unchanged either way.  Not during graph capture: launches
+ * captured earlier keep the setting they were captured with.
+ * Errors: EINVAL (bytes < 0), EBOUND (no persisting L2 on the device, or one
+ * layer's table larger than an access-policy window), ECUDA. */
+int hisparse_set_l2_persisting(hisparse_handle *h, int64_t bytes);
+
+/* (Library call.)  Fill `out` with facts about the instance. */
 int hisparse_get_info(const hisparse_handle *h, hisparse_info *out);
 
-/* Pinned, device-mapped, portable host memory for host pools: the PINNED kind
+/* (Library calls, not steps of the pages' method: the pages assume a pinned
+ * host pool, [DD] §3.2; these allocate one without rounding.)
+ * Pinned, device-mapped, portable host memory for host pools: the PINNED kind
  * below (cudaHostAlloc; contents unspecified).  Free with hisparse_host_free.
  * Errors: EINVAL, ENOMEM. */
 int hisparse_host_alloc(size_t bytes, void **out);
@@ -403,7 +460,8 @@ int hisparse_host_alloc_kind(size_t bytes, int32_t kind, void **out);
  * Errors: EINVAL. */
 int hisparse_host_hugepage_bytes(const void *p, size_t bytes, size_t *huge_out);
 
-/* The cudaError_t of the last failed CUDA call made by this thread through
+/* (Library calls.)
+ * The cudaError_t of the last failed CUDA call made by this thread through
  * the library (0 if none), and a static message for any return code. */
 int hisparse_last_cuda_error(void);
 const char *hisparse_strerror(int code);

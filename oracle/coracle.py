@@ -60,6 +60,14 @@ def _load():
         lib.hso_resolve_layer_res.argtypes = [P, vp, vp, vp, ctypes.c_int32, ctypes.c_int32,
                                               ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, vp]
         lib.hso_resolve_layer_res.restype = ctypes.c_int32
+        lib.hso_resolve_unit_res.argtypes = [P, ctypes.c_int32, vp, ctypes.c_int32,
+                                             ctypes.c_int32, vp, ctypes.c_int32, ctypes.c_int32,
+                                             ctypes.c_int32, vp]
+        lib.hso_resolve_unit_res.restype = ctypes.c_int32
+        lib.hso_short_lookup_unit.argtypes = [P, ctypes.c_int32, vp, ctypes.c_int32,
+                                              ctypes.c_int32, vp, ctypes.c_int32, ctypes.c_int32,
+                                              vp]
+        lib.hso_short_lookup_unit.restype = ctypes.c_int32
         lib.hso_set_newest_rows.argtypes = [P, vp, ctypes.c_int32]
         lib.hso_writeback.argtypes = [P, vp, ctypes.c_int32]
         lib.hso_writeback.restype = ctypes.c_int32
@@ -171,6 +179,51 @@ class OracleLayer:
                                                 0 if rb is None else rb.shape[1], int(res_tok),
                                                 int(bool(union)), nr, int(bool(io)), _p(out))
         return out, e
+
+    def resolve_with_seq_lens(self, sel, newest, prev, seq_lens, num_reqs=None, io=True,
+                              res_blocks=None, res_tok=1, union=False):
+        """One layer-step where each request carries its sequence length
+        (reading R17 of oracle/tiny.py): a request with seq_len <= B grows its
+        buffer by its previous token (a one-entry resolve of ``prev[r]`` when
+        it is >= 0, whose record the write-back has just stored; otherwise
+        its miss count and plan are 0) and then looks its selections up by
+        position; a longer one is resolved as usual.  The write-back itself
+        (``writeback``) comes first, as for any step.  Returns (out, err)."""
+        sel = np.ascontiguousarray(sel, dtype=np.int32)
+        nr = self.R if num_reqs is None else num_reqs
+        out = np.full((self.R, self.k), -1, np.int32)
+        rb = None if res_blocks is None else np.ascontiguousarray(res_blocks, dtype=np.int32)
+        nblk = 0 if rb is None else rb.shape[1]
+        err = 0
+        grow = np.full(self.k, -1, np.int32)
+        scratch = np.empty(self.k, np.int32)
+        for r in range(nr):
+            nw = -1 if newest is None else int(newest[r])
+            blk = None if rb is None else rb[r]
+            if int(seq_lens[r]) <= self.B:
+                if prev is not None and int(prev[r]) >= 0:
+                    grow[0] = int(prev[r])
+                    e = self._lib.hso_resolve_unit_res(ctypes.byref(self._s), r, _p(grow), -1,
+                                                       int(bool(io)), None, 0, 1, 0,
+                                                       _p(scratch))
+                    assert e == 0, "the previous token is a valid one-entry selection"
+                else:
+                    self.miss_count[r] = 0
+                    self.plan_count[r] = 0
+                row = np.ascontiguousarray(sel[r])
+                o = np.empty(self.k, np.int32)
+                err |= self._lib.hso_short_lookup_unit(ctypes.byref(self._s), r, _p(row), nw,
+                                                       int(seq_lens[r]), _p(blk), nblk,
+                                                       int(res_tok), _p(o))
+                out[r] = o
+            else:
+                row = np.ascontiguousarray(sel[r])
+                o = np.empty(self.k, np.int32)
+                err |= self._lib.hso_resolve_unit_res(ctypes.byref(self._s), r, _p(row), nw,
+                                                      int(bool(io)), _p(blk), nblk, int(res_tok),
+                                                      int(bool(union)), _p(o))
+                out[r] = o
+        return out, err
 
     def set_newest_rows(self, rows, num_reqs=None):
         rows = np.ascontiguousarray(rows, dtype=np.uint8)

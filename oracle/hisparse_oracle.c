@@ -236,6 +236,41 @@ int32_t hso_resolve_layer(hso_layer *L, const int32_t *sel, const int32_t *newes
   return hso_resolve_layer_res(L, sel, newest, NULL, 0, 1, 0, num_reqs, io, out);
 }
 
+/* Short-sequence lookup (gentlecold.top §5.4 and §5.5: when a request's
+   seq_len <= B its tokens sit in the buffer in order, and the kernel returns
+   each selection's slot by position, with no host IO and no LRU work).
+   Reading R17: for request r with seq_len <= B, a selection outputs -1 for
+   padding, its resident row first when the resident table has one (as in
+   the three-tier resolve), B for the newest token, else the slot numbered
+   like the position.  A position outside [0, seq_len) or [0, P), a newest
+   position outside [-1, P) or an invalid resident entry fails the request
+   (out all -1); repeats are not checked (nothing is allocated).  Nothing of
+   the unit's state changes here; the growth of the buffer by the previous
+   token is a one-entry resolve the caller runs before (see tiny.py).
+   Returns 0 or a bit-OR of HSO_ERR_*; sets unit_err[r]. */
+int32_t hso_short_lookup_unit(hso_layer *L, int32_t r, const int32_t *sel, int32_t newest,
+                              int32_t seq_len, const int32_t *blk, int32_t nblk, int32_t tok,
+                              int32_t *out) {
+  int32_t err = 0, i;
+  int64_t rr;
+  if (newest < -1 || (int64_t)newest >= L->P) err |= HSO_ERR_RANGE;
+  for (i = 0; i < L->k; i++) {
+    int32_t p = sel[i];
+    if (p == -1) { out[i] = -1; continue; }
+    if (p < -1 || (int64_t)p >= L->P) { err |= HSO_ERR_RANGE; continue; }
+    rr = resident_row(L, blk, nblk, tok, p);
+    if (rr == -2) { err |= HSO_ERR_RANGE; continue; }
+    if (rr >= 0) { out[i] = (int32_t)(L->B + 1 + rr); continue; }
+    if (newest >= 0 && p == newest) { out[i] = L->B; continue; }
+    if (p >= seq_len) { err |= HSO_ERR_RANGE; continue; }
+    out[i] = p;
+  }
+  if (err)
+    for (i = 0; i < L->k; i++) out[i] = -1;
+  L->unit_err[r] = err;
+  return err;
+}
+
 /* The caller writes the new token's KV into row B of each request. */
 void hso_set_newest_rows(hso_layer *L, const uint8_t *rows /* [R][rec] */, int32_t num_reqs) {
   int32_t r;

@@ -54,6 +54,29 @@ union mode:
       not an error.  Misses are the first references, in list order; the
       miss count and the plan count each missed position once.
 
+Short requests (gentlecold.top §5.4: when seq_len <= B every token of the
+request sits in the buffer in order and the kernel returns slots by position,
+with no host IO; the device buffer grows on demand; §5.5: the swap-in
+kernel's fast path returns before any LRU work; §5.3: a short request is
+admitted with all its tokens preloaded):
+  R17 a request whose seq_len (its positions so far, the newest included) is
+      at most B takes the short path.  First its buffer grows by the
+      previous token: when the step writes a previous token back
+      (``prev >= 0``), that token is resolved as a one-entry selection -- a
+      miss that takes the least recent slot, or a hit that moves its slot to
+      the recent end -- with its miss count and plan (so shared-index layers
+      follow); with no previous token the miss count and plan are 0.  Then
+      each selection outputs -1 for padding, its resident row when the
+      resident table has one, B for the newest token, else the slot numbered
+      like its position.  A position outside [0, seq_len), a newest position
+      outside [-1, P) or an invalid resident entry fails the lookup (output
+      all -1, error code set; the growth has happened).  Repeats are not
+      errors: nothing is allocated.  For a request admitted with its first n
+      positions preloaded and grown by one token per step since, the least
+      recent slot is always the next empty one, so slot s keeps position s
+      and the outputs equal those of the general resolve, all hits, without
+      its LRU work.  Longer requests are resolved as usual.
+
 See ``tests/test_oracle_pins.py`` for what pins each of these.
 
 [P1] = gentlecold.top, "HiSparse 深度解析：论文、SGLang 实现与 vLLM Hybrid
@@ -186,6 +209,57 @@ class Unit:
         self.lru = ev[M:] + ev[:M] + sorted(hit_slots)
         self.miss_count = M
         return out, plan, 0
+
+    # ------------------------------------------------------------------ #
+    def resolve_short(self, sel, newest, seq_len, prev=-1, res_blocks=None, res_tok=1):
+        """Short-request step (reading R17; caller checks seq_len <= B): grow
+        by ``prev`` (when >= 0; the host must already hold its record), then
+        look the selections up by position.  Returns ``(out, plan, err)``;
+        ``plan`` is the growth's."""
+        B, P = self.B, self.P
+        plan = []
+        if prev >= 0:
+            _, plan, e = self.resolve([prev])
+            assert e == 0, "the previous token must be a position in [0, P)"
+        else:
+            self.miss_count = 0
+        err = 0
+        if newest < -1 or newest >= P:
+            err |= ERR_RANGE
+        out = []
+        for p in sel:
+            if p == -1:
+                out.append(-1)
+                continue
+            if p < -1 or p >= P:
+                err |= ERR_RANGE
+                out.append(-1)
+                continue
+            row = -1
+            if res_blocks is not None and p // res_tok < len(res_blocks):
+                e = res_blocks[p // res_tok]
+                if e < -1:
+                    err |= ERR_RANGE
+                    out.append(-1)
+                    continue
+                if e >= 0:
+                    row = e * res_tok + p % res_tok
+                    if B + 1 + row > INT32_MAX:
+                        err |= ERR_RANGE
+                        out.append(-1)
+                        continue
+            if row >= 0:
+                out.append(B + 1 + row)
+            elif newest >= 0 and p == newest:
+                out.append(B)
+            elif p >= seq_len:
+                err |= ERR_RANGE
+                out.append(-1)
+            else:
+                out.append(p)                  # slot numbered like the position
+        if err:
+            out = [-1] * len(sel)
+        return out, plan, err
 
     # ------------------------------------------------------------------ #
     def admit(self, n, k=None):

@@ -17,7 +17,8 @@ from workload.traces import all_traces
 class Run:
     def __init__(self, w, flags=0, mirror=False, ctas_per_request=0, replay_ctas=0,
                  num_reqs=None, oracle_bytes=True, traces=None, lookup=0, pool_kind=H.HOST_PINNED,
-                 fused=True, resident=None, group=1, group_replay=True, inline_shared=False):
+                 fused=True, resident=None, group=1, group_replay=True, inline_shared=False,
+                 l2_persist=0):
         """``resident`` = (int32 [steps][R][nblk] block tables, tokens per
         block) runs every anchor through the three-tier resolve, with the
         table of step t in place before step t."""
@@ -33,6 +34,8 @@ class Run:
         self.hs = HiSparse(w.R, w.L, w.k, w.B, w.P, w.rec, self.mem.layer_buffers(),
                            anchor_of=w.anchor_of(), ctas_per_request=ctas_per_request,
                            replay_ctas=replay_ctas, lookup=lookup)
+        if l2_persist:
+            self.hs.set_l2_persisting(l2_persist)
         anchor_of = w.anchor_of()
         self.groups = [(a, [l for l in range(w.L) if anchor_of[l] == a]) for a in w.anchors()]
         tr = traces if traces is not None else all_traces(w)
@@ -80,6 +83,12 @@ class Run:
                 o.reset()
             self.oracle[l] = o
         self.oracle_out = np.full((len(self.groups), w.R, w.k), -7, np.int32)
+        self.seq_np = self.seq = None
+        if w.admit_preload:   # short requests: admitted with their prefill preloaded
+            self.seq_np = (w.L_ctx + 1 + np.arange(w.steps, dtype=np.int32))[:, None].repeat(
+                w.R, axis=1)                                               # [T][R]
+            self.seq = torch.from_numpy(np.ascontiguousarray(self.seq_np)).to(dev)
+            self.admit(list(range(w.R)), [w.L_ctx] * w.R)
         self.t = 0
 
     # ------------------------------------------------------------------ #
@@ -89,7 +98,8 @@ class Run:
         self.step_runner.issue(self.sel[t], self.out,
                                newest=self.newest[t] if self.newest is not None else None,
                                wb_pos=self.wb[t] if (self.w.write_through and t > 0) else None,
-                               new_rows=self.new_rows[t] if self.new_rows is not None else None)
+                               new_rows=self.new_rows[t] if self.new_rows is not None else None,
+                               seq_lens=self.seq[t] if self.seq is not None else None)
 
     def oracle_step(self, t):
         w = self.w
@@ -104,10 +114,17 @@ class Run:
                 self.oracle[l].set_newest_rows(self.new_rows_np[t, l], num_reqs=nr)
         for gi, (a, fl) in enumerate(self.groups):
             nw = self.newest_np[t] if self.newest_np is not None else None
-            out, _ = self.oracle[a].resolve(self.sel_np[t, gi], nw, num_reqs=nr, io=io,
-                                            res_blocks=None if self.res_np is None else
-                                            self.res_np[t], res_tok=self.res_tok,
-                                            union=bool(self.flags & H.UNION))
+            if self.seq_np is not None:
+                prev = self.wb_np[t, a] if t > 0 else np.full(w.R, -1, np.int32)
+                out, _ = self.oracle[a].resolve_with_seq_lens(
+                    self.sel_np[t, gi], nw, prev, self.seq_np[t], num_reqs=nr, io=io,
+                    res_blocks=None if self.res_np is None else self.res_np[t],
+                    res_tok=self.res_tok, union=bool(self.flags & H.UNION))
+            else:
+                out, _ = self.oracle[a].resolve(self.sel_np[t, gi], nw, num_reqs=nr, io=io,
+                                                res_blocks=None if self.res_np is None else
+                                                self.res_np[t], res_tok=self.res_tok,
+                                                union=bool(self.flags & H.UNION))
             self.oracle_out[gi, :nr] = out[:nr]
             for f in fl:
                 self.oracle[a].replay_into(self.oracle[f], num_reqs=nr)

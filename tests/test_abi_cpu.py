@@ -15,7 +15,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 def declared_functions():
     src = open(os.path.join(ROOT, "include", "hisparse.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(hisparse_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(hisparse_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_library_exports_every_declared_symbol():
@@ -39,7 +39,7 @@ def declared_arity():
     src = open(os.path.join(ROOT, "include", "hisparse.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     out = {}
-    for name, params in re.findall(r"\b(hisparse_[a-z_]+)\s*\(([^;{]*?)\)\s*;", src, flags=re.S):
+    for name, params in re.findall(r"\b(hisparse_[a-z0-9_]+)\s*\(([^;{]*?)\)\s*;", src, flags=re.S):
         params = params.strip()
         out[name] = 0 if params in ("", "void") else params.count(",") + 1
     return out

@@ -290,6 +290,19 @@ def test_from_mirror_with_write_through_shared_layers(mode):
              group_replay=mode == "group")
 
 
+def test_l2_persisting_page_tables_change_nothing():
+    """With the page tables kept persisting in L2, every step equals the
+    oracle; turning it off again works; a negative size is refused."""
+    w = get("dsa").scaled(R=3, groups=2, L_ctx=16384, steps=6)
+    _run_all(w, l2_persist=16 << 20)
+    mem = WorkloadMemory(w.R, w.L, w.B, w.P, w.rec)
+    hs = HiSparse(w.R, w.L, w.k, w.B, w.P, w.rec, mem.layer_buffers())
+    assert H.hisparse_set_l2_persisting(hs.h, -1) == H.EINVAL
+    assert H.hisparse_set_l2_persisting(hs.h, 8 << 20) == H.OK
+    assert H.hisparse_set_l2_persisting(hs.h, 0) == H.OK
+    hs.close(); mem.close()
+
+
 def test_huge_page_pool():
     """The same results from a huge-page-backed, registered host pool."""
     _run_all(get("dsa").scaled(R=3, groups=2, L_ctx=65536, steps=6), pool_kind=H.HOST_HUGE)
@@ -873,4 +886,134 @@ def test_graph_with_host_inputs_and_outputs_by_sm_copy():
         torch.cuda.synchronize()
         np.testing.assert_array_equal(h_out[t].numpy(), ref)
     assert np.array_equal(mem.hot[0].cpu().numpy(), o.hot)
+    hs.close(); mem.close()
+
+
+# ---------------------------------------------------------------------- #
+# Short requests: growth by the previous token, lookup by position         #
+# ---------------------------------------------------------------------- #
+@pytest.mark.parametrize("cs", [0, 1, 3])
+@pytest.mark.parametrize("shared", ["none", "group", "inline"])
+def test_short_requests_mixed_batch(cs, shared):
+    """A batch of short requests (admitted with their tokens preloaded, then
+    grown by one token per step), requests that outgrow B during the run, and
+    long requests, through the fused write-through with per-request sequence
+    lengths: every step's slot vectors, slot maps, LRU orders, page tables,
+    miss counts, plans, hot bytes of every layer and written-back host rows
+    equal the oracle's."""
+    R, k, B, rec, steps = 6, 64, 256, 64, 10
+    lens0 = np.array([40, 200, 250, 600, 1000, 253], np.int32)
+    P = int(lens0.max()) + steps
+    L = 1 if shared == "none" else 3
+    anchor_of = [-1] + [0] * (L - 1)
+    rng = np.random.default_rng(17 + cs)
+    mem = WorkloadMemory(R, L, B, P, rec)
+    for l in range(L):
+        mem.host_view(l)[:] = rng.integers(0, 256, size=(R, P, rec), dtype=np.uint8)
+    hs = HiSparse(R, L, k, B, P, rec, mem.layer_buffers(), anchor_of=anchor_of,
+                  ctas_per_request=cs)
+    orc = []
+    for l in range(L):
+        o = OracleLayer(R, k, B, P, rec, host_split=0, metadata=l == 0)
+        o.host_tail[:] = mem.host_view(l)
+        orc.append(o)
+    orc[0].reset()
+    short0 = [r for r in range(R) if lens0[r] + 1 <= B]
+    reqs = _dev(np.arange(R, dtype=np.int32))
+    pre = np.where(lens0 + 1 <= B, lens0, 0).astype(np.int32)
+    hs.admit(-1, reqs, _dev(pre))
+    for r in range(R):
+        orc[0].admit(r, int(pre[r]))
+        for l in range(1, L):
+            orc[l].preload_bytes(r, int(pre[r]))
+    out = torch.empty((R, k), dtype=torch.int32, device="cuda")
+    try:
+        for t in range(steps):
+            seq = lens0 + t + 1
+            newest = lens0 + t
+            prev = (newest - 1) if t > 0 else np.full(R, -1, np.int32)
+            new_rows = rng.integers(0, 256, size=(L, R, rec), dtype=np.uint8)
+            sel = np.full((R, k), -1, np.int32)
+            for r in range(R):
+                m = min(k - 2, int(seq[r]))
+                pick = rng.choice(int(seq[r]), size=m, replace=False)
+                if t > 0 and prev[r] not in pick:
+                    pick[0] = prev[r]              # the local window: last token again
+                sel[r, :m] = pick
+            sel[1, 5] = sel[1, 6]                  # a repeat (short request: not an error)
+            d_new = _dev(new_rows, torch.uint8)
+            d_prev = _dev(prev.astype(np.int32))
+            flags = H.WITH_SHARED if shared == "inline" else (H.RECORD_PLAN if L > 1 else 0)
+            for l in range(1, L):
+                if shared == "inline":
+                    hs.writeback(l, d_prev, new_rows=d_new[l])
+            hs.resolve_ex(0, _dev(sel), out, newest=_dev(newest.astype(np.int32)),
+                          prev_pos=d_prev, new_rows=d_new[0], flags=flags,
+                          seq_lens=_dev(seq.astype(np.int32)))
+            if shared == "group":
+                for l in range(1, L):
+                    hs.writeback(l, d_prev, new_rows=d_new[l])
+                hs.prefetch_plan(0, -1)
+            # oracle: write-backs, new tokens, the step, the shared layers' bytes
+            for l in range(L):
+                if t > 0:
+                    orc[l].writeback(prev)
+                orc[l].set_newest_rows(new_rows[l])
+            oo, e = orc[0].resolve_with_seq_lens(sel, newest, prev, seq)
+            for l in range(1, L):
+                orc[0].replay_into(orc[l])
+            torch.cuda.synchronize()
+            np.testing.assert_array_equal(out.cpu().numpy(), oo, err_msg=f"out step {t}")
+            sp, lru, pt, mc = hs.export_state(0)
+            np.testing.assert_array_equal(sp, orc[0].slot_pos, err_msg=f"slot_pos step {t}")
+            np.testing.assert_array_equal(lru, orc[0].lru, err_msg=f"lru step {t}")
+            np.testing.assert_array_equal(pt, orc[0].page_table, err_msg=f"page table step {t}")
+            np.testing.assert_array_equal(mc, orc[0].miss_count, err_msg=f"misses step {t}")
+            if shared == "group":
+                c, pp, ps = hs.export_plan(0)
+                for r in range(R):
+                    assert list(zip(pp[r, :c[r]], ps[r, :c[r]])) == list(zip(
+                        orc[0].plan_pos[r, :orc[0].plan_count[r]],
+                        orc[0].plan_slot[r, :orc[0].plan_count[r]])), f"plan {r} step {t}"
+            hot = mem.hot.cpu().numpy()
+            for l in range(L):
+                np.testing.assert_array_equal(hot[l], orc[l].hot, err_msg=f"hot {l} step {t}")
+                np.testing.assert_array_equal(mem.host_view(l), orc[l].host_tail,
+                                              err_msg=f"host rows {l} step {t}")
+            flags_, ue = hs.status()
+            np.testing.assert_array_equal(ue[0], orc[0].unit_err, err_msg=f"unit errors {t}")
+        # the short requests took the short path throughout, with one growth per step
+        sp = hs.export_state(0)[0]
+        for r in short0:
+            n = min(int(lens0[r]) + steps - 1, B)
+            if lens0[r] + steps <= B:
+                assert sp[r, :n].tolist() == list(range(n)), f"request {r} not in order"
+    finally:
+        hs.close()
+        mem.close()
+
+
+def test_short_workload_full_size_every_step():
+    """8 requests x 4 layers with 3K-position contexts and B=4096, admitted
+    with their prefill preloaded: every step takes the short path (growth by
+    the previous token, lookup by position), write-through fused."""
+    _run_all(get("short"))
+
+
+@pytest.mark.parametrize("cs", [1, 3])
+def test_short_workload_crossing_the_buffer(cs):
+    """Contexts that outgrow B during the run: the short path until seq_len
+    exceeds B, the general resolve after, every step compared."""
+    _run_all(get("short").scaled(R=3, groups=2, L_ctx=1020, k=256, B=1024, steps=10,
+                                 W_loc=16), ctas_per_request=cs)
+
+
+def test_short_requests_rejected_by_the_hash_lookup():
+    R, k, B, P = 2, 8, 16, 64
+    mem, hs = _instance(R, k, B, P, lookup=H.LOOKUP_HASH)
+    out = torch.empty((R, k), dtype=torch.int32, device="cuda")
+    sel = _dev(np.array([[1, 2, 3, 4, 5, 6, 7, 8]] * R, np.int32))
+    with pytest.raises(H.HiSparseError) as ei:
+        hs.resolve_ex(0, sel, out, seq_lens=_dev(np.array([9, 9], np.int32)))
+    assert ei.value.code == H.EINVAL
     hs.close(); mem.close()

@@ -478,3 +478,189 @@ def _preload_one_short(o, r, n):
                                     _preload_one_short])
 def test_preload_pin_catches_planted_mistakes(mutant):
     assert not _preload_matches_replay(mutant)
+
+
+# ---------------------------------------------------------------------- #
+# Short requests (reading R17)                                             #
+# ---------------------------------------------------------------------- #
+import copy  # noqa: E402
+
+
+def _short_run(cls, B=16, k=5, n=6, steps=9, seed=0, check=True):
+    """A request admitted with n positions preloaded, then decoded on the
+    short path until seq_len reaches B: every step writes the previous token
+    back (the host callable returns what the write-back stored), grows the
+    buffer by it and looks the selection up.  With ``check``, asserts the
+    closed forms after every step; returns False on the first failure."""
+    rng = random.Random(seed)
+    store = {}
+    host = lambda p: store.get(p, ("prefill", p))   # noqa: E731
+    u = cls(B, 4 * B, k=k, host=host)
+    u.admit(n, k=k)
+    t = 0
+    while n + t + 1 <= B and t < steps:
+        newest = n + t
+        prev = newest - 1 if t > 0 else -1
+        seq_len = n + t + 1
+        if prev >= 0:
+            store[prev] = ("written", prev)     # the write-back of the previous token
+        pool = list(range(seq_len))
+        sel = rng.sample(pool, min(k - 1, seq_len)) + [-1]
+        rng.shuffle(sel)
+        ref = copy.deepcopy(u)
+        out, plan, err = u.resolve_short(sel, newest, seq_len, prev=prev)
+        ok = err == 0
+        grown = n + t                           # slots 0..grown-1 hold their positions
+        ok = ok and u.slot_pos[:grown] == list(range(grown))
+        ok = ok and all(u.hot[s] == host(s) for s in range(grown))
+        ok = ok and u.lru == list(range(grown, B)) + list(range(n)) + list(range(n, grown))
+        ok = ok and plan == ([(prev, prev)] if prev >= 0 else [])
+        # the general resolve on the grown state gives the same slots, all hits
+        if prev >= 0:
+            ref.resolve([prev])
+        o2, p2, e2 = ref.resolve(sel, newest)
+        ok = ok and out == o2 and p2 == [] and e2 == 0
+        if check:
+            assert ok, f"step {t}"
+        elif not ok:
+            return False
+        t += 1
+    return True
+
+
+@pytest.mark.parametrize("B,k,n", [(16, 5, 6), (8, 3, 0), (32, 7, 31), (12, 12, 1)])
+def test_short_path_grows_in_order_and_equals_the_general_resolve(B, k, n):
+    """Closed forms of R17 for an admitted short request: slot s holds
+    position s and its record, the LRU order is the remaining empties, the
+    preloaded slots, then the grown ones, each growth is one planned miss into
+    the next empty slot, and every lookup equals the general resolve's output
+    on the same state (all hits, no misses)."""
+    for seed in range(4):
+        _short_run(Unit, B=B, k=k, n=n, steps=B, seed=seed)
+
+
+def _short_error_pin(cls):
+    """A position at or past seq_len, or a bad newest position, fails the
+    lookup (all -1) after the growth has happened; a repeated position is not
+    an error; padding stays -1; a resident row comes first."""
+    u = cls(8, 40, k=4, host=lambda p: p)
+    u.admit(3, k=4)
+    out, plan, err = u.resolve_short([0, 1, 4, -1], 3, 4, prev=-1)
+    assert err == ERR_RANGE and out == [-1] * 4 and plan == []
+    out, plan, err = u.resolve_short([0, 0, 2, -1], 4, 5, prev=3)
+    assert err == 0 and out == [0, 0, 2, -1] and plan == [(3, 3)] and u.slot_pos[3] == 3
+    out, plan, err = u.resolve_short([0, 1, 2, 4], 4, 5, prev=-1)
+    assert err == 0 and out == [0, 1, 2, 8] and u.miss_count == 0
+    out, plan, err = u.resolve_short([0, 1, 2, 3], 40, 5)
+    assert err == ERR_RANGE and out == [-1] * 4
+    out, plan, err = u.resolve_short([0, 9, 2, -1], 4, 5, res_blocks=[-1, -1, 7], res_tok=4)
+    assert err == 0 and out == [0, 8 + 1 + 7 * 4 + 1, 2, -1]
+
+
+def test_short_path_errors_and_repeats():
+    _short_error_pin(Unit)
+
+
+def test_short_to_long_transition():
+    """At seq_len = B + 1 the general resolve takes over: the token at B - 1
+    was never grown (its step is no longer short), so it is host-only, misses
+    and takes the one empty slot, B - 1, which the growths left least recent."""
+    B, k, n = 8, 3, 5
+    store = {}
+    u = Unit(B, 40, k=k, host=lambda p: store.get(p, p))
+    u.admit(n, k=k)
+    for t in range(1, B - n):                 # grow positions n .. B-2
+        store[n + t - 1] = ("w", n + t - 1)
+        u.resolve_short([0, -1, -1], n + t, n + t + 1, prev=n + t - 1)
+    assert u.slot_pos == list(range(B - 1)) + [-1]
+    assert u.lru == [B - 1] + list(range(B - 1))
+    store[B - 1] = ("w", B - 1)                 # the transition step's write-back
+    out, plan, err = u.resolve([B - 1, 0, B], newest=B)
+    assert err == 0 and out == [B - 1, 0, B] and plan == [(B - 1, B - 1)]
+    assert u.hot[B - 1] == ("w", B - 1) and u.lru == list(range(1, B - 1)) + [B - 1, 0]
+
+
+def test_short_path_python_equals_c():
+    """The C model's step with per-request sequence lengths (short requests
+    grown and looked up by position, long ones resolved) equals the Python
+    model's, field by field, over mixed batches, a resident table included."""
+    from oracle.coracle import OracleLayer
+    R, k, B, P, rec = 4, 6, 16, 64, 8
+    rng = np.random.default_rng(5)
+    host = rng.integers(0, 256, size=(R, P, rec), dtype=np.uint8)
+    lens0 = [3, 10, 20, 40]                     # two short, two long
+    c = OracleLayer(R, k, B, P, rec, host=host)
+    c.reset()
+    py = []
+    for r in range(R):
+        u = Unit(B, P, k=k, host=lambda p, r=r: bytes(host[r, p]))
+        pre = lens0[r] if lens0[r] <= B else 0
+        u.admit(pre, k=k)
+        c.admit(r, pre)
+        py.append(u)
+    blocks = np.full((R, P // 8), -1, np.int32)
+    blocks[2, 1] = 3
+    for t in range(8):
+        seq = np.array([L + t + 1 for L in lens0], np.int32)
+        newest = seq - 1
+        prev = np.where(np.full(R, t > 0), newest - 1, -1).astype(np.int32)
+        sel = np.full((R, k), -1, np.int32)
+        for r in range(R):
+            m = min(k - 1, int(seq[r]))
+            sel[r, :m] = rng.choice(int(seq[r]), size=m, replace=False)
+        out, err = c.resolve_with_seq_lens(sel, newest, prev, seq, res_blocks=blocks, res_tok=8)
+        for r in range(R):
+            u = py[r]
+            if seq[r] <= B:
+                o, plan, e = u.resolve_short(sel[r].tolist(), int(newest[r]), int(seq[r]),
+                                             prev=int(prev[r]), res_blocks=blocks[r].tolist(),
+                                             res_tok=8)
+            else:
+                o, plan, e = u.resolve(sel[r].tolist(), int(newest[r]),
+                                       res_blocks=blocks[r].tolist(), res_tok=8)
+            assert out[r].tolist() == o and c.unit_err[r] == e
+            assert c.slot_pos[r].tolist() == u.slot_pos and c.lru[r].tolist() == u.lru
+            assert int(c.miss_count[r]) == u.miss_count
+            assert list(zip(c.plan_pos[r, :c.plan_count[r]].tolist(),
+                            c.plan_slot[r, :c.plan_count[r]].tolist())) == plan
+            for s in range(B):
+                if u.slot_pos[s] >= 0:
+                    assert bytes(c.hot[r, s]) == u.hot[s]
+
+
+class _ShortNoNewest(Unit):
+    def resolve_short(self, sel, newest, seq_len, prev=-1, res_blocks=None, res_tok=1):
+        return super().resolve_short(sel, -1 if newest < seq_len - 1 else -1, seq_len + 1,
+                                     prev, res_blocks, res_tok)
+
+
+class _ShortRangeOffByOne(Unit):
+    def resolve_short(self, sel, newest, seq_len, prev=-1, res_blocks=None, res_tok=1):
+        return super().resolve_short([p if p < seq_len + 1 else p for p in sel], newest,
+                                     seq_len + 1, prev, res_blocks, res_tok)
+
+
+class _ShortGrowsIntoRecentSlot(Unit):
+    def resolve_short(self, sel, newest, seq_len, prev=-1, res_blocks=None, res_tok=1):
+        if prev >= 0 and prev not in self.page_table:
+            self.lru = self.lru[::-1]           # the victim becomes the most recent slot
+            out = super().resolve_short(sel, newest, seq_len, prev, res_blocks, res_tok)
+            return out
+        return super().resolve_short(sel, newest, seq_len, prev, res_blocks, res_tok)
+
+
+class _ShortNoGrowth(Unit):
+    def resolve_short(self, sel, newest, seq_len, prev=-1, res_blocks=None, res_tok=1):
+        return super().resolve_short(sel, newest, seq_len, -1, res_blocks, res_tok)
+
+
+@pytest.mark.parametrize("cls", [_ShortNoNewest, _ShortGrowsIntoRecentSlot, _ShortNoGrowth])
+def test_short_path_pins_catch_planted_mistakes(cls):
+    caught = not all(_short_run(cls, B=16, k=5, n=6, steps=16, seed=s, check=False)
+                     for s in range(4))
+    assert caught
+
+
+def test_short_path_range_pin_catches_an_off_by_one():
+    with pytest.raises(AssertionError):
+        _short_error_pin(_ShortRangeOffByOne)

@@ -32,6 +32,8 @@ class Workload:
     all_hit: bool = False  # every step repeats step 0's selection list
     seed: int = 0
     sel_block_tokens: int = 1  # > 1: the selector picks blocks of this many positions
+    admit_preload: bool = False  # requests admitted with their prefill preloaded and
+                                 # resolved with their sequence lengths (short requests)
 
     @property
     def L(self):
@@ -83,6 +85,12 @@ WORKLOADS = {
     "blocks": Workload("blocks", R=8, groups=4, followers=0, L_ctx=131072, k=2048, B=4096,
                        rec=1152, steps=32, write_through=False, f=0.87, W_hist=4, n_sink=4,
                        W_loc=128, zipf_s=1.1, seed=606, sel_block_tokens=4),
+    # Short requests: 8 requests x 4 layers whose contexts fit the buffer (3K
+    # positions prefilled, B=4096): admitted with their tokens preloaded, then
+    # grown by one token per step and looked up by position.
+    "short": Workload("short", R=8, groups=4, followers=0, L_ctx=3072, k=2048, B=4096,
+                      rec=1152, steps=32, write_through=True, f=0.87, W_hist=4, n_sink=4,
+                      W_loc=128, zipf_s=1.1, seed=707, admit_preload=True),
     # Shared-index groups: 32 requests x 4 groups of (1 anchor + 3 shared layers).
     "shared": Workload("shared", R=32, groups=4, followers=3, L_ctx=131072, k=2048, B=4096,
                        rec=1152, steps=32, write_through=False, f=0.87, W_hist=4, n_sink=4,

@@ -82,8 +82,7 @@ def parse():
                     help="after the timed pass, compare its final state with the oracle "
                          "(the default)")
     ap.add_argument("--no-verify", dest="verify", action="store_false")
-    ap.add_argument("--workloads", default="tiny,quest,short,shared_inline,shared_anchor,sweep,"
-                                           "sweep_allhit",
+    ap.add_argument("--workloads", default=",".join(SUB_WORKLOADS),
                     help="the other workloads measured after the headline, each on its own "
                          "pool, reported in the line's `workloads` object (one GPU only)")
     ap.add_argument("--no-workloads", action="store_true")
@@ -344,7 +343,7 @@ TARGET_LINK_FRAC = 0.8   # the miss-fetch path's target share of the measured ho
 
 # The default line's other workloads (name -> how it is built and run).
 SUB_WORKLOADS = ("tiny", "quest", "short", "shared_inline", "shared_anchor", "sweep",
-                 "sweep_allhit")
+                 "sweep_huge", "sweep_allhit")
 SWEEP_POINT = (4096, 0.87)           # (B, reuse fraction) of the capacity-sweep entry
 SWEEP_CONTEXTS = (1048576, 524288, 262144)
 HOST_MARGIN_GIB = 32                 # host memory left free beside a pinned pool
@@ -659,10 +658,10 @@ def measure(o, w, dev, h2d_gbs, dist=None, world=1, headline=False, rank=0, cloc
     cur = torch.cuda.current_stream()
 
     def wake():
-        """About 20 ms of HBM writes: a GPU that sat idle (while the host
-        checked results or sampled clocks) runs its first microseconds of
-        work slower, which a serving GPU, busy step after step, does not."""
-        for i in range(400):
+        """About 2 ms of HBM writes before the warm-up, so that the timed steps
+        do not start on a GPU that sat idle while the host prepared them (a
+        serving GPU is busy step after step)."""
+        for i in range(40):
             flush.fill_(i & 0xFF)
 
     def from_admission(warm=True):
@@ -765,11 +764,6 @@ def measure(o, w, dev, h2d_gbs, dist=None, world=1, headline=False, rank=0, cloc
         clocks.__exit__()
     flags, _ = hs.status()
 
-    # ---- the timed run's final state against the oracle ----
-    verify = None
-    if o.verify and not o.resident and w.sel_block_tokens == 1 and o.verify_rows == 1:
-        verify = verify_against_oracle(w, hs, mem, groups, traces, T)
-
     replay_launches = sum((-(-len(f) // 8) if o.replay == "group" else
                            0 if o.replay == "inline" else len(f)) for _, f in groups if f)
     launches = K * (G + replay_launches + (1 if (wb is not None and o.unfused) else 0))
@@ -807,6 +801,14 @@ def measure(o, w, dev, h2d_gbs, dist=None, world=1, headline=False, rank=0, cloc
         torch.cuda.synchronize()
     flags |= hs.status()[0]
     miss = miss_hist[W:].cpu().numpy().astype(np.int64)       # [K][G][R]
+    # ---- the timed steps' final state against the oracle (pass 2 ran the same
+    #      steps from the admission state, so the state is the timed run's).
+    #      Checked after all GPU timing: the host work of the check can make
+    #      the GPU drop its translations of the host pool, which slows the next
+    #      pass. ----
+    verify = None
+    if o.verify and not o.resident and w.sel_block_tokens == 1 and o.verify_rows == 1:
+        verify = verify_against_oracle(w, hs, mem, groups, traces, T)
 
     total_ms = sum(step_ms)
     sel_per_step = G * w.R * w.k
@@ -1144,7 +1146,7 @@ def sub_workload(args, name):
     if name in ("shared_inline", "shared_anchor"):
         return get("shared"), opts_for(args, replay="inline" if name == "shared_inline"
                                        else "group", interleave=True, **base)
-    if name in ("sweep", "sweep_allhit"):
+    if name in ("sweep", "sweep_huge", "sweep_allhit"):
         B, f = SWEEP_POINT
         L, why = pick_sweep_context(B, f)
         if L is None:
@@ -1158,6 +1160,8 @@ def sub_workload(args, name):
                 return None, {"reason": "the HBM mirror does not fit", "hbm_free_gb":
                               round(free / 1e9, 1), "mirror_gb": round(w.host_bytes() / 1e9, 1)}
         kw = dict(base, mirror=name == "sweep_allhit")
+        if name == "sweep_huge":   # the same point on a huge-page-backed pool
+            kw["pool"] = "huge"
         o = opts_for(args, replay="group", interleave=False, **kw)
         o._context_choice = why
         return w, o

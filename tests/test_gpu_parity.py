@@ -1043,3 +1043,80 @@ def test_short_requests_rejected_by_the_hash_lookup():
         hs.resolve_ex(0, sel, out, seq_lens=_dev(np.array([9, 9], np.int32)))
     assert ei.value.code == H.EINVAL
     hs.close(); mem.close()
+
+
+@pytest.mark.parametrize("opt", ["resident", "union", "blocks"])
+def test_short_requests_with_extended_options(opt):
+    """Short and long requests in one batch with the other options of the
+    general RESOLVE: a resident block table (resident rows come first on the
+    short path too), union verify rows (repeats resolve once on the general
+    path and are simply looked up on the short one), and block-id selections
+    expanded in the kernel."""
+    from oracle.tiny import expand_blocks
+    R, k, B, rec, steps, bt = 4, 64, 128, 32, 8, 4
+    lens0 = np.array([20, 100, 300, 121], np.int32)   # short, short, long, crossing
+    P = int(lens0.max()) + steps
+    rng = np.random.default_rng(31)
+    mem = WorkloadMemory(R, 1, B, P, rec)
+    mem.host_view(0)[:] = rng.integers(0, 256, size=(R, P, rec), dtype=np.uint8)
+    hs = HiSparse(R, 1, k, B, P, rec, mem.layer_buffers())
+    o = OracleLayer(R, k, B, P, rec, host_split=0)
+    o.host_tail[:] = mem.host_view(0)
+    o.reset()
+    pre = np.where(lens0 + 1 <= B, lens0, 0).astype(np.int32)
+    hs.admit(0, _dev(np.arange(R, dtype=np.int32)), _dev(pre))
+    for r in range(R):
+        o.admit(r, int(pre[r]))
+    out = torch.empty((R, k), dtype=torch.int32, device="cuda")
+    blocks = None
+    if opt == "resident":
+        blocks = np.full((R, P // 16 + 1), -1, np.int32)
+        blocks[0, 0] = 5        # positions 0..15 of request 0 resident
+        blocks[2, 3] = 9        # positions 48..63 of request 2 resident
+    try:
+        for t in range(steps):
+            seq = lens0 + t + 1
+            newest = lens0 + t
+            prev = (newest - 1) if t > 0 else np.full(R, -1, np.int32)
+            new_rows = rng.integers(0, 256, size=(R, rec), dtype=np.uint8)
+            if opt == "blocks":
+                kb = k // bt
+                sel_gpu = np.full((R, kb), -1, np.int32)
+                for r in range(R):
+                    nb = min(kb, int(seq[r]) // bt)
+                    sel_gpu[r, :nb] = rng.choice(int(seq[r]) // bt, size=nb, replace=False)
+                sel = np.array([expand_blocks(row.tolist(), bt) for row in sel_gpu], np.int32)
+            else:
+                sel = np.full((R, k), -1, np.int32)
+                for r in range(R):
+                    m = min(k, int(seq[r]))
+                    sel[r, :m] = rng.choice(int(seq[r]), size=m, replace=False)
+                if opt == "union":
+                    sel[:, k // 2:] = sel[:, :k // 2]   # a second verify row repeating the first
+                sel_gpu = sel
+            flags = H.UNION if opt == "union" else 0
+            hs.resolve_ex(0, _dev(sel_gpu), out, newest=_dev(newest.astype(np.int32)),
+                          prev_pos=_dev(prev.astype(np.int32)), new_rows=_dev(new_rows, torch.uint8),
+                          res_blocks=None if blocks is None else _dev(blocks),
+                          res_block_tokens=16 if blocks is not None else 0,
+                          sel_block_tokens=bt if opt == "blocks" else 1, flags=flags,
+                          seq_lens=_dev(seq.astype(np.int32)))
+            if t > 0:
+                o.writeback(prev)
+            o.set_newest_rows(new_rows)
+            oo, _ = o.resolve_with_seq_lens(sel, newest, prev, seq, res_blocks=blocks,
+                                            res_tok=16, union=opt == "union")
+            torch.cuda.synchronize()
+            np.testing.assert_array_equal(out.cpu().numpy(), oo, err_msg=f"out step {t}")
+            sp, lru, pt, mc = hs.export_state(0)
+            np.testing.assert_array_equal(sp, o.slot_pos, err_msg=f"slot_pos step {t}")
+            np.testing.assert_array_equal(lru, o.lru, err_msg=f"lru step {t}")
+            np.testing.assert_array_equal(pt, o.page_table, err_msg=f"page table step {t}")
+            np.testing.assert_array_equal(mc, o.miss_count, err_msg=f"misses step {t}")
+            np.testing.assert_array_equal(mem.hot[0].cpu().numpy(), o.hot, err_msg=f"hot step {t}")
+            np.testing.assert_array_equal(mem.host_view(0), o.host_tail, err_msg=f"host step {t}")
+            flags_, ue = hs.status()
+            np.testing.assert_array_equal(ue[0], o.unit_err, err_msg=f"unit errors {t}")
+    finally:
+        hs.close()
+        mem.close()

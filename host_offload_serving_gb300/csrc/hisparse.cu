@@ -1431,15 +1431,53 @@ __device__ void pt_short_path(const PtArgs &a, int r, int32_t prev, int32_t newe
   int16_t *g_lru = a.lru + static_cast<int64_t>(r) * B;
   const uint4 *keep = reinterpret_cast<const uint4 *>(smem + L.l_prevrow);
 
-  // (1) write-through
-  pt_leader_write_through(a, r, prev, smem, L);
+  // (0) every load the three steps need goes out at once: row B and the new
+  // token's row, the previous token's page-table entry, the LRU row and the
+  // selections (one memory round trip instead of three)
+  const bool grow = a.prev_pos && prev >= 0 && prev < P;
+  const bool through = a.prev_pos || a.new_rows;
+  uint4 *rowb = reinterpret_cast<uint4 *>(a.hot + static_cast<int64_t>(r) * a.hot_req_stride +
+                                          static_cast<int64_t>(B) * a.hot_row_stride);
+  const uint4 *nrow = a.new_rows ? reinterpret_cast<const uint4 *>(
+                                       a.new_rows + static_cast<int64_t>(r) * a.rec16 * 16)
+                                 : nullptr;
+  uint4 kv = make_uint4(0, 0, 0, 0), nv = make_uint4(0, 0, 0, 0);
+  if (through && tid < a.rec16) kv = rowb[tid];
+  if (nrow && tid < a.rec16) nv = nrow[tid];
+  const int32_t hs0 = (grow && tid == 0) ? g_pt[prev] : -1;
+  const bool lru16 = grow && B % 8 == 0;
+  int4 lv = make_int4(0, 0, 0, 0);
+  if (lru16 && tid < B / 8) lv = reinterpret_cast<const int4 *>(g_lru)[tid];
+  int32_t sv[2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int i = tid + u * kThreads;
+    sv[u] = i < k ? sel_position<true>(a, r, i) : -1;
+  }
+  // (1) write-through, first half: row B kept, the new token in its place
+  uint4 *keep_w = reinterpret_cast<uint4 *>(smem + L.l_prevrow);
+  if (through) {
+    for (int c = tid; c < a.rec16; c += kThreads) {
+      keep_w[c] = c == tid ? kv : rowb[c];
+      if (nrow) rowb[c] = c == tid ? nv : nrow[c];
+    }
+    if (prev >= P && tid == 0) atomicOr(a.status, HISPARSE_ERR_RANGE);
+  }
+  if (grow) {
+    if (lru16) {
+      if (tid < B / 8) reinterpret_cast<int4 *>(l_lru)[tid] = lv;
+      for (int c = tid + kThreads; c < B / 8; c += kThreads)
+        reinterpret_cast<int4 *>(l_lru)[c] = reinterpret_cast<const int4 *>(g_lru)[c];
+    } else {
+      for (int j = tid; j < B; j += kThreads) l_lru[j] = g_lru[j];
+    }
+  }
   if (tid == 0) {
     l_misc[kLErr] = (newest < -1 || newest >= P) ? HISPARSE_ERR_RANGE : 0u;
-    l_misc[kLM] = 0;
+    l_misc[kLM] = static_cast<uint32_t>(hs0);
     l_misc[kLHits] = 0;
   }
   __syncthreads();
-  const bool grow = a.prev_pos && prev >= 0 && prev < P;
   if (grow) {
     uint4 *hrow = reinterpret_cast<uint4 *>(a.host_w + static_cast<int64_t>(r) * a.host_req_stride +
                                             static_cast<int64_t>(prev) * a.host_row_stride);
@@ -1450,9 +1488,6 @@ __device__ void pt_short_path(const PtArgs &a, int r, int32_t prev, int32_t newe
       for (int c = tid; c < a.rec16; c += kThreads) st_v4(mrow + c, keep[c]);
     }
     // (2) growth by the previous token
-    for (int j = tid; j < B; j += kThreads) l_lru[j] = g_lru[j];
-    if (tid == 0) l_misc[kLM] = static_cast<uint32_t>(g_pt[prev]);
-    __syncthreads();
     const int32_t hslot = static_cast<int32_t>(l_misc[kLM]);
     const bool bad = hslot >= B || hslot < -1;   // a corrupt page-table entry
     if (hslot >= 0 && !bad)
@@ -1505,7 +1540,8 @@ __device__ void pt_short_path(const PtArgs &a, int r, int32_t prev, int32_t newe
   const int32_t *g_res = a.res_blocks ? a.res_blocks + static_cast<int64_t>(r) * a.res_nblk : nullptr;
   uint32_t err = 0;
   for (int i = tid; i < k; i += kThreads) {
-    const int32_t p = sel_position<true>(a, r, i);
+    const int u = (i - tid) / kThreads;
+    const int32_t p = u < 2 ? sv[u] : sel_position<true>(a, r, i);
     int32_t v = -1;
     if (p != -1) {
       if (p < -1 || p >= P) {

@@ -1945,6 +1945,8 @@ struct hisparse_handle {
   int32_t cs, cap_log2, replay_ctas, sm_count, device, lookup, ks;
   uint32_t smem;
   float l2_hit_ratio = 0.f;   // > 0: RESOLVE launches keep the page table persisting in L2
+  bool l2_limit_saved = false;
+  size_t l2_prev_limit = 0;   // the persisting-L2 limit before this handle changed it
   std::vector<int32_t> anchor_of;
   std::vector<LayerDev> layers;
   std::vector<int32_t> bucket_shift, nbuckets;  // per layer: fetch-order buckets
@@ -2095,6 +2097,17 @@ void first_touch(void *p, size_t bytes) {
     th.emplace_back([=] { std::memset(static_cast<char *>(p) + b, 0, e - b); });
   }
   for (auto &t : th) t.join();
+}
+
+// Turn the handle's L2 window off: persisting lines back to normal and the
+// context's set-aside back to what it was before the handle changed it.
+int l2_persisting_off(hisparse_handle *h) {
+  h->l2_hit_ratio = 0.f;
+  if (!h->l2_limit_saved) return HISPARSE_OK;
+  HS_CUDA(cudaCtxResetPersistingL2Cache());
+  HS_CUDA(cudaDeviceSetLimit(cudaLimitPersistingL2CacheSize, h->l2_prev_limit));
+  h->l2_limit_saved = false;
+  return HISPARSE_OK;
 }
 
 }  // namespace
@@ -2351,7 +2364,7 @@ int hisparse_init(const hisparse_config *cfg, const hisparse_layer_buffers *laye
 
 int hisparse_destroy(hisparse_handle *h) {
   if (!h) return HISPARSE_EINVAL;
-  int rc = HISPARSE_OK;
+  int rc = l2_persisting_off(h);
   if (h->arena) {
     cudaError_t e = cudaDeviceSynchronize();
     if (e == cudaSuccess) e = cudaFree(h->arena);
@@ -2752,11 +2765,7 @@ int hisparse_export_plan(hisparse_handle *h, int32_t layer, int32_t *count, int3
 
 int hisparse_set_l2_persisting(hisparse_handle *h, int64_t bytes) {
   if (!h || bytes < 0) return HISPARSE_EINVAL;
-  if (bytes == 0) {
-    h->l2_hit_ratio = 0.f;
-    HS_CUDA(cudaCtxResetPersistingL2Cache());
-    return HISPARSE_OK;
-  }
+  if (bytes == 0) return l2_persisting_off(h);
   int max_persist = 0, max_window = 0;
   HS_CUDA(cudaDeviceGetAttribute(&max_persist, cudaDevAttrMaxPersistingL2CacheSize, h->device));
   HS_CUDA(cudaDeviceGetAttribute(&max_window, cudaDevAttrMaxAccessPolicyWindowSize, h->device));
@@ -2766,6 +2775,10 @@ int hisparse_set_l2_persisting(hisparse_handle *h, int64_t bytes) {
   for (int l = 0; l < h->L; ++l)
     if (h->anchor_of[l] == -1) tables += table;
   const int64_t aside = std::min<int64_t>(bytes, max_persist);
+  if (!h->l2_limit_saved) {
+    HS_CUDA(cudaDeviceGetLimit(&h->l2_prev_limit, cudaLimitPersistingL2CacheSize));
+    h->l2_limit_saved = true;
+  }
   HS_CUDA(cudaDeviceSetLimit(cudaLimitPersistingL2CacheSize, static_cast<size_t>(aside)));
   // the share of each window's lines marked persisting, so that all layers'
   // persisting lines fit the set-aside together

@@ -414,8 +414,10 @@ int hisparse_reset(hisparse_handle *h, int32_t layer, void *stream);
  * a limit of this CUDA context that ends with it) to min(bytes, the device
  * maximum), and every later page-table RESOLVE launch carries an
  * access-policy window over its layer's page table whose hit ratio lets the
- * tables of all RESOLVE layers share the set-aside.  bytes == 0 turns it off
- * and returns persisting lines to normal (cudaCtxResetPersistingL2Cache).
+ * tables of all RESOLVE layers share the set-aside.  bytes == 0 turns it off:
+ * persisting lines go back to normal (cudaCtxResetPersistingL2Cache) and the
+ * set-aside to what it was before this handle first changed it;
+ * hisparse_destroy does the same.
  * Results are unchanged either way.  Not during graph capture: launches
  * captured earlier keep the setting they were captured with.
  * Errors: EINVAL (bytes < 0), EBOUND (no persisting L2 on the device, or one

@@ -342,8 +342,8 @@ def cpu_oracle_rate_threads(w, traces, host_views, threads, union=False):
 TARGET_LINK_FRAC = 0.8   # the miss-fetch path's target share of the measured host link
 
 # The default line's other workloads (name -> how it is built and run).
-SUB_WORKLOADS = ("tiny", "quest", "short", "shared_inline", "shared_anchor", "sweep",
-                 "sweep_huge", "sweep_allhit")
+SUB_WORKLOADS = ("tiny", "quest", "short", "shared_inline", "shared_inline_huge",
+                 "shared_anchor", "sweep", "sweep_huge", "sweep_allhit")
 SWEEP_POINT = (4096, 0.87)           # (B, reuse fraction) of the capacity-sweep entry
 SWEEP_CONTEXTS = (1048576, 524288, 262144)
 HOST_MARGIN_GIB = 32                 # host memory left free beside a pinned pool
@@ -1143,9 +1143,12 @@ def sub_workload(args, name):
         return get("quest"), opts_for(args, replay="group", interleave=False, **base)
     if name == "short":
         return get("short"), opts_for(args, replay="group", interleave=False, **base)
-    if name in ("shared_inline", "shared_anchor"):
-        return get("shared"), opts_for(args, replay="inline" if name == "shared_inline"
-                                       else "group", interleave=True, **base)
+    if name in ("shared_inline", "shared_anchor", "shared_inline_huge"):
+        kw = dict(base)
+        if name == "shared_inline_huge":   # the same on a huge-page-backed pool
+            kw["pool"] = "huge"
+        return get("shared"), opts_for(args, replay="group" if name == "shared_anchor"
+                                       else "inline", interleave=True, **kw)
     if name in ("sweep", "sweep_huge", "sweep_allhit"):
         B, f = SWEEP_POINT
         L, why = pick_sweep_context(B, f)

@@ -92,3 +92,20 @@ def test_workload_sizes():
     assert abs(dsa.host_bytes() / 1e9 - 4.83) < 0.01
     assert WORKLOADS["shared"].anchor_of()[:5] == [-1, 0, 0, 0, -1]
     assert WORKLOADS["shared"].anchors() == [0, 4, 8, 12]
+
+
+def test_short_workload_fits_the_short_path():
+    """The short-request workload: every request's context fits the buffer
+    for the whole run (seq_len = L_ctx + t + 1 <= B), every selection is a
+    position below seq_len, and the newest position is selected (the local
+    window), so every step of every unit takes the short path."""
+    w = get("short")
+    assert w.admit_preload and w.write_through
+    assert w.L_ctx + w.steps <= w.B
+    for r in range(2):
+        sel, newest = unit_trace(w, 0, r)
+        for t in range(w.steps):
+            seq_len = w.L_ctx + t + 1
+            assert newest[t] == seq_len - 1
+            assert sel[t].min() >= 0 and sel[t].max() < seq_len
+            assert newest[t] in set(sel[t].tolist())

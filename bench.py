@@ -808,7 +808,8 @@ def measure(o, w, dev, h2d_gbs, dist=None, world=1, headline=False, rank=0, cloc
     #      pass. ----
     verify = None
     if o.verify and not o.resident and w.sel_block_tokens == 1 and o.verify_rows == 1:
-        verify = verify_against_oracle(w, hs, mem, groups, traces, T)
+        verify = verify_against_oracle(w, hs, mem, groups, traces, T,
+                                       check_bytes=not o.skip_io)
 
     total_ms = sum(step_ms)
     sel_per_step = G * w.R * w.k
@@ -1311,11 +1312,11 @@ def run_ours(args):
     return 0
 
 
-def verify_against_oracle(w, hs, mem, groups, traces, steps):
+def verify_against_oracle(w, hs, mem, groups, traces, steps, check_bytes=True):
     """Replay the same steps on the oracle and compare the final state: slot
-    maps, LRU orders, page tables and miss counts of every anchor, and the
-    bytes of a sample of occupied hot rows (of every layer) against records
-    generated afresh for their positions."""
+    maps, LRU orders, page tables and miss counts of every anchor, and (unless
+    the run skipped the copies) the bytes of a sample of occupied hot rows of
+    every layer against records generated afresh for their positions."""
     import numpy as np
     from oracle.coracle import OracleLayer
     from workload import records as REC
@@ -1346,7 +1347,7 @@ def verify_against_oracle(w, hs, mem, groups, traces, steps):
         # record of the position in slot s
         nbad = nchk = 0
         picks = []
-        for r in range(w.R):
+        for r in range(w.R if check_bytes else 0):
             occ = np.flatnonzero(sp[r] >= 0)
             if len(occ):
                 picks += [(r, int(s)) for s in rng.choice(occ, size=min(32, len(occ)),
